@@ -1,0 +1,113 @@
+"""Seeded synthetic inputs shared by the oracle-side tests and the CUDA path.
+
+This module draws random numbers and lays them out; it holds none of the
+attention arithmetic. It is the one module that both the oracle checks and
+the library's callers (tests, bench) use, so that both sides see identical
+bf16 bytes.
+
+Workloads (the shapes of the pages' GEM jagged attention, broadcast-Q and
+block-diagonal cases; user-sequence data is proprietary, so these stand in):
+
+===========  ====================================================  =====
+name         lengths                                               H, D
+===========  ====================================================  =====
+tiny         B=4, uniform integers in [1, 128]                     2, 64
+gem          B=1024, rint(exp(ln 256 + 0.8 z)) clipped to [1,2048]  4, 128
+stress       4 x 16384 plus 252 uniform in [1, 256], shuffled       4, 128
+bcast        Lq=256 dense Q; B=512 K/V lengths uniform [64, 1024]   4, 128
+blockdiag    B=1152, L=4096 (64 blocks of 64 tokens)               2, 128
+blockdiag64  same, D=64                                            2, 64
+===========  ====================================================  =====
+
+Lengths come from ``numpy.random.default_rng(seed)``; values are N(0, 1)
+drawn as fp32 by a seeded ``torch.Generator`` on the requested device and
+rounded to bf16 (round to nearest even) by torch.
+"""
+
+import math
+
+import numpy as np
+import torch
+
+SEEDS = {"tiny": 1, "gem": 2, "stress": 3, "bcast": 4, "blockdiag": 5, "blockdiag64": 5}
+
+
+def lengths_for(name, seed=None):
+    """Sequence lengths (numpy int64) of a named jagged workload."""
+    seed = SEEDS[name] if seed is None else seed
+    rng = np.random.default_rng(seed)
+    if name == "tiny":
+        return rng.integers(1, 129, 4).astype(np.int64)
+    if name == "gem":
+        z = rng.standard_normal(1024)
+        return np.clip(np.rint(np.exp(math.log(256.0) + 0.8 * z)), 1, 2048).astype(np.int64)
+    if name == "stress":
+        L = np.concatenate([np.full(4, 16384), rng.integers(1, 257, 252)]).astype(np.int64)
+        return L[rng.permutation(L.size)]
+    if name == "bcast":
+        return rng.integers(64, 1025, 512).astype(np.int64)
+    raise KeyError(name)
+
+
+def offsets_of(lengths, dtype=np.int64):
+    """Prefix sums [B+1] with offsets[0] = 0."""
+    off = np.zeros(len(lengths) + 1, dtype=np.int64)
+    off[1:] = np.cumsum(np.asarray(lengths, dtype=np.int64))
+    return off.astype(dtype)
+
+
+def randn_bf16(shape, seed, device="cpu"):
+    """N(0,1) fp32 from a seeded torch generator on `device`, rounded to bf16."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def jagged_inputs(lengths, H, D, seed, device="cpu", with_grad=True):
+    """Packed q, k, v (and dO) [T, H, D] bf16 for the given lengths."""
+    T = int(np.sum(lengths))
+    names = ("q", "k", "v", "do") if with_grad else ("q", "k", "v")
+    return {n: randn_bf16((T, H, D), seed * 1000 + i, device) for i, n in enumerate(names)}
+
+
+def bcast_inputs(lengths, Lq, H, D, seed, device="cpu", with_grad=True):
+    """q [Lq, H, D]; k, v [Tk, H, D]; dO [B, Lq, H, D] (bf16)."""
+    Tk = int(np.sum(lengths))
+    out = {
+        "q": randn_bf16((Lq, H, D), seed * 1000 + 0, device),
+        "k": randn_bf16((Tk, H, D), seed * 1000 + 1, device),
+        "v": randn_bf16((Tk, H, D), seed * 1000 + 2, device),
+    }
+    if with_grad:
+        out["do"] = randn_bf16((len(lengths), Lq, H, D), seed * 1000 + 3, device)
+    return out
+
+
+def blockdiag_inputs(B, L, H, D, seed, device="cpu", with_grad=True):
+    """q, k, v (and dO) [B, L, H, D] bf16."""
+    names = ("q", "k", "v", "do") if with_grad else ("q", "k", "v")
+    return {n: randn_bf16((B, L, H, D), seed * 1000 + i, device) for i, n in enumerate(names)}
+
+
+WORKLOADS = {
+    "tiny": dict(kind="jagged", H=2, D=64, offsets_dtype=np.int32),
+    "gem": dict(kind="jagged", H=4, D=128, offsets_dtype=np.int64),
+    "stress": dict(kind="jagged", H=4, D=128, offsets_dtype=np.int64),
+    "bcast": dict(kind="bcast", H=4, D=128, Lq=256, offsets_dtype=np.int64),
+    "blockdiag": dict(kind="blockdiag", B=1152, L=4096, H=2, D=128),
+    "blockdiag64": dict(kind="blockdiag", B=1152, L=4096, H=2, D=64),
+}
+
+
+def useful_flops(name_or_kind, lengths=None, H=None, D=None, Lq=None, B=None, L=None, block=64):
+    """Useful (unpadded) forward FLOPs: 4 * H * D * sum_b Lq_b * Lk_b.
+
+    The backward counts 2.5x this (five contractions against two).
+    """
+    if name_or_kind == "jagged":
+        return 4.0 * H * D * float(np.sum(np.asarray(lengths, dtype=np.float64) ** 2))
+    if name_or_kind == "bcast":
+        return 4.0 * H * D * Lq * float(np.sum(lengths))
+    if name_or_kind == "blockdiag":
+        return 4.0 * H * D * B * L * block
+    raise KeyError(name_or_kind)

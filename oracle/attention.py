@@ -1,0 +1,233 @@
+"""fp64 NumPy oracle for exact softmax attention over packed (jagged) sequences.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): the CUDA path never
+imports this module and this module imports nothing from the CUDA path.
+
+What is computed is the plain definition of softmax attention, written out
+per sequence and per head, with no blocking, fusion or online rescaling:
+
+* forward, for one sequence b and head h ([TLX-BA] section 2, the standard
+  FlashAttention loop, which reaches this result tile by tile; [JFA-GEM]
+  "Desarrollo de Jagged Flash Attention": FlashAttention run directly on the
+  packed Q, K, V with an offsets tensor and no padding):
+
+      S   = scale * Q K^T                      (Lq x Lk)
+      P   = row-softmax(S)
+      O   = P V
+      LSE = max_j S_ij + ln sum_j exp(S_ij - max_j S_ij)   (natural log)
+
+  [TLX-BA] section 2 stores L = m + log(l) for the backward pass; here it is
+  expressed in natural-log units of the scaled score.
+
+* backward, with the upstream gradient dO of the same shape as O
+  ([TLX-BA] sections 2 and 4: P rebuilt from S, Di = rowsum(dO * O)):
+
+      dV = P^T dO
+      dP = dO V^T
+      Di = sum_d dO_id O_id
+      dS = P * (dP - Di)
+      dQ = scale * dS K
+      dK = scale * dS^T Q
+
+* broadcast-Q ([JFA-GEM] "Optimización del proceso de Backward y dQ"): one
+  dense Q is shared by every jagged K/V sequence; O and LSE are per
+  sequence and dQ is the sum over sequences of each sequence's dQ.
+
+* block-diagonal ([TLX-BA] sections 1-2): the sequence is cut into fixed
+  64-token blocks and each query block attends only to its own key/value
+  block, i.e. the definition above applied to every block independently.
+
+Inputs are NumPy arrays. Callers pass the bf16 values already widened to
+float64 (exactly); all arithmetic here is float64. Query rows are processed
+in chunks only to bound memory: every row's softmax is still taken over all
+of its keys at once.
+
+Layouts (shared with the library's documented ABI, so tests can compare):
+packed tensors are [T, H, D] (token, head, dim); offsets is [B+1] with
+offsets[0] = 0, non-decreasing, offsets[B] = T; jagged LSE is [H, T];
+broadcast-Q O is [B, Lq, H, D] and its LSE is [B, H, Lq]; block-diagonal
+tensors are [B, L, H, D].
+"""
+
+import numpy as np
+
+ROW_CHUNK = 2048
+BLOCK = 64  # [TLX-BA] section 2: fixed 64-token blocks
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+def softmax_rows(S):
+    """Row softmax of a 2-D fp64 score matrix and its natural-log LSE.
+
+    Returns (P, lse). A row with no keys is not allowed here; callers
+    handle empty key sets before calling.
+    """
+    m = S.max(axis=1, keepdims=True)
+    e = np.exp(S - m)
+    l = e.sum(axis=1, keepdims=True)
+    return e / l, (m + np.log(l))[:, 0]
+
+
+def seq_fwd(Q, K, V, scale):
+    """Attention forward for one sequence and one head.
+
+    Q [Lq, D], K [Lk, D], V [Lk, Dv] (fp64). Returns O [Lq, Dv] and
+    LSE [Lq]. With Lk = 0 the output is 0 and the LSE is -inf (no keys:
+    the empty sum), the reading used for broadcast-Q sequences of length 0.
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    Lq, Lk = Q.shape[0], K.shape[0]
+    O = np.zeros((Lq, V.shape[1]))
+    lse = np.full(Lq, -np.inf)
+    if Lq == 0 or Lk == 0:
+        return O, lse
+    for r0 in range(0, Lq, ROW_CHUNK):
+        r1 = min(Lq, r0 + ROW_CHUNK)
+        S = scale * (Q[r0:r1] @ K.T)
+        P, lse[r0:r1] = softmax_rows(S)
+        O[r0:r1] = P @ V
+    return O, lse
+
+
+def seq_bwd(Q, K, V, dO, scale, O=None):
+    """Attention backward for one sequence and one head.
+
+    Q [Lq, D], K [Lk, D], V [Lk, D], dO [Lq, D] (fp64). O is the oracle's
+    own forward output (recomputed when not given). Returns dQ, dK, dV.
+    """
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    Lq, Lk = Q.shape[0], K.shape[0]
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    if Lq == 0 or Lk == 0:
+        return dQ, dK, dV
+    if O is None:
+        O, _ = seq_fwd(Q, K, V, scale)
+    for r0 in range(0, Lq, ROW_CHUNK):
+        r1 = min(Lq, r0 + ROW_CHUNK)
+        S = scale * (Q[r0:r1] @ K.T)
+        P, _ = softmax_rows(S)
+        dV += P.T @ dO[r0:r1]
+        dP = dO[r0:r1] @ V.T
+        Di = np.sum(dO[r0:r1] * O[r0:r1], axis=1, keepdims=True)
+        dS = P * (dP - Di)
+        dQ[r0:r1] = scale * (dS @ K)
+        dK += scale * (dS.T @ Q[r0:r1])
+    return dQ, dK, dV
+
+
+def _bounds(offsets):
+    off = np.asarray(offsets, dtype=np.int64)
+    return [(int(off[b]), int(off[b + 1])) for b in range(len(off) - 1)]
+
+
+def jagged_fwd(q, k, v, offsets, scale):
+    """Jagged self-attention forward over packed [T, H, D] tensors.
+
+    Returns O [T, H, D] and LSE [H, T] (fp64).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, H, _ = q.shape
+    o = np.zeros((T, H, v.shape[2]))
+    lse = np.full((H, T), -np.inf)
+    for s, e in _bounds(offsets):
+        for h in range(H):
+            o[s:e, h], lse[h, s:e] = seq_fwd(q[s:e, h], k[s:e, h], v[s:e, h], scale)
+    return o, lse
+
+
+def jagged_bwd(q, k, v, do, offsets, scale):
+    """Jagged self-attention backward. Returns dQ, dK, dV [T, H, D] (fp64)."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    H = q.shape[1]
+    for s, e in _bounds(offsets):
+        for h in range(H):
+            dq[s:e, h], dk[s:e, h], dv[s:e, h] = seq_bwd(
+                q[s:e, h], k[s:e, h], v[s:e, h], do[s:e, h], scale)
+    return dq, dk, dv
+
+
+def bcastq_fwd(q, k, v, kv_offsets, scale):
+    """Broadcast-Q forward: q [Lq, H, D] shared by every sequence of the
+    packed k, v [Tk, H, D]. Returns O [B, Lq, H, D], LSE [B, H, Lq]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Lq, H, _ = q.shape
+    bounds = _bounds(kv_offsets)
+    o = np.zeros((len(bounds), Lq, H, v.shape[2]))
+    lse = np.full((len(bounds), H, Lq), -np.inf)
+    for b, (s, e) in enumerate(bounds):
+        for h in range(H):
+            o[b, :, h], lse[b, h] = seq_fwd(q[:, h], k[s:e, h], v[s:e, h], scale)
+    return o, lse
+
+
+def bcastq_bwd(q, k, v, do, kv_offsets, scale):
+    """Broadcast-Q backward: do [B, Lq, H, D]. Returns dQ [Lq, H, D] summed
+    over the B sequences, and dK, dV [Tk, H, D]."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    H = q.shape[1]
+    dq = np.zeros_like(q)
+    dk, dv = np.zeros_like(k), np.zeros_like(v)
+    for b, (s, e) in enumerate(_bounds(kv_offsets)):
+        for h in range(H):
+            dq_b, dk[s:e, h], dv[s:e, h] = seq_bwd(
+                q[:, h], k[s:e, h], v[s:e, h], do[b, :, h], scale)
+            dq[:, h] += dq_b
+    return dq, dk, dv
+
+
+def _blocks(x, block):
+    """View [B, L, H, D] as [B*L/block, block, H, D]."""
+    B, L, H, D = x.shape
+    return x.reshape(B * (L // block), block, H, D)
+
+
+def blockdiag_fwd(q, k, v, scale, block=BLOCK):
+    """Block-diagonal attention forward on [B, L, H, D]; L % block == 0.
+
+    Each block of `block` tokens attends only within itself. Returns O
+    [B, L, H, D] (no LSE: [TLX-BA] section 2, none is stored)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, L, H, D = q.shape
+    assert L % block == 0
+    qb, kb, vb = _blocks(q, block), _blocks(k, block), _blocks(v, block)
+    o = np.zeros_like(qb)
+    for h in range(H):
+        S = scale * np.einsum("nid,njd->nij", qb[:, :, h], kb[:, :, h])
+        m = S.max(axis=2, keepdims=True)
+        e = np.exp(S - m)
+        P = e / e.sum(axis=2, keepdims=True)
+        o[:, :, h] = np.einsum("nij,njd->nid", P, vb[:, :, h])
+    return o.reshape(B, L, H, v.shape[3])
+
+
+def blockdiag_bwd(q, k, v, do, scale, block=BLOCK):
+    """Block-diagonal attention backward on [B, L, H, D].
+
+    Same formulas as :func:`seq_bwd`, per block, with Di = rowsum(dO * O)
+    taken from the oracle's own fp64 O. Returns dQ, dK, dV [B, L, H, D]."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, L, H, D = q.shape
+    assert L % block == 0
+    qb, kb, vb, dob = (_blocks(x, block) for x in (q, k, v, do))
+    dq, dk, dv = np.zeros_like(qb), np.zeros_like(kb), np.zeros_like(vb)
+    for h in range(H):
+        Q, K, V, dO = qb[:, :, h], kb[:, :, h], vb[:, :, h], dob[:, :, h]
+        S = scale * np.einsum("nid,njd->nij", Q, K)
+        m = S.max(axis=2, keepdims=True)
+        e = np.exp(S - m)
+        P = e / e.sum(axis=2, keepdims=True)
+        O = np.einsum("nij,njd->nid", P, V)
+        dv[:, :, h] = np.einsum("nij,nid->njd", P, dO)
+        dP = np.einsum("nid,njd->nij", dO, V)
+        Di = np.sum(dO * O, axis=2, keepdims=True)
+        dS = P * (dP - Di)
+        dq[:, :, h] = scale * np.einsum("nij,njd->nid", dS, K)
+        dk[:, :, h] = scale * np.einsum("nij,nid->njd", dS, Q)
+    shape = (B, L, H, D)
+    return dq.reshape(shape), dk.reshape(shape), dv.reshape(shape)
