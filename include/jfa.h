@@ -1,0 +1,212 @@
+/*
+ * jfa.h -- C ABI of libjfa: Jagged Flash Attention for GB300 (sm_103a).
+ *
+ * Exact softmax attention, forward and backward, over packed bf16 Q/K/V
+ * whose sequence boundaries are given by an offsets tensor, so that no
+ * padding token is ever materialised ("Desarrollo de Jagged Flash Attention
+ * para el modelo GEM", first section: FlashAttention applied directly to the
+ * packed Q, K, V plus an offsets tensor). Two special cases are provided:
+ * broadcast-Q (one dense Q shared by every jagged K/V sequence, dQ summed
+ * over the batch; same article, "Optimización del proceso de Backward y dQ")
+ * and fixed 64-token block-diagonal attention ("TLX Block Attention",
+ * sections 1-2).
+ *
+ * Common conventions
+ * ------------------
+ * - Every pointer is owned by the caller. The library allocates and frees
+ *   no memory. Device buffers must be device-resident (cudaMalloc, or a
+ *   framework allocator) and 16-byte aligned; host buffers are plain host
+ *   memory.
+ * - Packed tensors are bf16, contiguous, laid out [T, H, D] (token, head,
+ *   dim). D must be 64 or 128. H >= 1. T < 2^31.
+ * - offsets: device array of B+1 integers (int32 or int64, chosen by
+ *   jfa_index_t), offsets[0] = 0, non-decreasing, offsets[B] = T. The
+ *   kernels read it on the device; the scheduler reads a host copy.
+ * - scale: the softmax scale applied to Q K^T (normally 1/sqrt(D)).
+ * - LSE (log-sum-exp of the scaled scores, natural log) is fp32.
+ * - All calls that take a stream are asynchronous on that stream. Argument
+ *   errors are detected on the host and returned before anything is
+ *   launched. Launch failures return JFA_ERR_CUDA. A kernel whose bounded
+ *   waits expire writes a code into the status word at the start of its
+ *   workspace and exits; jfa_check_status() synchronises the stream and
+ *   reports it as JFA_ERR_TIMEOUT.
+ * - A more detailed message for the last error of the calling thread is
+ *   available from jfa_last_error().
+ * - Work tiles: the forward kernels take tiles of 256 query rows (two
+ *   128-row halves sharing K/V), the backward kernels tiles of 128 key rows.
+ *   The tile lists come from jfa_sched_build() with the tile_rows reported
+ *   by jfa_tile_rows().
+ */
+#ifndef JFA_H_
+#define JFA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *jfa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  JFA_OK = 0,
+  JFA_ERR_INVALID_ARG = 1, /* bad pointer, size, layout or offsets */
+  JFA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. D not in {64,128}) */
+  JFA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than jfa_workspace_size() */
+  JFA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  JFA_ERR_TIMEOUT = 5      /* a kernel's bounded wait expired (see jfa_check_status) */
+} jfa_status;
+
+typedef enum { JFA_I32 = 0, JFA_I64 = 1 } jfa_index_t;
+
+typedef enum {
+  JFA_OP_FWD = 0,
+  JFA_OP_BWD = 1,
+  JFA_OP_BCASTQ_FWD = 2,
+  JFA_OP_BCASTQ_BWD = 3,
+  JFA_OP_BLOCKDIAG_FWD = 4,
+  JFA_OP_BLOCKDIAG_BWD = 5
+} jfa_op;
+
+/* Human-readable name of a status code (static string). */
+const char *jfa_status_str(jfa_status s);
+
+/* Detail message of the last non-OK status returned on this thread
+ * (static thread-local buffer; empty string when none). */
+const char *jfa_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * Host tile scheduler.
+ *
+ * "Desarrollo de Jagged Flash Attention para el modelo GEM", section
+ * "Optimizaciones específicas para el flujo de trabajo de GEM": tiles are
+ * sorted on the host by their K/V workload, largest first, and dealt to the
+ * SMs in a zigzag (boustrophedon) order: even passes fill SMs left to
+ * right, odd passes right to left.
+ *
+ * A tile is (b, h, m): sequence b, head h, row block m of tile_rows rows.
+ * Sequence b has ceil(rows_b / tile_rows) row blocks, with rows_b =
+ * fixed_rows if fixed_rows > 0, else its length offsets[b+1]-offsets[b].
+ * Its work is fixed_work if fixed_work > 0, else its length. The sort is
+ * stable (ties keep the order b, h, m). Sorted position i goes to pass
+ * p = i / num_sms and SM (i % num_sms) on even p, num_sms-1-(i % num_sms)
+ * on odd p. With zigzag = 0 the unsorted tiles are dealt round-robin
+ * (SM i % num_sms), the naive order kept for comparison.
+ *
+ * Output is CSR: sm_ptr[num_sms+1] (sm_ptr[0] = 0) and tiles[3*n_tiles]
+ * holding (b, h, m) int32 triples, each SM's tiles in dealt order. Both
+ * are host buffers owned by the caller.
+ * ---------------------------------------------------------------------- */
+
+/* Number of tiles jfa_sched_build() will emit. host_offsets: host array of
+ * B+1 entries. Returns JFA_ERR_INVALID_ARG for bad offsets or sizes. */
+jfa_status jfa_sched_size(int64_t B, int H, int tile_rows, const void *host_offsets,
+                          jfa_index_t idx, int64_t fixed_rows, int64_t *n_tiles);
+
+jfa_status jfa_sched_build(int64_t B, int H, int tile_rows, int num_sms,
+                           const void *host_offsets, jfa_index_t idx, int64_t fixed_rows,
+                           int64_t fixed_work, int zigzag, int32_t *sm_ptr, int32_t *tiles);
+
+/* Rows per tile that the kernels of `op` expect from the scheduler. */
+jfa_status jfa_tile_rows(jfa_op op, int D, int *tile_rows);
+
+/* Number of SMs of the current device (the persistent grid size). */
+jfa_status jfa_num_sms(int *num_sms);
+
+/* ------------------------------------------------------------------------
+ * Workspace.
+ *
+ * Every kernel call takes a device workspace that starts with a 256-byte
+ * status block. The backward calls also keep an fp32 dQ accumulator there
+ * ([H, T, D] for jfa_bwd, [H, Lq, D] for jfa_bcastq_bwd), which the call
+ * clears itself. `n` is T for JFA_OP_FWD / JFA_OP_BWD, Lq for the
+ * broadcast-Q ops and is ignored for the block-diagonal ops.
+ * ---------------------------------------------------------------------- */
+size_t jfa_workspace_size(jfa_op op, int64_t n, int H, int D);
+
+/* Clears the status block (asynchronous on `stream`). */
+jfa_status jfa_workspace_init(void *workspace, size_t ws_bytes, jfa_stream_t stream);
+
+/* Synchronises `stream`, reads the status block: JFA_OK, or
+ * JFA_ERR_TIMEOUT if a kernel gave up waiting (the block is then cleared so
+ * the workspace can be reused). */
+jfa_status jfa_check_status(void *workspace, jfa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Jagged forward: for each sequence b and head h,
+ *   O = softmax(scale * Q K^T) V,  LSE_i = ln sum_j exp(scale * q_i . k_j)
+ * ("TLX Block Attention", section 2: the standard FlashAttention loop with
+ * running max, correction factor and final normalisation, storing
+ * L = m + log(l) for the backward pass).
+ *
+ * q, k, v: device bf16 [T, H, D]. offsets: device [B+1]. d_sm_ptr,
+ * d_tiles: device copies of jfa_sched_build() output for
+ * tile_rows = jfa_tile_rows(JFA_OP_FWD). num_sms: length of d_sm_ptr - 1
+ * (the grid size). o: device bf16 [T, H, D]. lse: device fp32 [H, T].
+ * ---------------------------------------------------------------------- */
+jfa_status jfa_fwd(const void *q, const void *k, const void *v, const void *offsets,
+                   jfa_index_t idx, int64_t B, int64_t T, int H, int D, float scale,
+                   const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_sms, void *o,
+                   float *lse, void *workspace, size_t ws_bytes, jfa_stream_t stream);
+
+/* Jagged backward: given dO (device bf16 [T, H, D]) and the forward's O and
+ * LSE, writes dQ, dK, dV (device bf16 [T, H, D]):
+ *   P = exp(scale * Q K^T - LSE), dV = P^T dO, dP = dO V^T,
+ *   Di = rowsum(dO * O) (computed inside the kernel, no separate pass),
+ *   dS = P * (dP - Di), dQ = scale * dS K, dK = scale * dS^T Q
+ * ("TLX Block Attention", sections 2 and 4; "Desarrollo de Jagged Flash
+ * Attention ...", "Cambios estructurales ...": a warp dedicated to the dQ
+ * reduction). Tiles: jfa_sched_build() with tile_rows =
+ * jfa_tile_rows(JFA_OP_BWD) over key blocks. workspace >=
+ * jfa_workspace_size(JFA_OP_BWD, T, H, D). */
+jfa_status jfa_bwd(const void *q, const void *k, const void *v, const void *o,
+                   const float *lse, const void *dout, const void *offsets, jfa_index_t idx,
+                   int64_t B, int64_t T, int H, int D, float scale, const int32_t *d_sm_ptr,
+                   const int32_t *d_tiles, int num_sms, void *dq, void *dk, void *dv,
+                   void *workspace, size_t ws_bytes, jfa_stream_t stream);
+
+/* Broadcast-Q forward: q device bf16 [Lq, H, D] is shared by every
+ * sequence of k, v (device bf16 [Tk, H, D], boundaries kv_offsets [B+1]).
+ * o: device bf16 [B, Lq, H, D]; lse: device fp32 [B, H, Lq]. A sequence of
+ * length 0 gets O = 0 and LSE = -inf. Tiles: jfa_sched_build() with
+ * tile_rows = jfa_tile_rows(JFA_OP_BCASTQ_FWD), fixed_rows = Lq. */
+jfa_status jfa_bcastq_fwd(const void *q, const void *k, const void *v, const void *kv_offsets,
+                          jfa_index_t idx, int64_t B, int64_t Lq, int64_t Tk, int H, int D,
+                          float scale, const int32_t *d_sm_ptr, const int32_t *d_tiles,
+                          int num_sms, void *o, float *lse, void *workspace, size_t ws_bytes,
+                          jfa_stream_t stream);
+
+/* Broadcast-Q backward: dout device bf16 [B, Lq, H, D]; writes
+ * dq = sum over b of each sequence's dQ (device bf16 [Lq, H, D]) and dk,
+ * dv (device bf16 [Tk, H, D]). The per-sequence dQ partials are summed in
+ * fp32 through a double-buffered shared-memory staging area ("Optimización
+ * del proceso de Backward y dQ"). Tiles: tile_rows =
+ * jfa_tile_rows(JFA_OP_BCASTQ_BWD) over key blocks, fixed_work = Lq. */
+jfa_status jfa_bcastq_bwd(const void *q, const void *k, const void *v, const void *o,
+                          const float *lse, const void *dout, const void *kv_offsets,
+                          jfa_index_t idx, int64_t B, int64_t Lq, int64_t Tk, int H, int D,
+                          float scale, const int32_t *d_sm_ptr, const int32_t *d_tiles,
+                          int num_sms, void *dq, void *dk, void *dv, void *workspace,
+                          size_t ws_bytes, jfa_stream_t stream);
+
+/* Block-diagonal forward ("TLX Block Attention", sections 1-2): q, k, v
+ * device bf16 [B, L, H, D], L a multiple of 64; each 64-token block attends
+ * only within itself. One score tile per block, no online correction and
+ * no LSE. o: device bf16 [B, L, H, D]. */
+jfa_status blockdiag_fwd(const void *q, const void *k, const void *v, int64_t B, int64_t L,
+                         int H, int D, float scale, void *o, void *workspace, size_t ws_bytes,
+                         jfa_stream_t stream);
+
+/* Block-diagonal backward ("TLX Block Attention", section 4): recomputes
+ * S and P from Q and K (no LSE, no O), Di = rowsum(P * dP) (equal to
+ * rowsum(dO * O) since O = P V), then dQ, dK, dV (device bf16 [B, L, H, D]). */
+jfa_status blockdiag_bwd(const void *q, const void *k, const void *v, const void *dout,
+                         int64_t B, int64_t L, int H, int D, float scale, void *dq, void *dk,
+                         void *dv, void *workspace, size_t ws_bytes, jfa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JFA_H_ */

@@ -1,0 +1,282 @@
+"""Jagged Flash Attention for GB300 (sm_103a): thin Python binding of libjfa.
+
+Every step of the attention runs in libjfa's CUDA kernels behind the C ABI
+declared in ``include/jfa.h``; this module only marshals arguments: it
+allocates outputs and workspaces with torch, calls the host scheduler,
+copies its tile lists to the device and passes raw pointers and the current
+CUDA stream. There is no fallback: if ``libjfa.so`` is missing or the
+tensors are not CUDA tensors, the calls raise.
+
+Functions mirror the C entry points:
+
+* :func:`jfa_fwd`, :func:`jfa_bwd` -- jagged self-attention over packed
+  ``[T, H, D]`` bf16 tensors and an offsets tensor ``[B+1]``;
+* :func:`jfa_bcastq_fwd`, :func:`jfa_bcastq_bwd` -- one dense Q
+  ``[Lq, H, D]`` shared by every jagged K/V sequence;
+* :func:`blockdiag_fwd`, :func:`blockdiag_bwd` -- 64-token block-diagonal
+  attention on ``[B, L, H, D]``;
+* :func:`schedule` -- the host LPT + zigzag tile scheduler.
+"""
+
+import ctypes
+import math
+import os
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libjfa.so")
+
+JFA_I32, JFA_I64 = 0, 1
+OP_FWD, OP_BWD, OP_BCASTQ_FWD, OP_BCASTQ_BWD, OP_BLOCKDIAG_FWD, OP_BLOCKDIAG_BWD = range(6)
+
+_STATUS = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED",
+           3: "JFA_ERR_WORKSPACE", 4: "JFA_ERR_CUDA", 5: "JFA_ERR_TIMEOUT"}
+
+EXPORTS = [
+    "jfa_status_str", "jfa_last_error", "jfa_sched_size", "jfa_sched_build", "jfa_tile_rows",
+    "jfa_num_sms", "jfa_workspace_size", "jfa_workspace_init", "jfa_check_status", "jfa_fwd",
+    "jfa_bwd", "jfa_bcastq_fwd", "jfa_bcastq_bwd", "blockdiag_fwd", "blockdiag_bwd",
+]
+
+
+class JFAError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("%s: %s" % (_STATUS.get(code, code), msg))
+        self.code = code
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libjfa (ctypes), with argument types set. Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libjfa.so is not built (run __graft_entry__.build() or "
+                           "python -m jagged_flash_attention_flashattention_gb300.build)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "jfa_status_str": ([I], ctypes.c_char_p),
+        "jfa_last_error": ([], ctypes.c_char_p),
+        "jfa_sched_size": ([I64, I, I, P, I, I64, P], I),
+        "jfa_sched_build": ([I64, I, I, I, P, I, I64, I64, I, P, P], I),
+        "jfa_tile_rows": ([I, I, P], I),
+        "jfa_num_sms": ([P], I),
+        "jfa_workspace_size": ([I, I64, I, I], SZ),
+        "jfa_workspace_init": ([P, SZ, P], I),
+        "jfa_check_status": ([P, P], I),
+        "jfa_fwd": ([P, P, P, P, I, I64, I64, I, I, F, P, P, I, P, P, P, SZ, P], I),
+        "jfa_bwd": ([P, P, P, P, P, P, P, I, I64, I64, I, I, F, P, P, I, P, P, P, P, SZ, P], I),
+        "jfa_bcastq_fwd": ([P, P, P, P, I, I64, I64, I64, I, I, F, P, P, I, P, P, P, SZ, P], I),
+        "jfa_bcastq_bwd": ([P, P, P, P, P, P, P, I, I64, I64, I64, I, I, F, P, P, I, P, P, P, P,
+                            SZ, P], I),
+        "blockdiag_fwd": ([P, P, P, I64, I64, I, I, F, P, P, SZ, P], I),
+        "blockdiag_bwd": ([P, P, P, P, I64, I64, I, I, F, P, P, P, P, SZ, P], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _check(code):
+    if code != 0:
+        raise JFAError(code, lib().jfa_last_error().decode())
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+        if t.dtype != torch.bfloat16:
+            raise ValueError("tensors must be bf16")
+
+
+def num_sms():
+    n = ctypes.c_int(0)
+    _check(lib().jfa_num_sms(ctypes.byref(n)))
+    return n.value
+
+
+def tile_rows(op, D):
+    n = ctypes.c_int(0)
+    _check(lib().jfa_tile_rows(op, D, ctypes.byref(n)))
+    return n.value
+
+
+def schedule(offsets_host, H, tile_rows_, n_sms, fixed_rows=0, fixed_work=0, zigzag=True):
+    """Host LPT + zigzag schedule. Returns (sm_ptr [n_sms+1], tiles [n, 3]) int32 numpy."""
+    off = np.ascontiguousarray(offsets_host)
+    idx = JFA_I64 if off.dtype == np.int64 else JFA_I32
+    if off.dtype not in (np.int32, np.int64):
+        raise ValueError("offsets must be int32 or int64")
+    B = off.size - 1
+    n = ctypes.c_int64(0)
+    L = lib()
+    _check(L.jfa_sched_size(B, H, tile_rows_, off.ctypes.data, idx, fixed_rows, ctypes.byref(n)))
+    sm_ptr = np.zeros(n_sms + 1, dtype=np.int32)
+    tiles = np.zeros((max(n.value, 1), 3), dtype=np.int32)
+    _check(L.jfa_sched_build(B, H, tile_rows_, n_sms, off.ctypes.data, idx, fixed_rows,
+                             fixed_work, 1 if zigzag else 0, sm_ptr.ctypes.data,
+                             tiles.ctypes.data))
+    return sm_ptr, tiles[: n.value]
+
+
+class Plan:
+    """Schedules (on the device) and workspace for one batch layout.
+
+    kind: "jagged" (offsets of the packed Q/K/V) or "bcast" (offsets of the
+    packed K/V, dense Q of length Lq). The host offsets are read once here;
+    the device offsets tensor is what the kernels read.
+    """
+
+    def __init__(self, offsets, H, D, kind="jagged", Lq=0, zigzag=True, device=None):
+        if not offsets.is_cuda:
+            raise ValueError("offsets must be a CUDA tensor")
+        self.offsets = offsets
+        self.idx = JFA_I64 if offsets.dtype == torch.int64 else JFA_I32
+        host = offsets.cpu().numpy()
+        self.host_offsets = host
+        self.B = host.size - 1
+        self.T = int(host[-1])
+        self.H, self.D, self.kind, self.Lq = H, D, kind, int(Lq)
+        self.n_sms = num_sms()
+        dev = offsets.device
+        if kind == "jagged":
+            fwd = schedule(host, H, tile_rows(OP_FWD, D), self.n_sms, zigzag=zigzag)
+            bwd = schedule(host, H, tile_rows(OP_BWD, D), self.n_sms, zigzag=zigzag)
+        else:
+            fwd = schedule(host, H, tile_rows(OP_BCASTQ_FWD, D), self.n_sms, fixed_rows=self.Lq,
+                           zigzag=zigzag)
+            bwd = schedule(host, H, tile_rows(OP_BCASTQ_BWD, D), self.n_sms, fixed_work=self.Lq,
+                           zigzag=zigzag)
+        self.fwd_sched = tuple(torch.from_numpy(a.copy()).to(dev) for a in fwd)
+        self.bwd_sched = tuple(torch.from_numpy(a.copy()).to(dev) for a in bwd)
+        self.n_fwd_tiles, self.n_bwd_tiles = fwd[1].shape[0], bwd[1].shape[0]
+        rows = self.T if kind == "jagged" else self.Lq
+        op = OP_BWD if kind == "jagged" else OP_BCASTQ_BWD
+        nbytes = lib().jfa_workspace_size(op, rows, H, D)
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+
+    def check(self):
+        """Synchronises and raises if a kernel reported a timeout."""
+        _check(lib().jfa_check_status(_ptr(self.workspace), _stream()))
+
+
+def _scale(scale, D):
+    return 1.0 / math.sqrt(D) if scale is None else float(scale)
+
+
+def jfa_fwd(q, k, v, offsets, scale=None, plan=None):
+    """Jagged forward. q, k, v: [T, H, D] bf16 CUDA; offsets [B+1] int32/int64 CUDA.
+    Returns (o [T, H, D] bf16, lse [H, T] fp32)."""
+    _need_cuda(q, k, v)
+    T, H, D = q.shape
+    plan = plan or Plan(offsets, H, D)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    sp, tl = plan.fwd_sched
+    _check(lib().jfa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), plan.idx, plan.B, T, H, D,
+                         _scale(scale, D), _ptr(sp), _ptr(tl), plan.n_sms, _ptr(o), _ptr(lse),
+                         _ptr(plan.workspace), plan.workspace.numel(), _stream()))
+    return o, lse
+
+
+def jfa_bwd(q, k, v, o, lse, do, offsets, scale=None, plan=None):
+    """Jagged backward. Returns (dq, dk, dv), each [T, H, D] bf16."""
+    _need_cuda(q, k, v, o, do)
+    T, H, D = q.shape
+    plan = plan or Plan(offsets, H, D)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    sp, tl = plan.bwd_sched
+    _check(lib().jfa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(offsets),
+                         plan.idx, plan.B, T, H, D, _scale(scale, D), _ptr(sp), _ptr(tl),
+                         plan.n_sms, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(plan.workspace),
+                         plan.workspace.numel(), _stream()))
+    return dq, dk, dv
+
+
+def jfa_bcastq_fwd(q, k, v, kv_offsets, scale=None, plan=None):
+    """Broadcast-Q forward. q [Lq, H, D]; k, v [Tk, H, D]; kv_offsets [B+1].
+    Returns (o [B, Lq, H, D], lse [B, H, Lq])."""
+    _need_cuda(q, k, v)
+    Lq, H, D = q.shape
+    plan = plan or Plan(kv_offsets, H, D, kind="bcast", Lq=Lq)
+    Tk, B = k.shape[0], plan.B
+    o = torch.empty((B, Lq, H, D), dtype=q.dtype, device=q.device)
+    lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    sp, tl = plan.fwd_sched
+    _check(lib().jfa_bcastq_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_offsets), plan.idx, B, Lq, Tk,
+                                H, D, _scale(scale, D), _ptr(sp), _ptr(tl), plan.n_sms, _ptr(o),
+                                _ptr(lse), _ptr(plan.workspace), plan.workspace.numel(),
+                                _stream()))
+    return o, lse
+
+
+def jfa_bcastq_bwd(q, k, v, o, lse, do, kv_offsets, scale=None, plan=None):
+    """Broadcast-Q backward. Returns (dq [Lq, H, D] summed over sequences, dk, dv [Tk, H, D])."""
+    _need_cuda(q, k, v, o, do)
+    Lq, H, D = q.shape
+    plan = plan or Plan(kv_offsets, H, D, kind="bcast", Lq=Lq)
+    Tk, B = k.shape[0], plan.B
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    sp, tl = plan.bwd_sched
+    _check(lib().jfa_bcastq_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                _ptr(kv_offsets), plan.idx, B, Lq, Tk, H, D, _scale(scale, D),
+                                _ptr(sp), _ptr(tl), plan.n_sms, _ptr(dq), _ptr(dk), _ptr(dv),
+                                _ptr(plan.workspace), plan.workspace.numel(), _stream()))
+    return dq, dk, dv
+
+
+_ws_cache = {}
+
+
+def _small_workspace(device):
+    key = str(device)
+    if key not in _ws_cache:
+        _ws_cache[key] = torch.zeros(lib().jfa_workspace_size(OP_BLOCKDIAG_FWD, 0, 1, 64),
+                                     dtype=torch.uint8, device=device)
+    return _ws_cache[key]
+
+
+def blockdiag_fwd(q, k, v, scale=None):
+    """64-token block-diagonal forward on [B, L, H, D] bf16. Returns o."""
+    _need_cuda(q, k, v)
+    B, L, H, D = q.shape
+    o = torch.empty_like(q)
+    ws = _small_workspace(q.device)
+    _check(lib().blockdiag_fwd(_ptr(q), _ptr(k), _ptr(v), B, L, H, D, _scale(scale, D), _ptr(o),
+                               _ptr(ws), ws.numel(), _stream()))
+    return o
+
+
+def blockdiag_bwd(q, k, v, do, scale=None):
+    """64-token block-diagonal backward. Returns (dq, dk, dv)."""
+    _need_cuda(q, k, v, do)
+    B, L, H, D = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = _small_workspace(q.device)
+    _check(lib().blockdiag_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, L, H, D, _scale(scale, D),
+                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream()))
+    return dq, dk, dv
+
+
+def check_status(workspace=None, device=None):
+    """Synchronises the current stream and raises JFAError if a kernel gave up waiting."""
+    ws = workspace if workspace is not None else _small_workspace(device or torch.device("cuda"))
+    _check(lib().jfa_check_status(_ptr(ws), _stream()))

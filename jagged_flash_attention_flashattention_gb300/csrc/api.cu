@@ -1,0 +1,398 @@
+// api.cu -- the extern "C" entry points of libjfa (declared in include/jfa.h):
+// argument checks, TMA descriptor encoding and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "host_common.h"
+#include "jfa.h"
+#include "kernels.h"
+
+using namespace jfa;
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+constexpr uint64_t kTimeoutNs = 4ull * 1000 * 1000 * 1000;  // bounded waits give up after 4 s
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 [rows, H, D] as a 3-D tensor {D, H, rows}; box {64, 1, box_rows}, 128-byte swizzle.
+jfa_status map_rows_bf16(CUtensorMap *m, const void *base, int64_t rows, int H, int D,
+                         int box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return fail(JFA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  if (rows < 1) rows = 1;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(JFA_ERR_CUDA, "tensor map encode failed (%d)", (int)r);
+  return JFA_OK;
+}
+
+// fp32 [H, rows, D] as {D, rows, H}; box {32, 32, 1}, no swizzle.
+jfa_status map_acc_f32(CUtensorMap *m, void *base, int64_t rows, int H, int D) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return fail(JFA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  if (rows < 1) rows = 1;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)rows * D * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(JFA_ERR_CUDA, "tensor map encode failed (%d)", (int)r);
+  return JFA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+jfa_status need_ptr(const void *p, const char *name) {
+  if (!p) return fail(JFA_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(JFA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return JFA_OK;
+}
+
+#define JFA_TRY(x)                    \
+  do {                                \
+    jfa_status _s = (x);              \
+    if (_s != JFA_OK) return _s;      \
+  } while (0)
+
+jfa_status check_dims(int64_t B, int64_t T, int H, int D) {
+  if (D != 64 && D != 128) return fail(JFA_ERR_UNSUPPORTED, "D = %d (supported: 64, 128)", D);
+  if (H < 1) return fail(JFA_ERR_INVALID_ARG, "H = %d < 1", H);
+  if (B < 0 || T < 0) return fail(JFA_ERR_INVALID_ARG, "negative size");
+  if (T >= (int64_t(1) << 31) - 256) return fail(JFA_ERR_INVALID_ARG, "T too large");
+  return JFA_OK;
+}
+
+jfa_status check_ws(void *ws, size_t ws_bytes, size_t need) {
+  if (!ws) return fail(JFA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned16(ws)) return fail(JFA_ERR_WORKSPACE, "workspace not 16-byte aligned");
+  if (ws_bytes < need)
+    return fail(JFA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, need);
+  return JFA_OK;
+}
+
+jfa_status check_sched(const int32_t *sm_ptr, const int32_t *tiles, int num_sms) {
+  if (num_sms < 1) return fail(JFA_ERR_INVALID_ARG, "num_sms = %d < 1", num_sms);
+  if (!sm_ptr) return fail(JFA_ERR_INVALID_ARG, "sm_ptr is NULL");
+  if (!tiles) return fail(JFA_ERR_INVALID_ARG, "tiles is NULL");
+  return JFA_OK;
+}
+
+jfa_status cuda_status(cudaError_t e, const char *what) {
+  if (e != cudaSuccess) return fail(JFA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return JFA_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+// ------------------------------------------------------------------ misc
+
+extern "C" jfa_status jfa_tile_rows(jfa_op op, int D, int *tile_rows) {
+  if (!tile_rows) return fail(JFA_ERR_INVALID_ARG, "tile_rows is NULL");
+  if (D != 64 && D != 128) return fail(JFA_ERR_UNSUPPORTED, "D = %d", D);
+  switch (op) {
+    case JFA_OP_FWD:
+    case JFA_OP_BCASTQ_FWD: *tile_rows = 256; return JFA_OK;
+    case JFA_OP_BWD:
+    case JFA_OP_BCASTQ_BWD: *tile_rows = 128; return JFA_OK;
+    case JFA_OP_BLOCKDIAG_FWD:
+    case JFA_OP_BLOCKDIAG_BWD: *tile_rows = 128; return JFA_OK;
+  }
+  return fail(JFA_ERR_INVALID_ARG, "unknown op %d", (int)op);
+}
+
+extern "C" jfa_status jfa_num_sms(int *num_sms) {
+  if (!num_sms) return fail(JFA_ERR_INVALID_ARG, "num_sms is NULL");
+  int dev = 0;
+  JFA_TRY(cuda_status(cudaGetDevice(&dev), "cudaGetDevice"));
+  JFA_TRY(cuda_status(cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev),
+                      "cudaDeviceGetAttribute"));
+  return JFA_OK;
+}
+
+extern "C" size_t jfa_workspace_size(jfa_op op, int64_t n, int H, int D) {
+  if (n < 0 || H < 1 || D < 1) return kStatusBytes;
+  switch (op) {
+    case JFA_OP_BWD:
+    case JFA_OP_BCASTQ_BWD:
+      return kStatusBytes + round_up((size_t)n * H * D * sizeof(float), 256);
+    default: return kStatusBytes;
+  }
+}
+
+extern "C" jfa_status jfa_workspace_init(void *workspace, size_t ws_bytes, jfa_stream_t stream) {
+  JFA_TRY(check_ws(workspace, ws_bytes, kStatusBytes));
+  return cuda_status(cudaMemsetAsync(workspace, 0, kStatusBytes, (cudaStream_t)stream),
+                     "cudaMemsetAsync");
+}
+
+extern "C" jfa_status jfa_check_status(void *workspace, jfa_stream_t stream) {
+  JFA_TRY(check_ws(workspace, kStatusBytes, kStatusBytes));
+  uint32_t st[4] = {0, 0, 0, 0};
+  JFA_TRY(cuda_status(cudaMemcpyAsync(st, workspace, sizeof(st), cudaMemcpyDeviceToHost,
+                                      (cudaStream_t)stream),
+                      "cudaMemcpyAsync"));
+  JFA_TRY(cuda_status(cudaStreamSynchronize((cudaStream_t)stream), "cudaStreamSynchronize"));
+  if (st[0] != 0) {
+    cudaMemsetAsync(workspace, 0, kStatusBytes, (cudaStream_t)stream);
+    cudaStreamSynchronize((cudaStream_t)stream);
+    return fail(JFA_ERR_TIMEOUT, "kernel wait site %u in block %u gave up", st[1], st[2]);
+  }
+  return JFA_OK;
+}
+
+// ------------------------------------------------------------------ forward
+
+namespace {
+
+jfa_status fwd_common(const void *q, const void *k, const void *v, const void *offsets,
+                      jfa_index_t idx, int64_t B, int64_t q_rows, int64_t Tk, int64_t Lq, int H,
+                      int D, float scale, const int32_t *sm_ptr, const int32_t *tiles,
+                      int num_sms, void *o, float *lse, void *ws, size_t ws_bytes,
+                      cudaStream_t st) {
+  JFA_TRY(check_dims(B, Tk, H, D));
+  if (idx != JFA_I32 && idx != JFA_I64) return fail(JFA_ERR_INVALID_ARG, "bad index type");
+  if (!(scale > 0.f)) return fail(JFA_ERR_INVALID_ARG, "scale must be > 0");
+  JFA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
+  JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
+  JFA_TRY(need_ptr(offsets, "offsets"));
+  if (B == 0 || q_rows == 0) return JFA_OK;
+  JFA_TRY(need_ptr(q, "q"));
+  JFA_TRY(need_ptr(o, "o"));
+  JFA_TRY(need_ptr(lse, "lse"));
+  if (Tk > 0) {
+    JFA_TRY(need_ptr(k, "k"));
+    JFA_TRY(need_ptr(v, "v"));
+  } else {
+    k = v = q;  // never read: every sequence is empty
+  }
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  JFA_TRY(map_rows_bf16(&p.tm_q, q, q_rows, H, D, 128));
+  JFA_TRY(map_rows_bf16(&p.tm_k, k, Tk > 0 ? Tk : q_rows, H, D, 128));
+  JFA_TRY(map_rows_bf16(&p.tm_v, v, Tk > 0 ? Tk : q_rows, H, D, 128));
+  p.offsets = offsets;
+  p.idx64 = idx == JFA_I64;
+  p.sm_ptr = sm_ptr;
+  p.tiles = tiles;
+  p.o = o;
+  p.lse = lse;
+  p.T = Lq > 0 ? Tk : q_rows;
+  p.H = H;
+  p.Lq = (int)Lq;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = static_cast<uint32_t *>(ws);
+  p.timeout_ns = kTimeoutNs;
+  return cuda_status(launch_fwd(p, D, num_sms, st), "fwd launch");
+}
+
+}  // namespace
+
+extern "C" jfa_status jfa_fwd(const void *q, const void *k, const void *v, const void *offsets,
+                              jfa_index_t idx, int64_t B, int64_t T, int H, int D, float scale,
+                              const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_sms,
+                              void *o, float *lse, void *workspace, size_t ws_bytes,
+                              jfa_stream_t stream) {
+  return fwd_common(q, k, v, offsets, idx, B, T, T, 0, H, D, scale, d_sm_ptr, d_tiles, num_sms,
+                    o, lse, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" jfa_status jfa_bcastq_fwd(const void *q, const void *k, const void *v,
+                                     const void *kv_offsets, jfa_index_t idx, int64_t B,
+                                     int64_t Lq, int64_t Tk, int H, int D, float scale,
+                                     const int32_t *d_sm_ptr, const int32_t *d_tiles,
+                                     int num_sms, void *o, float *lse, void *workspace,
+                                     size_t ws_bytes, jfa_stream_t stream) {
+  if (Lq < 0 || Lq >= (1 << 30)) return fail(JFA_ERR_INVALID_ARG, "bad Lq");
+  if (Lq == 0) return JFA_OK;
+  return fwd_common(q, k, v, kv_offsets, idx, B, Lq, Tk, Lq, H, D, scale, d_sm_ptr, d_tiles,
+                    num_sms, o, lse, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ backward
+
+namespace {
+
+jfa_status launch_status(cudaError_t e, const char *what) {
+  if (e == cudaErrorNotSupported) return fail(JFA_ERR_UNSUPPORTED, "%s: not built", what);
+  return cuda_status(e, what);
+}
+
+jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dout, const void *offsets, jfa_index_t idx,
+                      int64_t B, int64_t q_rows, int64_t Tk, int64_t Lq, int H, int D,
+                      float scale, const int32_t *sm_ptr, const int32_t *tiles, int num_sms,
+                      void *dq, void *dk, void *dv, void *ws, size_t ws_bytes, cudaStream_t st) {
+  JFA_TRY(check_dims(B, Tk, H, D));
+  if (idx != JFA_I32 && idx != JFA_I64) return fail(JFA_ERR_INVALID_ARG, "bad index type");
+  if (!(scale > 0.f)) return fail(JFA_ERR_INVALID_ARG, "scale must be > 0");
+  const int64_t acc_rows = Lq > 0 ? Lq : q_rows;
+  const size_t need = kStatusBytes + round_up((size_t)acc_rows * H * D * sizeof(float), 256);
+  JFA_TRY(check_ws(ws, ws_bytes, need));
+  JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
+  JFA_TRY(need_ptr(offsets, "offsets"));
+  if (B == 0 || q_rows == 0) return JFA_OK;
+  JFA_TRY(need_ptr(q, "q"));
+  JFA_TRY(need_ptr(o, "o"));
+  JFA_TRY(need_ptr(lse, "lse"));
+  JFA_TRY(need_ptr(dout, "dout"));
+  JFA_TRY(need_ptr(dq, "dq"));
+  if (Tk > 0) {
+    JFA_TRY(need_ptr(k, "k"));
+    JFA_TRY(need_ptr(v, "v"));
+    JFA_TRY(need_ptr(dk, "dk"));
+    JFA_TRY(need_ptr(dv, "dv"));
+  } else {
+    k = v = q;
+  }
+  float *acc = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kStatusBytes);
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  const int64_t o_rows = Lq > 0 ? B * Lq : q_rows;
+  JFA_TRY(map_rows_bf16(&p.tm_q, q, acc_rows, H, D, 64));
+  JFA_TRY(map_rows_bf16(&p.tm_do, dout, o_rows, H, D, 64));
+  JFA_TRY(map_rows_bf16(&p.tm_o, o, o_rows, H, D, 64));
+  JFA_TRY(map_rows_bf16(&p.tm_k, k, Tk > 0 ? Tk : 1, H, D, 128));
+  JFA_TRY(map_rows_bf16(&p.tm_v, v, Tk > 0 ? Tk : 1, H, D, 128));
+  JFA_TRY(map_acc_f32(&p.tm_dqacc, acc, acc_rows, H, D));
+  p.offsets = offsets;
+  p.idx64 = idx == JFA_I64;
+  p.sm_ptr = sm_ptr;
+  p.tiles = tiles;
+  p.lse = lse;
+  p.dk = dk;
+  p.dv = dv;
+  p.T = Lq > 0 ? Tk : q_rows;
+  p.H = H;
+  p.Lq = (int)Lq;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = static_cast<uint32_t *>(ws);
+  p.timeout_ns = kTimeoutNs;
+  JFA_TRY(cuda_status(cudaMemsetAsync(acc, 0, (size_t)acc_rows * H * D * sizeof(float), st),
+                      "cudaMemsetAsync"));
+  if (Tk > 0) JFA_TRY(launch_status(launch_bwd(p, D, num_sms, st), "bwd launch"));
+  return launch_status(launch_dq_convert(acc, dq, acc_rows, H, D, st), "dq convert");
+}
+
+}  // namespace
+
+extern "C" jfa_status jfa_bwd(const void *q, const void *k, const void *v, const void *o,
+                              const float *lse, const void *dout, const void *offsets,
+                              jfa_index_t idx, int64_t B, int64_t T, int H, int D, float scale,
+                              const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_sms,
+                              void *dq, void *dk, void *dv, void *workspace, size_t ws_bytes,
+                              jfa_stream_t stream) {
+  return bwd_common(q, k, v, o, lse, dout, offsets, idx, B, T, T, 0, H, D, scale, d_sm_ptr,
+                    d_tiles, num_sms, dq, dk, dv, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" jfa_status jfa_bcastq_bwd(const void *q, const void *k, const void *v, const void *o,
+                                     const float *lse, const void *dout, const void *kv_offsets,
+                                     jfa_index_t idx, int64_t B, int64_t Lq, int64_t Tk, int H,
+                                     int D, float scale, const int32_t *d_sm_ptr,
+                                     const int32_t *d_tiles, int num_sms, void *dq, void *dk,
+                                     void *dv, void *workspace, size_t ws_bytes,
+                                     jfa_stream_t stream) {
+  if (Lq < 0 || Lq >= (1 << 30)) return fail(JFA_ERR_INVALID_ARG, "bad Lq");
+  if (Lq == 0) return JFA_OK;
+  return bwd_common(q, k, v, o, lse, dout, kv_offsets, idx, B, Lq, Tk, Lq, H, D, scale,
+                    d_sm_ptr, d_tiles, num_sms, dq, dk, dv, workspace, ws_bytes,
+                    (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------ block-diagonal
+
+namespace {
+
+jfa_status blockdiag_common(const void *q, const void *k, const void *v, const void *dout,
+                            int64_t B, int64_t L, int H, int D, float scale, void *o, void *dq,
+                            void *dk, void *dv, void *ws, size_t ws_bytes, bool bwd,
+                            cudaStream_t st) {
+  JFA_TRY(check_dims(B, B * L, H, D));
+  if (L < 0 || L % 64 != 0) return fail(JFA_ERR_INVALID_ARG, "L = %lld is not a multiple of 64", (long long)L);
+  if (!(scale > 0.f)) return fail(JFA_ERR_INVALID_ARG, "scale must be > 0");
+  JFA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
+  if (B == 0 || L == 0) return JFA_OK;
+  JFA_TRY(need_ptr(q, "q"));
+  JFA_TRY(need_ptr(k, "k"));
+  JFA_TRY(need_ptr(v, "v"));
+  BlockdiagParams p;
+  memset(&p, 0, sizeof(p));
+  const int64_t rows = B * L;
+  JFA_TRY(map_rows_bf16(&p.tm_q, q, rows, H, D, 128));
+  JFA_TRY(map_rows_bf16(&p.tm_k, k, rows, H, D, 128));
+  JFA_TRY(map_rows_bf16(&p.tm_v, v, rows, H, D, 128));
+  if (bwd) {
+    JFA_TRY(need_ptr(dout, "dout"));
+    JFA_TRY(need_ptr(dq, "dq"));
+    JFA_TRY(need_ptr(dk, "dk"));
+    JFA_TRY(need_ptr(dv, "dv"));
+    JFA_TRY(map_rows_bf16(&p.tm_do, dout, rows, H, D, 128));
+  } else {
+    JFA_TRY(need_ptr(o, "o"));
+  }
+  p.o = o;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.rows = rows;
+  p.H = H;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = static_cast<uint32_t *>(ws);
+  p.timeout_ns = kTimeoutNs;
+  int dev = 0, sms = 0;
+  JFA_TRY(cuda_status(cudaGetDevice(&dev), "cudaGetDevice"));
+  JFA_TRY(cuda_status(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                      "cudaDeviceGetAttribute"));
+  return launch_status(bwd ? launch_blockdiag_bwd(p, D, sms, st) : launch_blockdiag_fwd(p, D, sms, st),
+                       bwd ? "blockdiag bwd launch" : "blockdiag fwd launch");
+}
+
+}  // namespace
+
+extern "C" jfa_status blockdiag_fwd(const void *q, const void *k, const void *v, int64_t B,
+                                    int64_t L, int H, int D, float scale, void *o,
+                                    void *workspace, size_t ws_bytes, jfa_stream_t stream) {
+  return blockdiag_common(q, k, v, nullptr, B, L, H, D, scale, o, nullptr, nullptr, nullptr,
+                          workspace, ws_bytes, false, (cudaStream_t)stream);
+}
+
+extern "C" jfa_status blockdiag_bwd(const void *q, const void *k, const void *v,
+                                    const void *dout, int64_t B, int64_t L, int H, int D,
+                                    float scale, void *dq, void *dk, void *dv, void *workspace,
+                                    size_t ws_bytes, jfa_stream_t stream) {
+  return blockdiag_common(q, k, v, dout, B, L, H, D, scale, nullptr, dq, dk, dv, workspace,
+                          ws_bytes, true, (cudaStream_t)stream);
+}

@@ -1,0 +1,565 @@
+// bwd.cu -- persistent, warp-specialised attention backward for sm_103a,
+// jagged self-attention and broadcast-Q.
+//
+// Method ("TLX Block Attention", sections 2 and 4): with P rebuilt from the
+// stored log-sum-exp, P = exp(scale * Q K^T - LSE), and Di = rowsum(dO * O):
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - Di),
+//   dQ = scale * dS K,  dK = scale * dS^T Q.
+// Structure ("Desarrollo de Jagged Flash Attention para el modelo GEM",
+// "Cambios estructurales y gestión de memoria" and "Optimización del proceso
+// de Backward y dQ"): warp-specialised roles including a dQ-reduction group,
+// early release of the dQ tensor memory so the MMA warp can start the next
+// product, and, for broadcast-Q, a double-buffered shared-memory staging of
+// the dQ partials that are summed over the whole batch.
+//
+// A tile is 128 key rows of one (sequence, head). dK and dV for those rows
+// stay in tensor memory while the kernel walks every 64-row query block of
+// the sequence (or the dense Q for broadcast-Q). Per query block:
+//   S^T  = K Q^T        (M=128 keys, N=64 queries, K=D)      -> TMEM
+//   dP^T = V dO^T                                            -> TMEM
+//   P^T, dS^T computed by the compute warps (one key row per thread);
+//   Di for the block's 64 query rows is formed inline from the O and dO
+//   tiles already in shared memory (no separate pass);
+//   dV  += P^T dO       (A = P^T bf16 from TMEM)
+//   dK  += dS^T Q       (A = dS^T bf16 from TMEM)
+//   dQ^T = K^T dS^T     (both operands MN-major in shared memory)  -> TMEM
+// The dQ group reads dQ^T out of TMEM (one head-dim lane per thread),
+// releases the TMEM at once, scales, stages 32x32 fp32 boxes in shared
+// memory (two buffers per warp) and adds them into an fp32 accumulator in
+// global memory with TMA reduce-add. A light kernel converts the
+// accumulator to bf16 at the end.
+//
+// Roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
+// warps 4-7 compute + dK/dV epilogue, warps 8-11 dQ reduction.
+// Tensor memory columns: dV [0,128) dK [128,256) S/P [256,320)
+// dP/dS [320,384) dQ^T [384,448).
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace jfa {
+namespace {
+
+using namespace dev;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int KV_TILE = 128 * D * 2;  // 128-row K or V tile
+  static constexpr int QT = 64 * D * 2;        // 64-row Q, dO or O tile
+  static constexpr int QCHUNK = 64 * 128;      // one 64-column box of a 64-row tile
+  static constexpr int NSTAGE = 2;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = KV_TILE;
+  static constexpr int OFF_ZERO = 2 * KV_TILE;  // D = 64: zero rows padding K^T to M = 128
+  static constexpr int ZERO_BYTES = D == 64 ? 16384 : 0;
+  static constexpr int OFF_STAGE = OFF_ZERO + ZERO_BYTES;
+  static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 3 * QT;  // two 128x64 bf16 dS^T buffers
+  static constexpr int OFF_DQS = OFF_DS + 2 * 16384;          // dQ staging: 4 warps x 2 x 4 KB
+  static constexpr int OFF_LSE = OFF_DQS + 4 * 8192;
+  static constexpr int OFF_DI = OFF_LSE + NSTAGE * 256;
+  static constexpr int OFF_BAR = OFF_DI + NSTAGE * 256;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;
+  static constexpr uint32_t KT_LBO = D == 128 ? 16384 : (OFF_ZERO - OFF_K);
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, 64, 0, 0);
+  static constexpr uint32_t IDESC_G = idesc_bf16(128, D, 0, 1);   // dV, dK
+  static constexpr uint32_t IDESC_Q = idesc_bf16(128, 64, 1, 1);  // dQ^T
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+enum : uint32_t { COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 320, COL_DQ = 384 };
+
+struct BwdBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t stage_full[2], stage_empty[2];
+  uint64_t s_full, dp_full, p_ready, ds_ready;
+  uint64_t ds_free[2];
+  uint64_t dq_full, dq_free;
+  uint64_t dkdv_full, dkdv_free;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct BwdTile {
+  int b, h, nq, nkv;  // query blocks to walk; valid key rows in this tile
+  int kv_row0;        // first key row (tm_k / tm_v / dK / dV)
+  int q_row0;         // first query row of the sequence in tm_q and in the dQ accumulator
+  int o_row0;         // first row of the sequence in tm_o / tm_do
+  int Lq;             // query rows of the sequence
+  int64_t lse0;       // LSE index of query row 0 (jagged: + h*T; bcast: (b*H+h)*Lq)
+};
+
+__device__ __forceinline__ int64_t load_off(const void *off, int idx64, int i) {
+  return idx64 ? static_cast<const int64_t *>(off)[i] : (int64_t) static_cast<const int *>(off)[i];
+}
+
+template <bool BCAST>
+__device__ __forceinline__ BwdTile decode_tile(const BwdParams &p, int t) {
+  BwdTile d;
+  d.b = p.tiles[3 * t];
+  d.h = p.tiles[3 * t + 1];
+  const int n = p.tiles[3 * t + 2];
+  const int64_t s0 = load_off(p.offsets, p.idx64, d.b);
+  const int L = (int)(load_off(p.offsets, p.idx64, d.b + 1) - s0);
+  d.Lq = BCAST ? p.Lq : L;
+  d.nq = (d.Lq + 63) / 64;
+  d.nkv = min(128, L - n * 128);
+  d.kv_row0 = (int)s0 + n * 128;
+  if (BCAST) {
+    d.q_row0 = 0;
+    d.o_row0 = d.b * p.Lq;
+    d.lse0 = ((int64_t)d.b * p.H + d.h) * p.Lq;
+  } else {
+    d.q_row0 = (int)s0;
+    d.o_row0 = (int)s0;
+    d.lse0 = (int64_t)d.h * p.T + s0;
+  }
+  return d;
+}
+
+template <int D, bool BCAST>
+__global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  BwdBars &bars = *reinterpret_cast<BwdBars *>(smem + C::OFF_BAR);
+  float *lse_s = reinterpret_cast<float *>(smem + C::OFF_LSE);  // [NSTAGE][64], log2 units
+  float *di_s = reinterpret_cast<float *>(smem + C::OFF_DI);    // [NSTAGE][64]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.kv_full, 1);
+    mbar_init(&bars.kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.stage_full[s], 1);
+      mbar_init(&bars.stage_empty[s], 2);  // MMA commit + compute warps done with O/dO
+      mbar_init(&bars.ds_free[s], 1);
+    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.p_ready, 4);
+    mbar_init(&bars.ds_ready, 4);
+    mbar_init(&bars.dq_full, 1);
+    mbar_init(&bars.dq_free, 4);
+    mbar_init(&bars.dkdv_full, 1);
+    mbar_init(&bars.dkdv_free, 4);
+    mbar_init(&bars.drain, 1);
+    bars.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (C::ZERO_BYTES > 0) {
+    uint4 *z = reinterpret_cast<uint4 *>(smem + C::OFF_ZERO);
+    for (int i = threadIdx.x; i < C::ZERO_BYTES / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+    fence_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_do);
+    prefetch_tmap(&p.tm_o);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+    prefetch_tmap(&p.tm_dqacc);
+  }
+  if (warp == 2) tmem_alloc(&bars.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  const WaitCtl ctl{p.status, &bars.abort_flag, p.timeout_ns};
+  const int tbeg = p.sm_ptr[blockIdx.x];
+  const int tend = p.sm_ptr[blockIdx.x + 1];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t kvph = 0, stph[2] = {0, 0};
+      int qb = 0;
+      for (int t = tbeg; t < tend; ++t) {
+        const BwdTile tl = decode_tile<BCAST>(p, t);
+        if (tl.nq == 0 || tl.nkv <= 0) continue;
+        if (!mbar_wait(&bars.kv_empty, kvph ^ 1, ctl, 1)) goto done;
+        kvph ^= 1;
+        mbar_arrive_expect_tx(&bars.kv_full, 2 * C::KV_TILE);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(smem + C::OFF_K + c * 16384, &p.tm_k, &bars.kv_full, c * 64, tl.h, tl.kv_row0);
+          tma_load_3d(smem + C::OFF_V + c * 16384, &p.tm_v, &bars.kv_full, c * 64, tl.h, tl.kv_row0);
+        }
+        for (int i = 0; i < tl.nq; ++i, ++qb) {
+          const int s = qb & 1;
+          if (!mbar_wait(&bars.stage_empty[s], stph[s] ^ 1, ctl, 2)) goto done;
+          stph[s] ^= 1;
+          mbar_arrive_expect_tx(&bars.stage_full[s], 3 * C::QT);
+          uint8_t *st = smem + C::OFF_STAGE + s * 3 * C::QT;
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_3d(st + c * C::QCHUNK, &p.tm_q, &bars.stage_full[s], c * 64, tl.h,
+                        tl.q_row0 + i * 64);
+            tma_load_3d(st + C::QT + c * C::QCHUNK, &p.tm_do, &bars.stage_full[s], c * 64, tl.h,
+                        tl.o_row0 + i * 64);
+            tma_load_3d(st + 2 * C::QT + c * C::QCHUNK, &p.tm_o, &bars.stage_full[s], c * 64,
+                        tl.h, tl.o_row0 + i * 64);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t kvph = 0, stph[2] = {0, 0}, pph = 0, dsph = 0, dqfph = 0, dkdvph = 0;
+      int qb = 0;
+      const uint32_t k_a = smem_u32(smem + C::OFF_K);
+      const uint32_t v_a = smem_u32(smem + C::OFF_V);
+      const uint32_t st_a = smem_u32(smem + C::OFF_STAGE);
+      const uint32_t ds_a = smem_u32(smem + C::OFF_DS);
+      // S^T (or dP^T) = X Y^T, X = K (or V) [128 x D], Y = Q (or dO) [64 x D], both K-major.
+      auto issue_xyT = [&](uint32_t dcol, uint32_t xa, uint32_t ya) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          mma_ss(tmem + dcol, sdesc_sw128(xa + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                 sdesc_sw128(ya + (k >> 2) * C::QCHUNK + (k & 3) * 32, 16, 1024), C::IDESC_S,
+                 k > 0);
+        }
+      };
+      // dV (or dK) += A^T-from-TMEM x Y, Y = dO (or Q) [64 x D] MN-major.
+      auto issue_grad = [&](uint32_t dcol, uint32_t acol, uint32_t ya, bool acc) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ts(tmem + dcol, tmem + acol + k * 8, sdesc_sw128(ya + k * 2048, C::QCHUNK, 1024),
+                 C::IDESC_G, (acc || k > 0) ? 1u : 0u);
+      };
+      for (int t = tbeg; t < tend; ++t) {
+        const BwdTile tl = decode_tile<BCAST>(p, t);
+        if (tl.nq == 0 || tl.nkv <= 0) continue;
+        if (!mbar_wait(&bars.kv_full, kvph, ctl, 10)) goto done;
+        kvph ^= 1;
+        for (int i = 0; i < tl.nq; ++i, ++qb) {
+          const int s = qb & 1;
+          const uint32_t q_a = st_a + s * 3 * C::QT;
+          const uint32_t do_a = q_a + C::QT;
+          if (i == 0) {
+            if (!mbar_wait(&bars.stage_full[s], stph[s], ctl, 11)) goto done;
+            stph[s] ^= 1;
+            tc_fence_after();
+            issue_xyT(COL_S, k_a, q_a);
+            mma_commit(&bars.s_full);
+            issue_xyT(COL_DP, v_a, do_a);
+            mma_commit(&bars.dp_full);
+          }
+          if (!mbar_wait(&bars.p_ready, pph, ctl, 12)) goto done;
+          pph ^= 1;
+          if (i == 0) {  // dK/dV accumulators must have been drained by the previous epilogue
+            if (!mbar_wait(&bars.dkdv_free, dkdvph ^ 1, ctl, 13)) goto done;
+            dkdvph ^= 1;
+          }
+          tc_fence_after();
+          issue_grad(COL_DV, COL_S, do_a, i > 0);
+          const bool more = i + 1 < tl.nq;
+          const int s2 = (qb + 1) & 1;
+          const uint32_t q2_a = st_a + s2 * 3 * C::QT;
+          if (more) {
+            if (!mbar_wait(&bars.stage_full[s2], stph[s2], ctl, 14)) goto done;
+            stph[s2] ^= 1;
+            tc_fence_after();
+            issue_xyT(COL_S, k_a, q2_a);
+            mma_commit(&bars.s_full);
+          }
+          if (!mbar_wait(&bars.ds_ready, dsph, ctl, 15)) goto done;
+          dsph ^= 1;
+          tc_fence_after();
+          issue_grad(COL_DK, COL_DP, q_a, i > 0);
+          mma_commit(&bars.stage_empty[s]);
+          if (!mbar_wait(&bars.dq_free, dqfph ^ 1, ctl, 16)) goto done;
+          dqfph ^= 1;
+          tc_fence_after();
+          {
+            const uint32_t dsb = ds_a + (qb & 1) * 16384;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ss(tmem + COL_DQ, sdesc_sw128(k_a + k * 2048, C::KT_LBO, 1024),
+                     sdesc_sw128(dsb + k * 2048, 8192, 1024), C::IDESC_Q, k > 0);
+          }
+          mma_commit(&bars.dq_full);
+          mma_commit(&bars.ds_free[qb & 1]);
+          if (more) {
+            issue_xyT(COL_DP, v_a, q2_a + C::QT);
+            mma_commit(&bars.dp_full);
+          }
+        }
+        mma_commit(&bars.dkdv_full);
+        mma_commit(&bars.kv_empty);
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------ compute + dK/dV epilogue
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // key row within the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t stph[2] = {0, 0}, sph = 0, dpph = 0, dsfph[2] = {0, 0}, dkdvph = 0;
+    int qb = 0;
+    for (int t = tbeg; t < tend; ++t) {
+      const BwdTile tl = decode_tile<BCAST>(p, t);
+      if (tl.nq == 0 || tl.nkv <= 0) continue;
+      const bool kv_ok = r < tl.nkv;
+      for (int i = 0; i < tl.nq; ++i, ++qb) {
+        const int s = qb & 1;
+        const uint8_t *st = smem + C::OFF_STAGE + s * 3 * C::QT;
+        if (!mbar_wait(&bars.stage_full[s], stph[s], ctl, 20)) goto done;
+        stph[s] ^= 1;
+        // LSE (log2 units) and Di = rowsum(dO * O) of the block's query rows.
+        if (r < 64) {
+          const int qrow = i * 64 + r;
+          float lse2 = INFINITY, di = 0.f;
+          if (qrow < tl.Lq) {
+            lse2 = p.lse[tl.lse0 + qrow] * 1.4426950408889634f;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+              const uint8_t *orow = st + 2 * C::QT + c * C::QCHUNK + r * 128;
+              const uint8_t *drow = st + C::QT + c * C::QCHUNK + r * 128;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int off = ((j ^ (r & 7)) << 4);
+                const uint4 ov = *reinterpret_cast<const uint4 *>(orow + off);
+                const uint4 dv = *reinterpret_cast<const uint4 *>(drow + off);
+                const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
+                const __nv_bfloat162 *d2 = reinterpret_cast<const __nv_bfloat162 *>(&dv);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 of = __bfloat1622float2(o2[e]);
+                  const float2 df = __bfloat1622float2(d2[e]);
+                  di = fmaf(of.x, df.x, di);
+                  di = fmaf(of.y, df.y, di);
+                }
+              }
+            }
+          }
+          lse_s[s * 64 + r] = lse2;
+          di_s[s * 64 + r] = di;
+        }
+        named_bar_sync(1, 128);
+        if (r == 0) mbar_arrive(&bars.stage_empty[s]);
+        // P^T row (this thread's key row against the block's 64 query columns).
+        if (!mbar_wait(&bars.s_full, sph, ctl, 21)) goto done;
+        sph ^= 1;
+        tc_fence_after();
+        float pr[64];
+        {
+          uint32_t a[32], b[32];
+          tmem_ld32(tmem + lane_off + COL_S, a);
+          tmem_ld32(tmem + lane_off + COL_S + 32, b);
+          tmem_wait_ld();
+          const float4 *l4 = reinterpret_cast<const float4 *>(lse_s + s * 64);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float4 lv = l4[c];
+            const float lv4[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = c * 4 + e;
+              const float sv = __uint_as_float(col < 32 ? a[col] : b[col - 32]);
+              pr[col] = kv_ok ? ex2(fmaf(sv, sl2, -lv4[e])) : 0.f;
+            }
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pr[2 * c], pr[2 * c + 1]);
+          tmem_st32(tmem + lane_off + COL_S, pk);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_ready);
+        // dS^T row = P^T * (dP^T - Di)
+        if (!mbar_wait(&bars.dp_full, dpph, ctl, 22)) goto done;
+        dpph ^= 1;
+        tc_fence_after();
+        {
+          uint32_t a[32], b[32];
+          tmem_ld32(tmem + lane_off + COL_DP, a);
+          tmem_ld32(tmem + lane_off + COL_DP + 32, b);
+          tmem_wait_ld();
+          const float4 *d4 = reinterpret_cast<const float4 *>(di_s + s * 64);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float4 dv = d4[c];
+            const float dv4[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = c * 4 + e;
+              const float dp = __uint_as_float(col < 32 ? a[col] : b[col - 32]);
+              pr[col] = pr[col] * (dp - dv4[e]);
+            }
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pr[2 * c], pr[2 * c + 1]);
+          tmem_st32(tmem + lane_off + COL_DP, pk);
+          // dS^T into shared memory (MN-major operand of the dQ^T product).
+          const int dsb = qb & 1;
+          if (!mbar_wait(&bars.ds_free[dsb], dsfph[dsb] ^ 1, ctl, 23)) goto done;
+          dsfph[dsb] ^= 1;
+          uint8_t *row = smem + C::OFF_DS + dsb * 16384 + r * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4 *>(row + ((j ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          fence_async_smem();
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.ds_ready);
+      }
+      // dK, dV epilogue for this tile's key rows.
+      if (!mbar_wait(&bars.dkdv_full, dkdvph, ctl, 24)) goto done;
+      dkdvph ^= 1;
+      tc_fence_after();
+      {
+        const int64_t grow = (int64_t)(tl.kv_row0 + r) * p.H + tl.h;
+        uint4 *dvp = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dv) + grow * D);
+        uint4 *dkp = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dk) + grow * D);
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          const float mul = which ? p.scale : 1.f;
+          uint4 *dst = which ? dkp : dvp;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + (which ? COL_DK : COL_DV) + c * 32, v);
+            tmem_wait_ld();
+            if (kv_ok) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                pk[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[c * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.dkdv_free);
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ reduction
+    const int wq = warp & 3;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    uint8_t *stg = smem + C::OFF_DQS + wq * 8192;
+    uint32_t dqph = 0;
+    int last_buf = -1;
+    for (int t = tbeg; t < tend; ++t) {
+      const BwdTile tl = decode_tile<BCAST>(p, t);
+      if (tl.nq == 0 || tl.nkv <= 0) continue;
+      for (int i = 0; i < tl.nq; ++i) {
+        if (!mbar_wait(&bars.dq_full, dqph, ctl, 30)) goto done;
+        dqph ^= 1;
+        tc_fence_after();
+        uint32_t v[2][32];
+        tmem_ld32(tmem + lane_off + COL_DQ, v[0]);
+        tmem_ld32(tmem + lane_off + COL_DQ + 32, v[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.dq_free);  // TMEM released before the reduction
+        if (wq * 32 >= D) continue;                  // D = 64: lanes 64..127 are padding
+        const int rows = min(64, tl.Lq - i * 64);
+#pragma unroll
+        for (int qc = 0; qc < 2; ++qc) {
+          if (qc * 32 >= rows) break;
+          float *buf = reinterpret_cast<float *>(stg + qc * 4096);
+          if (lane == 0) {
+            if (last_buf == qc) bulk_wait_read<0>();
+            else bulk_wait_read<1>();
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) buf[j * 32 + lane] = __uint_as_float(v[qc][j]) * p.scale;
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&p.tm_dqacc, buf, wq * 32, tl.q_row0 + i * 64 + qc * 32, tl.h);
+            bulk_commit();
+          }
+          last_buf = qc;
+        }
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+  }
+done:
+  if (warp == 1 && lane == 0 && bars.abort_flag) {
+    mma_commit(&bars.drain);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&bars.drain, 0) && globaltimer() - t0 < p.timeout_ns) {
+    }
+  }
+  if (warp >= 8 && lane == 0) bulk_wait<0>();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool BCAST>
+cudaError_t launch_t(const BwdParams &p, int num_sms, cudaStream_t st) {
+  auto kern = jfa_bwd_kernel<D, BCAST>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms, 384, BwdCfg<D>::SMEM, st>>>(p);
+  return cudaGetLastError();
+}
+
+// fp32 [H, rows, D] -> bf16 [rows, H, D]; 8 elements per thread.
+__global__ void dq_convert_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq,
+                                  int64_t rows, int H, int D) {
+  const int64_t n8 = rows * H * D / 8;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = i * 8;  // element index in [rows, H, D]
+    const int d = (int)(e % D);
+    const int64_t rh = e / D;
+    const int h = (int)(rh % H);
+    const int64_t row = rh / H;
+    const float4 *src = reinterpret_cast<const float4 *>(acc + ((int64_t)h * rows + row) * D + d);
+    const float4 a = src[0], b = src[1];
+    uint4 o;
+    o.x = pack_bf16(a.x, a.y);
+    o.y = pack_bf16(a.z, a.w);
+    o.z = pack_bf16(b.x, b.y);
+    o.w = pack_bf16(b.z, b.w);
+    *reinterpret_cast<uint4 *>(dq + e) = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdParams &p, int D, int num_sms, cudaStream_t st) {
+  const bool bcast = p.Lq > 0;
+  if (D == 128) return bcast ? launch_t<128, true>(p, num_sms, st) : launch_t<128, false>(p, num_sms, st);
+  return bcast ? launch_t<64, true>(p, num_sms, st) : launch_t<64, false>(p, num_sms, st);
+}
+
+cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, int D,
+                              cudaStream_t st) {
+  const int64_t n8 = rows * H * D / 8;
+  if (n8 == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (n8 + 255) / 256;
+  const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+  dq_convert_kernel<<<grid, 256, 0, st>>>(acc, static_cast<__nv_bfloat16 *>(dq), rows, H, D);
+  return cudaGetLastError();
+}
+
+}  // namespace jfa

@@ -1,0 +1,414 @@
+// fwd.cu -- persistent, warp-specialised attention forward for sm_103a,
+// jagged self-attention and broadcast-Q.
+//
+// Method: "TLX Block Attention", section 2 (the standard FlashAttention loop:
+// S = Q K^T per K/V tile, running row max m, correction alpha =
+// exp(m_old - m_new), O = alpha O + exp(S - m) V, l = alpha l + rowsum,
+// O /= l, L = m + log l stored for the backward pass), run directly on packed
+// sequences delimited by an offsets tensor ("Desarrollo de Jagged Flash
+// Attention para el modelo GEM", first section).
+//
+// Structure ("Cambios estructurales y gestión de memoria"; "A TLX nagyobb
+// kontrollt ad a Triton fölött": persistent kernel, one CTA per SM working
+// through many tiles; dedicated TMA-load, MMA, softmax and epilogue roles;
+// multi-buffered K/V; score, P and softmax state sharing one tensor-memory
+// allocation while the PV accumulator keeps its own):
+//
+//   warp 0       TMA producer: Q halves, then K/V tiles into a ring of slots
+//   warp 1       MMA issuer: S = Q K^T into TMEM, O += P V from TMEM P
+//   warp 2       owns the tensor-memory allocation
+//   warps 4-7    softmax + correction + epilogue for query rows   0..127
+//   warps 8-11   softmax + correction + epilogue for query rows 128..255
+//
+// A tile is 256 query rows of one (sequence, head): two 128-row halves that
+// share every K/V tile, so the tensor core works on one half while the
+// other half's softmax runs. Each softmax thread owns one query row (one
+// TMEM lane). P is written back as bf16 over the first half of its own S
+// columns and read from there by the PV MMA. The correction is applied
+// lazily: the running max is only raised when a tile's max exceeds it by
+// more than 2^8 (log2 domain), so O rarely needs rescaling in TMEM; the
+// final normalisation by l makes the result identical in exact arithmetic.
+// The K/V loop is peeled: only the last K/V tile of a sequence is masked.
+//
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [  0,128) S/P of half A   [128,256) S/P of half B
+//   [256,256+D) O of half A   [384,384+D) O of half B
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace jfa {
+namespace {
+
+using namespace dev;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int TILE_BYTES = 128 * D * 2;  // one 128-row Q, K or V tile
+  static constexpr int NSLOT = D == 128 ? 4 : 8;  // K/V ring depth
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = 2 * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE_BYTES;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;
+  static constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, 0, 1);
+};
+
+struct FwdBars {
+  uint64_t q_full[2], q_empty[2], s_full[2], p_ready[2], o_full[2], o_free[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct FwdTile {
+  int b, h, n_kv, Lk, nrows[2];
+  int q_coord;       // row coordinate of the tile's first query row in tm_q
+  int kv0;           // first key row in tm_k / tm_v
+  int64_t out_row0;  // row of the tile's first query row in O
+  int64_t lse0;      // index of that row's LSE
+};
+
+__device__ __forceinline__ int64_t load_off(const void *off, int idx64, int i) {
+  return idx64 ? static_cast<const int64_t *>(off)[i] : (int64_t) static_cast<const int *>(off)[i];
+}
+
+template <bool BCAST>
+__device__ __forceinline__ FwdTile decode_tile(const FwdParams &p, int t) {
+  FwdTile d;
+  d.b = p.tiles[3 * t];
+  d.h = p.tiles[3 * t + 1];
+  const int m = p.tiles[3 * t + 2];
+  const int64_t s0 = load_off(p.offsets, p.idx64, d.b);
+  const int L = (int)(load_off(p.offsets, p.idx64, d.b + 1) - s0);
+  const int Lq = BCAST ? p.Lq : L;
+  const int row0 = m * 256;
+  d.Lk = L;
+  d.n_kv = (L + 127) / 128;
+  d.nrows[0] = max(0, min(128, Lq - row0));
+  d.nrows[1] = max(0, min(128, Lq - row0 - 128));
+  d.kv0 = (int)s0;
+  if (BCAST) {
+    d.q_coord = row0;
+    d.out_row0 = (int64_t)d.b * Lq + row0;
+    d.lse0 = ((int64_t)d.b * p.H + d.h) * Lq + row0;
+  } else {
+    d.q_coord = (int)s0 + row0;
+    d.out_row0 = s0 + row0;
+    d.lse0 = (int64_t)d.h * p.T + s0 + row0;
+  }
+  return d;
+}
+
+template <int D, bool BCAST>
+__global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  FwdBars &bars = *reinterpret_cast<FwdBars *>(smem + C::OFF_BAR);
+  uint64_t *slot_full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR + sizeof(FwdBars) + 8);
+  uint64_t *slot_empty = slot_full + C::NSLOT;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars.q_full[x], 1);
+      mbar_init(&bars.q_empty[x], 1);
+      mbar_init(&bars.s_full[x], 1);
+      mbar_init(&bars.p_ready[x], 4);
+      mbar_init(&bars.o_full[x], 1);
+      mbar_init(&bars.o_free[x], 4);
+    }
+    mbar_init(&bars.drain, 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(&slot_full[s], 1);
+      mbar_init(&slot_empty[s], 1);
+    }
+    bars.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+  }
+  if (warp == 2) tmem_alloc(&bars.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  const WaitCtl ctl{p.status, &bars.abort_flag, p.timeout_ns};
+  const int tbeg = p.sm_ptr[blockIdx.x];
+  const int tend = p.sm_ptr[blockIdx.x + 1];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t qph[2] = {0, 0};
+      int slot = 0;
+      uint32_t sph = 0;
+      for (int t = tbeg; t < tend; ++t) {
+        const FwdTile tl = decode_tile<BCAST>(p, t);
+        if (tl.n_kv == 0) continue;
+        for (int x = 0; x < 2; ++x) {
+          if (tl.nrows[x] == 0) continue;
+          if (!mbar_wait(&bars.q_empty[x], qph[x] ^ 1, ctl, 1)) goto done;
+          qph[x] ^= 1;
+          mbar_arrive_expect_tx(&bars.q_full[x], C::TILE_BYTES);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::OFF_Q + x * C::TILE_BYTES + c * 16384, &p.tm_q,
+                        &bars.q_full[x], c * 64, tl.h, tl.q_coord + x * 128);
+        }
+        for (int j = 0; j < tl.n_kv; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            if (!mbar_wait(&slot_empty[slot], sph ^ 1, ctl, 2)) goto done;
+            mbar_arrive_expect_tx(&slot_full[slot], C::TILE_BYTES);
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(smem + C::OFF_RING + slot * C::TILE_BYTES + c * 16384,
+                          kv ? &p.tm_v : &p.tm_k, &slot_full[slot], c * 64, tl.h,
+                          tl.kv0 + j * 128);
+            if (++slot == C::NSLOT) {
+              slot = 0;
+              sph ^= 1;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t qph[2] = {0, 0}, pph[2] = {0, 0}, oph[2] = {0, 0};
+      int slot = 0;
+      uint32_t sph = 0;
+      const uint32_t q_addr = smem_u32(smem + C::OFF_Q);
+      const uint32_t ring = smem_u32(smem + C::OFF_RING);
+      auto issue_qk = [&](int x, int kslot) {
+        const uint32_t qa = q_addr + x * C::TILE_BYTES;
+        const uint32_t ka = ring + kslot * C::TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tmem + x * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                 C::IDESC_QK, k > 0);
+        }
+      };
+      auto issue_pv = [&](int x, int vslot, bool acc) {
+        const uint32_t va = ring + vslot * C::TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8,
+                 sdesc_sw128(va + k * 2048, 16384, 1024), C::IDESC_PV, (acc || k > 0) ? 1u : 0u);
+      };
+      for (int t = tbeg; t < tend; ++t) {
+        const FwdTile tl = decode_tile<BCAST>(p, t);
+        if (tl.n_kv == 0) continue;
+        const bool has[2] = {tl.nrows[0] > 0, tl.nrows[1] > 0};
+        for (int x = 0; x < 2; ++x) {
+          if (!has[x]) continue;
+          if (!mbar_wait(&bars.q_full[x], qph[x], ctl, 10)) goto done;
+          qph[x] ^= 1;
+        }
+        // S_0 for both halves.
+        int kslot = slot;
+        if (!mbar_wait(&slot_full[kslot], sph, ctl, 11)) goto done;
+        if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
+        tc_fence_after();
+        for (int x = 0; x < 2; ++x) {
+          if (!has[x]) continue;
+          issue_qk(x, kslot);
+          mma_commit(&bars.s_full[x]);
+          if (tl.n_kv == 1) mma_commit(&bars.q_empty[x]);
+        }
+        mma_commit(&slot_empty[kslot]);
+        for (int j = 1; j <= tl.n_kv; ++j) {
+          // V_{j-1}
+          const int vslot = slot;
+          if (!mbar_wait(&slot_full[vslot], sph, ctl, 12)) goto done;
+          if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
+          kslot = -1;
+          if (j < tl.n_kv) {
+            kslot = slot;
+            if (!mbar_wait(&slot_full[kslot], sph, ctl, 13)) goto done;
+            if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
+          }
+          for (int x = 0; x < 2; ++x) {
+            if (!has[x]) continue;
+            if (!mbar_wait(&bars.p_ready[x], pph[x], ctl, 14)) goto done;
+            pph[x] ^= 1;
+            if (j == 1) {  // first PV of the tile overwrites O: epilogue must be done with it
+              if (!mbar_wait(&bars.o_free[x], oph[x] ^ 1, ctl, 15)) goto done;
+              oph[x] ^= 1;
+            }
+            tc_fence_after();
+            issue_pv(x, vslot, j > 1);
+            if (j == tl.n_kv) mma_commit(&bars.o_full[x]);
+            if (kslot >= 0) {
+              issue_qk(x, kslot);
+              mma_commit(&bars.s_full[x]);
+              if (j == tl.n_kv - 1) mma_commit(&bars.q_empty[x]);
+            }
+          }
+          mma_commit(&slot_empty[vslot]);
+          if (kslot >= 0) mma_commit(&slot_empty[kslot]);
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------ softmax + epilogue
+    const int x = (warp - 4) >> 2;  // half
+    const int wq = warp & 3;        // TMEM lane quarter
+    const int r = wq * 32 + lane;   // row within the half
+    const uint32_t tS = tmem + ((uint32_t)(wq * 32) << 16) + x * 128;
+    const uint32_t tO = tmem + ((uint32_t)(wq * 32) << 16) + 256 + x * 128;
+    const float sl2 = p.scale_log2;
+    uint32_t sph = 0, oph = 0;
+    __nv_bfloat16 *obase = static_cast<__nv_bfloat16 *>(p.o);
+    for (int t = tbeg; t < tend; ++t) {
+      const FwdTile tl = decode_tile<BCAST>(p, t);
+      const int nrows = tl.nrows[x];
+      if (nrows == 0) continue;
+      const bool row_ok = r < nrows;
+      const int64_t orow = tl.out_row0 + x * 128 + r;
+      uint4 *optr = reinterpret_cast<uint4 *>(obase + (orow * p.H + tl.h) * D);
+      if (tl.n_kv == 0) {  // broadcast-Q sequence with no keys: O = 0, LSE = -inf
+        if (row_ok) {
+          for (int i = 0; i < D / 8; ++i) optr[i] = make_uint4(0, 0, 0, 0);
+          p.lse[tl.lse0 + x * 128 + r] = -INFINITY;
+        }
+        continue;
+      }
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < tl.n_kv; ++j) {
+        if (!mbar_wait(&bars.s_full[x], sph, ctl, 20 + x)) goto done;
+        sph ^= 1;
+        tc_fence_after();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+        tmem_wait_ld();
+        const int valid = tl.Lk - j * 128;
+        if (valid < 128) {  // peeled tail: mask keys past the sequence end
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= valid) s[c][i] = __float_as_uint(-INFINITY);
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(s[c][i]));
+        const float m_tile =
+            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+            sl2;
+        float alpha = 1.f;
+        if (j == 0) {
+          m_run = m_tile;
+        } else if (m_tile > m_run + 8.f) {
+          alpha = ex2(m_run - m_tile);
+          m_run = m_tile;
+        }
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(__uint_as_float(s[c][2 * i]), sl2, -m_run));
+            const float p1 = ex2(fmaf(__uint_as_float(s[c][2 * i + 1]), sl2, -m_run));
+            sum[i & 3] += p0 + p1;
+            pk[i] = pack_bf16(p0, p1);
+          }
+          tmem_st16(tS + c * 16, pk);
+        }
+        l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_ready[x]);
+      }
+      // epilogue
+      if (!mbar_wait(&bars.o_full[x], oph, ctl, 22 + x)) goto done;
+      oph ^= 1;
+      tc_fence_after();
+      {
+        const float inv_l = 1.f / l_run;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
+          if (row_ok) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l,
+                                __uint_as_float(o[2 * i + 1]) * inv_l);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              optr[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (row_ok) p.lse[tl.lse0 + x * 128 + r] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.o_free[x]);
+    }
+  }
+done:
+  if (warp == 1 && lane == 0 && bars.abort_flag) {
+    // Let any MMA still in flight finish before the tensor memory is freed.
+    mma_commit(&bars.drain);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&bars.drain, 0) && globaltimer() - t0 < p.timeout_ns) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool BCAST>
+cudaError_t launch_t(const FwdParams &p, int num_sms, cudaStream_t st) {
+  auto kern = jfa_fwd_kernel<D, BCAST>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms, 384, FwdCfg<D>::SMEM, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdParams &p, int D, int num_sms, cudaStream_t st) {
+  const bool bcast = p.Lq > 0;
+  if (D == 128) return bcast ? launch_t<128, true>(p, num_sms, st) : launch_t<128, false>(p, num_sms, st);
+  return bcast ? launch_t<64, true>(p, num_sms, st) : launch_t<64, false>(p, num_sms, st);
+}
+
+}  // namespace jfa

@@ -1,0 +1,82 @@
+// kernels.h -- parameter blocks and launchers of the device kernels
+// (internal to libjfa; the public interface is include/jfa.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace jfa {
+
+// Forward kernel (jagged and broadcast-Q). Tiles are 256 query rows: two
+// 128-row halves A and B that share every K/V tile.
+struct FwdParams {
+  CUtensorMap tm_q;  // bf16 [rows, H, D] viewed as {D, H, rows}, box {64, 1, 128}, 128B swizzle
+  CUtensorMap tm_k;  // bf16 [Tk, H, D], same box
+  CUtensorMap tm_v;
+  const void *offsets;  // device [B+1]
+  int idx64;            // offsets are int64
+  const int32_t *sm_ptr;
+  const int32_t *tiles;
+  void *o;      // bf16
+  float *lse;   // fp32
+  int64_t T;    // packed length (LSE row stride for the jagged layout)
+  int H;
+  int Lq;       // broadcast-Q: dense query length; 0 for jagged self-attention
+  float scale_log2;  // scale * log2(e)
+  uint32_t *status;
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_fwd(const FwdParams &p, int D, int num_sms, cudaStream_t st);
+
+// Backward kernel (jagged and broadcast-Q). Tiles are 128 key rows; the
+// kernel walks the sequence's query rows in blocks of 64.
+struct BwdParams {
+  CUtensorMap tm_q;   // bf16 query rows, box {64, 1, 64}
+  CUtensorMap tm_do;  // bf16 dO rows (same row space as O), box {64, 1, 64}
+  CUtensorMap tm_o;   // bf16 O rows, box {64, 1, 64}
+  CUtensorMap tm_k;   // bf16 [Tk, H, D], box {64, 1, 128}
+  CUtensorMap tm_v;
+  CUtensorMap tm_dqacc;  // fp32 [H, rows, D] as {D, rows, H}, box {32, 32, 1}, no swizzle
+  const void *offsets;
+  int idx64;
+  const int32_t *sm_ptr;
+  const int32_t *tiles;
+  const float *lse;
+  void *dk;  // bf16 [Tk, H, D]
+  void *dv;
+  int64_t T;
+  int H;
+  int Lq;  // broadcast-Q: dense query length; 0 for jagged
+  float scale;
+  float scale_log2;
+  uint32_t *status;
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_bwd(const BwdParams &p, int D, int num_sms, cudaStream_t st);
+
+// fp32 [H, rows, D] accumulator -> bf16 [rows, H, D]
+cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, int D,
+                              cudaStream_t st);
+
+// Block-diagonal kernels: [B, L, H, D], 64-token blocks, 128-row work units.
+struct BlockdiagParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // {D, H, B*L}, box {64, 1, 128}
+  void *o;   // forward output
+  void *dq;  // backward outputs
+  void *dk;
+  void *dv;
+  int64_t rows;  // B * L
+  int H;
+  float scale;
+  float scale_log2;
+  uint32_t *status;
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_blockdiag_fwd(const BlockdiagParams &p, int D, int num_sms, cudaStream_t st);
+cudaError_t launch_blockdiag_bwd(const BlockdiagParams &p, int D, int num_sms, cudaStream_t st);
+
+}  // namespace jfa

@@ -1,0 +1,43 @@
+"""Shared helpers for the parity tests: tolerances and comparisons.
+
+Tolerances (bf16 inputs, fp32 accumulation, bf16 outputs):
+O, dQ, dK, dV: max-abs error <= 2e-2 and relative L2 error <= 1e-2 against
+the fp64 oracle on the same bf16 inputs. LSE (fp32 output): max-abs error
+<= 1e-3; it is a log of a sum of exponentials of fp32 scores computed from
+exact bf16 products, so its error is a few ulp of fp32 times |S|.
+"""
+
+import numpy as np
+import torch
+
+ATOL = 2e-2
+RL2 = 1e-2
+LSE_ATOL = 1e-3
+
+
+def f64(t):
+    if isinstance(t, torch.Tensor):
+        return t.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def assert_close(got, ref, name, atol=ATOL, rl2=RL2):
+    got, ref = f64(got), f64(ref)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), "%s has non-finite values" % name
+    err = np.abs(got - ref)
+    mx = float(err.max()) if err.size else 0.0
+    den = float(np.linalg.norm(ref))
+    rel = float(np.linalg.norm(got - ref)) / den if den > 0 else float(np.linalg.norm(got))
+    assert mx <= atol and rel <= rl2, "%s: max-abs %.3g (tol %.3g), rel-L2 %.3g (tol %.3g)" % (
+        name, mx, atol, rel, rl2)
+    return mx, rel
+
+
+def assert_lse(got, ref, name="lse", atol=LSE_ATOL):
+    got, ref = f64(got), f64(ref)
+    inf_ref = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), inf_ref), name + ": -inf pattern differs"
+    if (~inf_ref).any():
+        mx = float(np.abs(got[~inf_ref] - ref[~inf_ref]).max())
+        assert mx <= atol, "%s: max-abs %.3g (tol %.3g)" % (name, mx, atol)
