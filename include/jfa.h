@@ -118,10 +118,9 @@ jfa_status jfa_num_sms(int *num_sms);
  * Workspace.
  *
  * Every kernel call takes a device workspace that starts with a 256-byte
- * status block. The backward calls also keep an fp32 dQ accumulator there
- * ([H, T, D] for jfa_bwd, [H, Lq, D] for jfa_bcastq_bwd), which the call
- * clears itself. `n` is T for JFA_OP_FWD / JFA_OP_BWD, Lq for the
- * broadcast-Q ops and is ignored for the block-diagonal ops.
+ * status block. jfa_bwd also keeps an fp32 dQ accumulator there ([T, H, D]),
+ * which the call clears itself. `n` is T for JFA_OP_FWD / JFA_OP_BWD and is
+ * ignored for the other ops.
  * ---------------------------------------------------------------------- */
 size_t jfa_workspace_size(jfa_op op, int64_t n, int H, int D);
 
@@ -178,16 +177,18 @@ jfa_status jfa_bcastq_fwd(const void *q, const void *k, const void *v, const voi
                           jfa_stream_t stream);
 
 /* Broadcast-Q backward: dout device bf16 [B, Lq, H, D]; writes
- * dq = sum over b of each sequence's dQ (device bf16 [Lq, H, D]) and dk,
+ * dq = sum over b of each sequence's dQ (device fp32 [Lq, H, D]) and dk,
  * dv (device bf16 [Tk, H, D]). The per-sequence dQ partials are summed in
  * fp32 through a double-buffered shared-memory staging area ("Optimización
- * del proceso de Backward y dQ"). Tiles: tile_rows =
+ * del proceso de Backward y dQ") straight into dq, which is therefore fp32:
+ * a sum over the whole batch grows with B and a bf16 result would lose more
+ * than the accumulation itself. The call clears dq first. Tiles: tile_rows =
  * jfa_tile_rows(JFA_OP_BCASTQ_BWD) over key blocks, fixed_work = Lq. */
 jfa_status jfa_bcastq_bwd(const void *q, const void *k, const void *v, const void *o,
                           const float *lse, const void *dout, const void *kv_offsets,
                           jfa_index_t idx, int64_t B, int64_t Lq, int64_t Tk, int H, int D,
                           float scale, const int32_t *d_sm_ptr, const int32_t *d_tiles,
-                          int num_sms, void *dq, void *dk, void *dv, void *workspace,
+                          int num_sms, float *dq, void *dk, void *dv, void *workspace,
                           size_t ws_bytes, jfa_stream_t stream);
 
 /* Block-diagonal forward ("TLX Block Attention", sections 1-2): q, k, v

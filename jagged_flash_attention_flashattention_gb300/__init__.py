@@ -141,16 +141,21 @@ class Plan:
     """Schedules (on the device) and workspace for one batch layout.
 
     kind: "jagged" (offsets of the packed Q/K/V) or "bcast" (offsets of the
-    packed K/V, dense Q of length Lq). The host offsets are read once here;
-    the device offsets tensor is what the kernels read.
+    packed K/V, dense Q of length Lq). The scheduler runs on the host, so it
+    reads host offsets: pass them as `host_offsets` (numpy) when the caller
+    already has them, otherwise they are copied from `offsets` once. Tile
+    lists are copied to the device asynchronously from pinned memory.
+    `workspace` (uint8 CUDA tensor) may be shared between plans; it is
+    allocated when absent or too small.
     """
 
-    def __init__(self, offsets, H, D, kind="jagged", Lq=0, zigzag=True, device=None):
+    def __init__(self, offsets, H, D, kind="jagged", Lq=0, zigzag=True, host_offsets=None,
+                 workspace=None):
         if not offsets.is_cuda:
             raise ValueError("offsets must be a CUDA tensor")
         self.offsets = offsets
         self.idx = JFA_I64 if offsets.dtype == torch.int64 else JFA_I32
-        host = offsets.cpu().numpy()
+        host = np.asarray(host_offsets) if host_offsets is not None else offsets.cpu().numpy()
         self.host_offsets = host
         self.B = host.size - 1
         self.T = int(host[-1])
@@ -165,13 +170,17 @@ class Plan:
                            zigzag=zigzag)
             bwd = schedule(host, H, tile_rows(OP_BCASTQ_BWD, D), self.n_sms, fixed_work=self.Lq,
                            zigzag=zigzag)
-        self.fwd_sched = tuple(torch.from_numpy(a.copy()).to(dev) for a in fwd)
-        self.bwd_sched = tuple(torch.from_numpy(a.copy()).to(dev) for a in bwd)
+        self._pinned = [torch.from_numpy(a).pin_memory() for a in fwd + bwd]
+        d = [t.to(dev, non_blocking=True) for t in self._pinned]
+        self.fwd_sched, self.bwd_sched = (d[0], d[1]), (d[2], d[3])
         self.n_fwd_tiles, self.n_bwd_tiles = fwd[1].shape[0], bwd[1].shape[0]
         rows = self.T if kind == "jagged" else self.Lq
         op = OP_BWD if kind == "jagged" else OP_BCASTQ_BWD
         nbytes = lib().jfa_workspace_size(op, rows, H, D)
-        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        if workspace is None or workspace.numel() < nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            _check(lib().jfa_workspace_init(_ptr(workspace), nbytes, _stream()))
+        self.workspace = workspace
 
     def check(self):
         """Synchronises and raises if a kernel reported a timeout."""
@@ -229,12 +238,14 @@ def jfa_bcastq_fwd(q, k, v, kv_offsets, scale=None, plan=None):
 
 
 def jfa_bcastq_bwd(q, k, v, o, lse, do, kv_offsets, scale=None, plan=None):
-    """Broadcast-Q backward. Returns (dq [Lq, H, D] summed over sequences, dk, dv [Tk, H, D])."""
+    """Broadcast-Q backward. Returns (dq [Lq, H, D] fp32 summed over sequences,
+    dk, dv [Tk, H, D] bf16)."""
     _need_cuda(q, k, v, o, do)
     Lq, H, D = q.shape
     plan = plan or Plan(kv_offsets, H, D, kind="bcast", Lq=Lq)
     Tk, B = k.shape[0], plan.B
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
     sp, tl = plan.bwd_sched
     _check(lib().jfa_bcastq_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
                                 _ptr(kv_offsets), plan.idx, B, Lq, Tk, H, D, _scale(scale, D),

@@ -53,14 +53,14 @@ jfa_status map_rows_bf16(CUtensorMap *m, const void *base, int64_t rows, int H, 
   return JFA_OK;
 }
 
-// fp32 [H, rows, D] as {D, rows, H}; box {32, 32, 1}, no swizzle.
+// fp32 [rows, H, D] as {D, H, rows}; box {32, 1, 32}, no swizzle.
 jfa_status map_acc_f32(CUtensorMap *m, void *base, int64_t rows, int H, int D) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return fail(JFA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   if (rows < 1) rows = 1;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)rows * D * 4};
-  cuuint32_t box[3] = {32, 32, 1};
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
+  cuuint32_t box[3] = {32, 1, 32};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -142,12 +142,8 @@ extern "C" jfa_status jfa_num_sms(int *num_sms) {
 
 extern "C" size_t jfa_workspace_size(jfa_op op, int64_t n, int H, int D) {
   if (n < 0 || H < 1 || D < 1) return kStatusBytes;
-  switch (op) {
-    case JFA_OP_BWD:
-    case JFA_OP_BCASTQ_BWD:
-      return kStatusBytes + round_up((size_t)n * H * D * sizeof(float), 256);
-    default: return kStatusBytes;
-  }
+  if (op == JFA_OP_BWD) return kStatusBytes + round_up((size_t)n * H * D * sizeof(float), 256);
+  return kStatusBytes;
 }
 
 extern "C" jfa_status jfa_workspace_init(void *workspace, size_t ws_bytes, jfa_stream_t stream) {
@@ -184,9 +180,10 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *o
   if (idx != JFA_I32 && idx != JFA_I64) return fail(JFA_ERR_INVALID_ARG, "bad index type");
   if (!(scale > 0.f)) return fail(JFA_ERR_INVALID_ARG, "scale must be > 0");
   JFA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
-  JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
+  if (num_sms < 1) return fail(JFA_ERR_INVALID_ARG, "num_sms = %d < 1", num_sms);
   JFA_TRY(need_ptr(offsets, "offsets"));
   if (B == 0 || q_rows == 0) return JFA_OK;
+  JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
   JFA_TRY(need_ptr(q, "q"));
   JFA_TRY(need_ptr(o, "o"));
   JFA_TRY(need_ptr(lse, "lse"));
@@ -257,11 +254,15 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   if (idx != JFA_I32 && idx != JFA_I64) return fail(JFA_ERR_INVALID_ARG, "bad index type");
   if (!(scale > 0.f)) return fail(JFA_ERR_INVALID_ARG, "scale must be > 0");
   const int64_t acc_rows = Lq > 0 ? Lq : q_rows;
-  const size_t need = kStatusBytes + round_up((size_t)acc_rows * H * D * sizeof(float), 256);
+  // Jagged: fp32 accumulator in the workspace, cast to bf16 at the end.
+  // Broadcast-Q: the caller's fp32 dq is the accumulator itself.
+  const size_t need =
+      kStatusBytes + (Lq > 0 ? 0 : round_up((size_t)acc_rows * H * D * sizeof(float), 256));
   JFA_TRY(check_ws(ws, ws_bytes, need));
-  JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
+  if (num_sms < 1) return fail(JFA_ERR_INVALID_ARG, "num_sms = %d < 1", num_sms);
   JFA_TRY(need_ptr(offsets, "offsets"));
   if (B == 0 || q_rows == 0) return JFA_OK;
+  JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
   JFA_TRY(need_ptr(q, "q"));
   JFA_TRY(need_ptr(o, "o"));
   JFA_TRY(need_ptr(lse, "lse"));
@@ -275,7 +276,8 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   } else {
     k = v = q;
   }
-  float *acc = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kStatusBytes);
+  float *acc = Lq > 0 ? static_cast<float *>(dq)
+                      : reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kStatusBytes);
   BwdParams p;
   memset(&p, 0, sizeof(p));
   const int64_t o_rows = Lq > 0 ? B * Lq : q_rows;
@@ -302,6 +304,7 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   JFA_TRY(cuda_status(cudaMemsetAsync(acc, 0, (size_t)acc_rows * H * D * sizeof(float), st),
                       "cudaMemsetAsync"));
   if (Tk > 0) JFA_TRY(launch_status(launch_bwd(p, D, num_sms, st), "bwd launch"));
+  if (Lq > 0) return JFA_OK;
   return launch_status(launch_dq_convert(acc, dq, acc_rows, H, D, st), "dq convert");
 }
 
@@ -321,7 +324,7 @@ extern "C" jfa_status jfa_bcastq_bwd(const void *q, const void *k, const void *v
                                      const float *lse, const void *dout, const void *kv_offsets,
                                      jfa_index_t idx, int64_t B, int64_t Lq, int64_t Tk, int H,
                                      int D, float scale, const int32_t *d_sm_ptr,
-                                     const int32_t *d_tiles, int num_sms, void *dq, void *dk,
+                                     const int32_t *d_tiles, int num_sms, float *dq, void *dk,
                                      void *dv, void *workspace, size_t ws_bytes,
                                      jfa_stream_t stream) {
   if (Lq < 0 || Lq >= (1 << 30)) return fail(JFA_ERR_INVALID_ARG, "bad Lq");

@@ -1,5 +1,562 @@
+// blockdiag.cu -- fixed 64-token block-diagonal attention, forward and
+// backward, for sm_103a ("TLX Block Attention", sections 1-4).
+//
+// Every 64-token query block attends only to its own 64-token key/value
+// block, so one score tile per block holds the whole softmax row: there is
+// no K/V loop, no online correction (alpha is identically 1), no LSE is
+// stored, the backward recomputes P from Q and K, Di is formed inline as
+// rowsum(P * dP) (equal to rowsum(dO * O) because O = P V), and every output
+// is one fresh product (no accumulation across iterations).
+//
+// Work unit: 128 rows of one head (two 64-token blocks). Scores are computed
+// as one 128x128 product; each thread (query row) uses only the 64 columns
+// of its own block and treats the off-diagonal half as zero probability.
+// With an arithmetic intensity near 32 FLOP/byte the kernels are bound by
+// HBM bandwidth, so the tensor core has slack for the masked half and the
+// design goal is to keep loads and stores in flight: persistent CTAs (one
+// per SM), TMA loads running ahead through shared-memory stages, and the
+// epilogue overlapped with the next unit's products.
+//
+// Forward roles: warp 0 TMA producer, warp 1 MMA, warp 2 TMEM owner, warps
+// 4-7 softmax + epilogue (one query row per thread). Two TMEM slots of
+// (S 128 columns, O D columns), two (Q, K, V) shared-memory stages.
+//
+// Backward roles: same split. Per unit: dP = dO V^T and S = Q K^T (query
+// rows on TMEM lanes); the compute warps form P, Di, dS and write P and dS as
+// bf16 [query][key] tiles to shared memory; then dV = P^T dO, dK = dS^T Q
+// (P^T, dS^T read MN-major) and dQ = dS K (dS read K-major) are fresh
+// products in TMEM. Input tiles go through a 5-slot ring loaded in the order
+// they are released (V after dP, dO after dV, Q after dK, K after dQ), so
+// the next unit's loads start while this unit computes.
+#include <cuda_bf16.h>
+
 #include "kernels.h"
+#include "sm103.cuh"
+
 namespace jfa {
-cudaError_t launch_blockdiag_fwd(const BlockdiagParams &, int, int, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_blockdiag_bwd(const BlockdiagParams &, int, int, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace dev;
+
+struct Unit {
+  int h, row0, nrows;
+};
+
+__device__ __forceinline__ Unit unit_of(int u, int H, int64_t rows) {
+  Unit x;
+  const int tile = u / H;
+  x.h = u - tile * H;
+  x.row0 = tile * 128;
+  x.nrows = (int)min((int64_t)128, rows - x.row0);
+  return x;
 }
+
+// ======================================================================= forward
+
+template <int D>
+struct FCfg {
+  static constexpr int TILE = 128 * D * 2;
+  static constexpr int NSTAGE = D == 128 ? 2 : 4;
+  static constexpr int OFF_STAGE = 0;
+  static constexpr int OFF_BAR = NSTAGE * 3 * TILE;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_O = idesc_bf16(128, D, 0, 1);
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct FBars {
+  uint64_t full[4], empty[4];
+  uint64_t s_full[2], p_ready[2], o_full[2], slot_free[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_constant__ BlockdiagParams p) {
+  using C = FCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  FBars &bars = *reinterpret_cast<FBars *>(smem + C::OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(&bars.full[s], 1);
+      mbar_init(&bars.empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars.s_full[x], 1);
+      mbar_init(&bars.p_ready[x], 4);
+      mbar_init(&bars.o_full[x], 1);
+      mbar_init(&bars.slot_free[x], 4);
+    }
+    mbar_init(&bars.drain, 1);
+    bars.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+  }
+  if (warp == 2) tmem_alloc(&bars.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const WaitCtl ctl{p.status, &bars.abort_flag, p.timeout_ns};
+  const int n_units = (int)((p.rows + 127) / 128) * p.H;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t eph[4] = {0, 0, 0, 0};
+      int n = 0;
+      for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
+        const Unit x = unit_of(u, p.H, p.rows);
+        const int s = n % C::NSTAGE;
+        if (!mbar_wait(&bars.empty[s], eph[s] ^ 1, ctl, 1)) goto done;
+        eph[s] ^= 1;
+        mbar_arrive_expect_tx(&bars.full[s], 3 * C::TILE);
+        uint8_t *st = smem + C::OFF_STAGE + s * 3 * C::TILE;
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(st + c * 16384, &p.tm_q, &bars.full[s], c * 64, x.h, x.row0);
+          tma_load_3d(st + C::TILE + c * 16384, &p.tm_k, &bars.full[s], c * 64, x.h, x.row0);
+          tma_load_3d(st + 2 * C::TILE + c * 16384, &p.tm_v, &bars.full[s], c * 64, x.h, x.row0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t fph[4] = {0, 0, 0, 0}, pph[2] = {0, 0}, fr[2] = {0, 0};
+      const uint32_t st0 = smem_u32(smem + C::OFF_STAGE);
+      int n = 0;
+      int prev_stage = -1;
+      for (int u = blockIdx.x;; u += gridDim.x, ++n) {
+        const bool have = u < n_units;
+        if (have) {
+          const int s = n % C::NSTAGE, ts = n & 1;
+          if (!mbar_wait(&bars.full[s], fph[s], ctl, 10)) goto done;
+          fph[s] ^= 1;
+          if (!mbar_wait(&bars.slot_free[ts], fr[ts] ^ 1, ctl, 11)) goto done;
+          fr[ts] ^= 1;
+          tc_fence_after();
+          const uint32_t qa = st0 + s * 3 * C::TILE, ka = qa + C::TILE;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+            mma_ss(tmem + ts * 256, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                   C::IDESC_S, k > 0);
+          }
+          mma_commit(&bars.s_full[ts]);
+        }
+        if (n > 0) {  // O = P V for the previous unit
+          const int pn = n - 1, ts = pn & 1;
+          if (!mbar_wait(&bars.p_ready[ts], pph[ts], ctl, 12)) goto done;
+          pph[ts] ^= 1;
+          tc_fence_after();
+          const uint32_t va = st0 + prev_stage * 3 * C::TILE + 2 * C::TILE;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + ts * 256 + 128, tmem + ts * 256 + k * 8,
+                   sdesc_sw128(va + k * 2048, 16384, 1024), C::IDESC_O, k > 0);
+          mma_commit(&bars.o_full[ts]);
+          mma_commit(&bars.empty[prev_stage]);
+        }
+        if (!have) break;
+        prev_stage = n % C::NSTAGE;
+      }
+    }
+  } else if (warp >= 4) {
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int blk = wq >> 1;  // rows 0-63 -> key block 0, rows 64-127 -> key block 1
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t sph[2] = {0, 0}, oph[2] = {0, 0};
+    float l_prev = 1.f;
+    Unit x_prev{0, 0, 0};
+    int n = 0;
+    __nv_bfloat16 *obase = static_cast<__nv_bfloat16 *>(p.o);
+    for (int u = blockIdx.x;; u += gridDim.x, ++n) {
+      const bool have = u < n_units;
+      float l_cur = 1.f;
+      if (have) {  // softmax of unit n
+        const int ts = n & 1;
+        if (!mbar_wait(&bars.s_full[ts], sph[ts], ctl, 20)) goto done;
+        sph[ts] ^= 1;
+        tc_fence_after();
+        const uint32_t tS = tmem + lane_off + ts * 256;
+        uint32_t a[32], b[32];
+        tmem_ld32(tS + blk * 64, a);
+        tmem_ld32(tS + blk * 64 + 32, b);
+        tmem_wait_ld();
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(__uint_as_float(a[i]), __uint_as_float(b[i])));
+        const float mo = mx * sl2;
+        float sum0 = 0.f, sum1 = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(__uint_as_float(a[2 * i]), sl2, -mo));
+          const float p1 = ex2(fmaf(__uint_as_float(a[2 * i + 1]), sl2, -mo));
+          const float q0 = ex2(fmaf(__uint_as_float(b[2 * i]), sl2, -mo));
+          const float q1 = ex2(fmaf(__uint_as_float(b[2 * i + 1]), sl2, -mo));
+          sum0 += p0 + p1;
+          sum1 += q0 + q1;
+          pk[i] = pack_bf16(p0, p1);
+          pk[16 + i] = pack_bf16(q0, q1);
+        }
+        l_cur = sum0 + sum1;
+        uint32_t zero[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) zero[i] = 0u;
+        // P occupies columns [0, 64) as bf16 pairs: keys 0-63 in [0,32), 64-127 in [32,64).
+        tmem_st32(tS + blk * 32, pk);
+        tmem_st32(tS + (1 - blk) * 32, zero);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_ready[ts]);
+      }
+      if (n > 0) {  // epilogue of unit n-1
+        const int ts = (n - 1) & 1;
+        if (!mbar_wait(&bars.o_full[ts], oph[ts], ctl, 21)) goto done;
+        oph[ts] ^= 1;
+        tc_fence_after();
+        const uint32_t tO = tmem + lane_off + ts * 256 + 128;
+        const bool row_ok = r < x_prev.nrows;
+        uint4 *optr = reinterpret_cast<uint4 *>(obase + ((int64_t)(x_prev.row0 + r) * p.H + x_prev.h) * D);
+        const float inv_l = 1.f / l_prev;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
+          if (row_ok) {
+            uint32_t q[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              q[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) optr[c * 4 + i] = make_uint4(q[4 * i], q[4 * i + 1], q[4 * i + 2], q[4 * i + 3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.slot_free[ts]);
+      }
+      if (!have) break;
+      l_prev = l_cur;
+      x_prev = unit_of(u, p.H, p.rows);
+    }
+  }
+done:
+  if (warp == 1 && lane == 0 && bars.abort_flag) {
+    mma_commit(&bars.drain);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&bars.drain, 0) && globaltimer() - t0 < p.timeout_ns) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ====================================================================== backward
+
+template <int D>
+struct BCfg {
+  static constexpr int TILE = 128 * D * 2;
+  static constexpr int NSLOT = D == 128 ? 5 : 8;
+  static constexpr int OFF_RING = 0;
+  static constexpr int OFF_P = NSLOT * TILE;  // bf16 [128 q][128 k] as two 64-key chunks
+  static constexpr int OFF_DS = OFF_P + 32768;
+  static constexpr int OFF_BAR = OFF_DS + 32768;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, 0, 0);   // S, dP
+  static constexpr uint32_t IDESC_T = idesc_bf16(128, D, 1, 1);     // dV, dK: A MN-major
+  static constexpr uint32_t IDESC_Q = idesc_bf16(128, D, 0, 1);     // dQ: A K-major
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+// TMEM columns: S [0,128) then dV; dP [128,256) then dK; dQ [256, 256+D).
+enum : uint32_t { BC_S = 0, BC_DP = 128, BC_DQ = 256 };
+enum { T_V = 0, T_DO = 1, T_Q = 2, T_K = 3 };  // ring load order = release order
+
+struct BBars {
+  uint64_t full[8], empty[8];
+  uint64_t s_full, dp_full, ps_ready, ps_free, g_full, g_free;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_constant__ BlockdiagParams p) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  BBars &bars = *reinterpret_cast<BBars *>(smem + C::OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(&bars.full[s], 1);
+      mbar_init(&bars.empty[s], 1);
+    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.ps_ready, 4);
+    mbar_init(&bars.ps_free, 1);
+    mbar_init(&bars.g_full, 1);
+    mbar_init(&bars.g_free, 4);
+    mbar_init(&bars.drain, 1);
+    bars.abort_flag = 0;
+    fence_mbar_init();
+  }
+  {  // P and dS tiles start at zero; each row only ever rewrites its own key block.
+    uint4 *z = reinterpret_cast<uint4 *>(smem + C::OFF_P);
+    for (int i = threadIdx.x; i < 65536 / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+    fence_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+    prefetch_tmap(&p.tm_do);
+  }
+  if (warp == 2) tmem_alloc(&bars.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const WaitCtl ctl{p.status, &bars.abort_flag, p.timeout_ns};
+  const int n_units = (int)((p.rows + 127) / 128) * p.H;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t eph[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      int slot = 0;
+      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit x = unit_of(u, p.H, p.rows);
+        for (int t = 0; t < 4; ++t) {
+          if (!mbar_wait(&bars.empty[slot], eph[slot] ^ 1, ctl, 1)) goto done;
+          eph[slot] ^= 1;
+          mbar_arrive_expect_tx(&bars.full[slot], C::TILE);
+          const CUtensorMap *m = t == T_V ? &p.tm_v : t == T_DO ? &p.tm_do : t == T_Q ? &p.tm_q : &p.tm_k;
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::OFF_RING + slot * C::TILE + c * 16384, m, &bars.full[slot], c * 64,
+                        x.h, x.row0);
+          if (++slot == C::NSLOT) slot = 0;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t fph[8] = {0, 0, 0, 0, 0, 0, 0, 0}, psr = 0, psf = 0, gf = 0;
+      const uint32_t ring = smem_u32(smem + C::OFF_RING);
+      const uint32_t pa = smem_u32(smem + C::OFF_P), dsa = smem_u32(smem + C::OFF_DS);
+      int slot = 0;
+      auto sl = [&](int t) { int s = slot + t; return s >= C::NSLOT ? s - C::NSLOT : s; };
+      auto ta = [&](int t) { return ring + sl(t) * C::TILE; };
+      auto wait_full = [&](int t) -> bool {
+        const int s = sl(t);
+        if (!mbar_wait(&bars.full[s], fph[s], ctl, 10 + t)) return false;
+        fph[s] ^= 1;
+        return true;
+      };
+      auto xyT = [&](uint32_t dcol, uint32_t xa, uint32_t ya) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tmem + dcol, sdesc_sw128(xa + off, 16, 1024), sdesc_sw128(ya + off, 16, 1024),
+                 C::IDESC_S, k > 0);
+        }
+      };
+      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        if (!mbar_wait(&bars.g_free, gf ^ 1, ctl, 20)) goto done;  // previous epilogue drained TMEM
+        gf ^= 1;
+        if (!wait_full(T_V) || !wait_full(T_DO)) goto done;
+        tc_fence_after();
+        xyT(BC_DP, ta(T_DO), ta(T_V));  // dP = dO V^T
+        mma_commit(&bars.dp_full);
+        mma_commit(&bars.empty[sl(T_V)]);
+        if (!wait_full(T_Q) || !wait_full(T_K)) goto done;
+        tc_fence_after();
+        xyT(BC_S, ta(T_Q), ta(T_K));  // S = Q K^T
+        mma_commit(&bars.s_full);
+        if (!mbar_wait(&bars.ps_ready, psr, ctl, 21)) goto done;
+        psr ^= 1;
+        tc_fence_after();
+        // dV = P^T dO  (A = P^T: MN-major view of the [q][k] tile; B = dO MN-major)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tmem + BC_S, sdesc_sw128(pa + k * 2048, 16384, 1024),
+                 sdesc_sw128(ta(T_DO) + k * 2048, 16384, 1024), C::IDESC_T, k > 0);
+        mma_commit(&bars.empty[sl(T_DO)]);
+        // dK = dS^T Q
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tmem + BC_DP, sdesc_sw128(dsa + k * 2048, 16384, 1024),
+                 sdesc_sw128(ta(T_Q) + k * 2048, 16384, 1024), C::IDESC_T, k > 0);
+        mma_commit(&bars.empty[sl(T_Q)]);
+        // dQ = dS K  (A = dS K-major; B = K MN-major)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tmem + BC_DQ, sdesc_sw128(dsa + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                 sdesc_sw128(ta(T_K) + k * 2048, 16384, 1024), C::IDESC_Q, k > 0);
+        mma_commit(&bars.empty[sl(T_K)]);
+        mma_commit(&bars.g_full);
+        mma_commit(&bars.ps_free);
+        slot = sl(4);
+        (void)psf;
+      }
+    }
+  } else if (warp >= 4) {
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int blk = wq >> 1;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t sph = 0, dpph = 0, psf = 0, gph = 0;
+    uint8_t *prow = smem + C::OFF_P + blk * 16384 + r * 128;
+    uint8_t *dsrow = smem + C::OFF_DS + blk * 16384 + r * 128;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const Unit x = unit_of(u, p.H, p.rows);
+      if (!mbar_wait(&bars.s_full, sph, ctl, 30)) goto done;
+      sph ^= 1;
+      if (!mbar_wait(&bars.dp_full, dpph, ctl, 31)) goto done;
+      dpph ^= 1;
+      tc_fence_after();
+      float pr[64];
+      float di = 0.f;
+      {
+        uint32_t a[32], b[32];
+        tmem_ld32(tmem + lane_off + BC_S + blk * 64, a);
+        tmem_ld32(tmem + lane_off + BC_S + blk * 64 + 32, b);
+        tmem_wait_ld();
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(__uint_as_float(a[i]), __uint_as_float(b[i])));
+        const float mo = mx * sl2;
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          pr[i] = ex2(fmaf(__uint_as_float(a[i]), sl2, -mo));
+          pr[32 + i] = ex2(fmaf(__uint_as_float(b[i]), sl2, -mo));
+          sum += pr[i] + pr[32 + i];
+        }
+        const float inv = 1.f / sum;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) pr[i] *= inv;
+      }
+      {
+        uint32_t a[32], b[32];
+        tmem_ld32(tmem + lane_off + BC_DP + blk * 64, a);
+        tmem_ld32(tmem + lane_off + BC_DP + blk * 64 + 32, b);
+        tmem_wait_ld();
+        float dp[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          dp[i] = __uint_as_float(a[i]);
+          dp[32 + i] = __uint_as_float(b[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 64; ++i) di = fmaf(pr[i], dp[i], di);  // Di = rowsum(P * dP)
+        if (!mbar_wait(&bars.ps_free, psf ^ 1, ctl, 32)) goto done;
+        psf ^= 1;
+        uint32_t pk[32], dk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          pk[i] = pack_bf16(pr[2 * i], pr[2 * i + 1]);
+          dk[i] = pack_bf16(pr[2 * i] * (dp[2 * i] - di), pr[2 * i + 1] * (dp[2 * i + 1] - di));
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int off = (j ^ (r & 7)) << 4;
+          *reinterpret_cast<uint4 *>(prow + off) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          *reinterpret_cast<uint4 *>(dsrow + off) = make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
+        }
+        fence_async_smem();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.ps_ready);
+      // epilogue: dQ (query row r), dV and dK (key row r)
+      if (!mbar_wait(&bars.g_full, gph, ctl, 33)) goto done;
+      gph ^= 1;
+      tc_fence_after();
+      {
+        const bool row_ok = r < x.nrows;
+        const int64_t g = ((int64_t)(x.row0 + r) * p.H + x.h) * D;
+#pragma unroll 1
+        for (int which = 0; which < 3; ++which) {
+          const uint32_t col = which == 0 ? BC_DQ : which == 1 ? BC_S : BC_DP;
+          const float mul = which == 1 ? 1.f : p.scale;
+          __nv_bfloat16 *base = static_cast<__nv_bfloat16 *>(which == 0 ? p.dq : which == 1 ? p.dv : p.dk);
+          uint4 *dst = reinterpret_cast<uint4 *>(base + g);
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + col + c * 32, v);
+            tmem_wait_ld();
+            if (row_ok) {
+              uint32_t q[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                q[i] = pack_bf16(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[c * 4 + i] = make_uint4(q[4 * i], q[4 * i + 1], q[4 * i + 2], q[4 * i + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.g_free);
+    }
+  }
+done:
+  if (warp == 1 && lane == 0 && bars.abort_flag) {
+    mma_commit(&bars.drain);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&bars.drain, 0) && globaltimer() - t0 < p.timeout_ns) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <typename K>
+cudaError_t launch_k(K kern, int smem, const BlockdiagParams &p, int num_sms, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int n_units = (int)((p.rows + 127) / 128) * p.H;
+  const int grid = n_units < num_sms ? n_units : num_sms;
+  kern<<<grid, 256, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_blockdiag_fwd(const BlockdiagParams &p, int D, int num_sms, cudaStream_t st) {
+  if (D == 128) return launch_k(blockdiag_fwd_kernel<128>, FCfg<128>::SMEM, p, num_sms, st);
+  return launch_k(blockdiag_fwd_kernel<64>, FCfg<64>::SMEM, p, num_sms, st);
+}
+
+cudaError_t launch_blockdiag_bwd(const BlockdiagParams &p, int D, int num_sms, cudaStream_t st) {
+  if (D == 128) return launch_k(blockdiag_bwd_kernel<128>, BCfg<128>::SMEM, p, num_sms, st);
+  return launch_k(blockdiag_bwd_kernel<64>, BCfg<64>::SMEM, p, num_sms, st);
+}
+
+}  // namespace jfa

@@ -26,8 +26,9 @@
 // The dQ group reads dQ^T out of TMEM (one head-dim lane per thread),
 // releases the TMEM at once, scales, stages 32x32 fp32 boxes in shared
 // memory (two buffers per warp) and adds them into an fp32 accumulator in
-// global memory with TMA reduce-add. A light kernel converts the
-// accumulator to bf16 at the end.
+// global memory with TMA reduce-add: a workspace accumulator that a light
+// kernel casts to bf16 at the end (jagged), or the caller's fp32 dQ itself
+// (broadcast-Q, where dQ is a sum over the whole batch).
 //
 // Roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
 // warps 4-7 compute + dK/dV epilogue, warps 8-11 dQ reduction.
@@ -484,7 +485,7 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add_3d(&p.tm_dqacc, buf, wq * 32, tl.q_row0 + i * 64 + qc * 32, tl.h);
+            tma_reduce_add_3d(&p.tm_dqacc, buf, wq * 32, tl.h, tl.q_row0 + i * 64 + qc * 32);
             bulk_commit();
           }
           last_buf = qc;
@@ -519,25 +520,13 @@ cudaError_t launch_t(const BwdParams &p, int num_sms, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// fp32 [H, rows, D] -> bf16 [rows, H, D]; 8 elements per thread.
-__global__ void dq_convert_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq,
-                                  int64_t rows, int H, int D) {
-  const int64_t n8 = rows * H * D / 8;
+// fp32 [rows, H, D] -> bf16 [rows, H, D]; 8 elements per thread.
+__global__ void dq_convert_kernel(const float4 *__restrict__ acc, uint4 *__restrict__ dq, int64_t n8) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t e = i * 8;  // element index in [rows, H, D]
-    const int d = (int)(e % D);
-    const int64_t rh = e / D;
-    const int h = (int)(rh % H);
-    const int64_t row = rh / H;
-    const float4 *src = reinterpret_cast<const float4 *>(acc + ((int64_t)h * rows + row) * D + d);
-    const float4 a = src[0], b = src[1];
-    uint4 o;
-    o.x = pack_bf16(a.x, a.y);
-    o.y = pack_bf16(a.z, a.w);
-    o.z = pack_bf16(b.x, b.y);
-    o.w = pack_bf16(b.z, b.w);
-    *reinterpret_cast<uint4 *>(dq + e) = o;
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    dq[i] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
+                       pack_bf16(b.z, b.w));
   }
 }
 
@@ -558,7 +547,8 @@ cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, i
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t want = (n8 + 255) / 256;
   const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
-  dq_convert_kernel<<<grid, 256, 0, st>>>(acc, static_cast<__nv_bfloat16 *>(dq), rows, H, D);
+  dq_convert_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4 *>(acc),
+                                          static_cast<uint4 *>(dq), n8);
   return cudaGetLastError();
 }
 

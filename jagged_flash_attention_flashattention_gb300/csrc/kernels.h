@@ -38,7 +38,7 @@ struct BwdParams {
   CUtensorMap tm_o;   // bf16 O rows, box {64, 1, 64}
   CUtensorMap tm_k;   // bf16 [Tk, H, D], box {64, 1, 128}
   CUtensorMap tm_v;
-  CUtensorMap tm_dqacc;  // fp32 [H, rows, D] as {D, rows, H}, box {32, 32, 1}, no swizzle
+  CUtensorMap tm_dqacc;  // fp32 [rows, H, D] as {D, H, rows}, box {32, 1, 32}, no swizzle
   const void *offsets;
   int idx64;
   const int32_t *sm_ptr;
@@ -57,7 +57,7 @@ struct BwdParams {
 
 cudaError_t launch_bwd(const BwdParams &p, int D, int num_sms, cudaStream_t st);
 
-// fp32 [H, rows, D] accumulator -> bf16 [rows, H, D]
+// fp32 [rows, H, D] accumulator -> bf16 [rows, H, D]
 cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, int D,
                               cudaStream_t st);
 

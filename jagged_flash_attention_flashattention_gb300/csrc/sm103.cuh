@@ -86,7 +86,7 @@ struct WaitCtl {
 
 enum : uint32_t { kErrTimeout = 5 };
 
-__device__ __noinline__ void report_timeout(const WaitCtl &c, int site) {
+static __device__ __noinline__ void report_timeout(const WaitCtl &c, int site) {
   if (atomicCAS(c.status, 0u, (uint32_t)kErrTimeout) == 0u) {
     c.status[1] = (uint32_t)site;
     c.status[2] = blockIdx.x;

@@ -5,6 +5,13 @@ O, dQ, dK, dV: max-abs error <= 2e-2 and relative L2 error <= 1e-2 against
 the fp64 oracle on the same bf16 inputs. LSE (fp32 output): max-abs error
 <= 1e-3; it is a log of a sum of exponentials of fp32 scores computed from
 exact bf16 products, so its error is a few ulp of fp32 times |S|.
+
+Edge-case shapes (not the five workload configurations) can produce outputs
+far above 1 in magnitude, e.g. dV of a one-key sequence is the sum of every
+query's dO. A bf16 output cannot be closer to the exact value than half a
+bf16 ulp, up to 2^-8 |x|, which exceeds 2e-2 once |x| >= 8. Those tests pass
+``bf16_out=True``, which adds exactly that rounding bound per element to the
+absolute tolerance; the configuration tests keep the plain bounds.
 """
 
 import numpy as np
@@ -21,11 +28,16 @@ def f64(t):
     return np.asarray(t, dtype=np.float64)
 
 
-def assert_close(got, ref, name, atol=ATOL, rl2=RL2):
+BF16_HALF_ULP = 2.0 ** -8
+
+
+def assert_close(got, ref, name, atol=ATOL, rl2=RL2, bf16_out=False):
     got, ref = f64(got), f64(ref)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), "%s has non-finite values" % name
     err = np.abs(got - ref)
+    if bf16_out:
+        err = np.maximum(err - BF16_HALF_ULP * np.abs(ref), 0.0)
     mx = float(err.max()) if err.size else 0.0
     den = float(np.linalg.norm(ref))
     rel = float(np.linalg.norm(got - ref)) / den if den > 0 else float(np.linalg.norm(got))
