@@ -161,7 +161,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def _setup(name, rank, dev):
+def _setup(name, rank, dev, seqs=0):
     """Inputs and one hot-path step for a named workload. Returns a dict."""
     import torch
 
@@ -173,6 +173,8 @@ def _setup(name, rank, dev):
     st = {"H": H, "D": D, "kind": cfg["kind"]}
     if cfg["kind"] == "jagged":
         L = _gem_lengths(rank) if name == "gem" else W.lengths_for(name)
+        if seqs:
+            L = L[:seqs]
         off_host = W.offsets_of(L, cfg["offsets_dtype"])
         inp = W.jagged_inputs(L, H, D, W.SEEDS[name] + 1000 * rank, device=dev)
         off = torch.from_numpy(off_host).to(dev)
@@ -241,7 +243,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     hbm_peak, tc_peak, tc_sust, peak_src = _peaks()
 
-    st = _setup(args.config, rank, dev)
+    st = _setup(args.config, rank, dev, args.seqs)
     fwd_flops, bwd_flops = st["fwd_flops"], st["bwd_flops"]
     stream = torch.cuda.current_stream()
 
@@ -289,7 +291,7 @@ def run_ours(args):
     value = ws * (fwd_flops + bwd_flops) / (ms_per_step * 1e-3) / 1e12
 
     e2e = None
-    if args.config == "gem":
+    if args.config == "gem" and not args.seqs:
         e2e = _e2e_gem(args, st, dev, ws)
 
     if rank == 0:
@@ -390,6 +392,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="jagged workloads: keep only the first N sequences (small profiling case)")
     ap.add_argument("--config", default="gem",
                     choices=["gem", "stress", "bcast", "blockdiag", "blockdiag64", "tiny"])
     args = ap.parse_args()
