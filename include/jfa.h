@@ -165,6 +165,31 @@ jfa_status jfa_bwd(const void *q, const void *k, const void *v, const void *o,
                    const int32_t *d_tiles, int num_sms, void *dq, void *dk, void *dv,
                    void *workspace, size_t ws_bytes, jfa_stream_t stream);
 
+/* jfa_bwd without a workspace argument. The paper has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory when
+ * they call, such as a plug-in inside a framework that owns all device memory
+ * through its own pool, or a latency-critical path that may not call
+ * cudaMalloc (which can synchronise the device). Inputs and outputs are as
+ * for jfa_bwd and are still the caller's; the scratch jfa_bwd would keep in
+ * its workspace (a 256-byte status block and an fp32 [T, H, D] dQ
+ * accumulator) lives instead in one static device array of 64 MiB per
+ * device, which stays allocated until the process exits on every device
+ * that has loaded it. Limit: T * H * D <= 16,777,152; larger problems return
+ * JFA_ERR_WORKSPACE with a message and launch nothing. The library
+ * allocates and frees nothing here. The first call on each device looks up
+ * the array's device address with that device current; make that first call
+ * before any stream capture. Every call on a device shares the one array
+ * (each call clears what must start at zero), so calls whose work overlaps
+ * on the GPU, e.g. on two streams, race and give wrong results: serialise
+ * them. A kernel timeout is not reported by this variant (its status block
+ * is cleared at every call); use jfa_bwd and jfa_check_status when that is
+ * needed. */
+jfa_status jfa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                           const float *lse, const void *dout, const void *offsets,
+                           jfa_index_t idx, int64_t B, int64_t T, int H, int D, float scale,
+                           const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_sms,
+                           void *dq, void *dk, void *dv, jfa_stream_t stream);
+
 /* Broadcast-Q forward: q device bf16 [Lq, H, D] is shared by every
  * sequence of k, v (device bf16 [Tk, H, D], boundaries kv_offsets [B+1]).
  * o: device bf16 [B, Lq, H, D]; lse: device fp32 [B, H, Lq]. A sequence of

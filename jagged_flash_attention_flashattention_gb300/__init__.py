@@ -38,6 +38,7 @@ EXPORTS = [
     "jfa_status_str", "jfa_last_error", "jfa_sched_size", "jfa_sched_build", "jfa_tile_rows",
     "jfa_num_sms", "jfa_workspace_size", "jfa_workspace_init", "jfa_check_status", "jfa_fwd",
     "jfa_bwd", "jfa_bcastq_fwd", "jfa_bcastq_bwd", "blockdiag_fwd", "blockdiag_bwd",
+    "jfa_bwd_noalloc",
 ]
 
 
@@ -77,6 +78,7 @@ def lib():
                             SZ, P], I),
         "blockdiag_fwd": ([P, P, P, I64, I64, I, I, F, P, P, SZ, P], I),
         "blockdiag_bwd": ([P, P, P, P, I64, I64, I, I, F, P, P, P, P, SZ, P], I),
+        "jfa_bwd_noalloc": ([P, P, P, P, P, P, P, I, I64, I64, I, I, F, P, P, I, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
