@@ -1,0 +1,134 @@
+"""CPU tests of the C ABI: the library loads, exports every symbol that
+include/jfa.h declares, rejects bad arguments on the host without touching a
+device, and its host scheduler matches the scheduler oracle exactly."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import jagged_flash_attention_flashattention_gb300 as jfa
+from jagged_flash_attention_flashattention_gb300 import workloads as W
+from oracle import sched as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(jfa.LIB_PATH):
+        from jagged_flash_attention_flashattention_gb300 import build
+
+        build.build()
+    return jfa.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "jfa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:jfa_status|size_t|const char \*)\s*\**\s*(\w+)\(", src,
+                                 flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 16, names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(jfa.EXPORTS)
+
+
+def test_status_strings(L):
+    assert L.jfa_status_str(0) == b"JFA_OK"
+    assert L.jfa_status_str(5) == b"JFA_ERR_TIMEOUT"
+
+
+def _null():
+    return ctypes.c_void_p(0)
+
+
+def test_fwd_rejects_unsupported_head_dim(L):
+    dummy = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(dummy, ctypes.c_void_p)
+    code = L.jfa_fwd(p, p, p, p, 0, 1, 10, 2, 96, 0.1, p, p, 1, p, p, p, 256, _null())
+    assert code == 2 and b"D = 96" in L.jfa_last_error()
+
+
+def test_fwd_rejects_missing_workspace(L):
+    dummy = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(dummy, ctypes.c_void_p)
+    assert L.jfa_fwd(p, p, p, p, 0, 1, 10, 2, 64, 0.1, p, p, 1, p, p, _null(), 256, _null()) == 3
+    assert L.jfa_fwd(p, p, p, p, 0, 1, 10, 2, 64, 0.1, p, p, 1, p, p, p, 16, _null()) == 3
+
+
+def test_fwd_rejects_bad_scale_and_index_type(L):
+    dummy = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(dummy, ctypes.c_void_p)
+    assert L.jfa_fwd(p, p, p, p, 0, 1, 10, 2, 64, -1.0, p, p, 1, p, p, p, 256, _null()) == 1
+    assert L.jfa_fwd(p, p, p, p, 7, 1, 10, 2, 64, 0.1, p, p, 1, p, p, p, 256, _null()) == 1
+
+
+def test_bwd_rejects_small_workspace(L):
+    dummy = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(dummy, ctypes.c_void_p)
+    need = L.jfa_workspace_size(jfa.OP_BWD, 1000, 2, 64)
+    assert need == 256 + 1000 * 2 * 64 * 4
+    code = L.jfa_bwd(p, p, p, p, p, p, p, 0, 1, 1000, 2, 64, 0.1, p, p, 1, p, p, p, p, need - 1,
+                     _null())
+    assert code == 3
+
+
+def test_blockdiag_rejects_length_not_multiple_of_64(L):
+    dummy = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(dummy, ctypes.c_void_p)
+    assert L.blockdiag_fwd(p, p, p, 2, 100, 2, 64, 0.1, p, p, 256, _null()) == 1
+    assert b"multiple of 64" in L.jfa_last_error()
+
+
+def test_tile_rows(L):
+    assert jfa.tile_rows(jfa.OP_FWD, 128) == 256
+    assert jfa.tile_rows(jfa.OP_BWD, 64) == 128
+
+
+def test_sched_rejects_bad_offsets(L):
+    off = np.array([0, 5, 3], dtype=np.int64)
+    with pytest.raises(jfa.JFAError):
+        jfa.schedule(off, 2, 128, 4)
+    off = np.array([1, 5], dtype=np.int64)
+    with pytest.raises(jfa.JFAError):
+        jfa.schedule(off, 2, 128, 4)
+
+
+@pytest.mark.parametrize("name,tile_rows,sms", [("tiny", 256, 3), ("gem", 256, 152),
+                                                ("gem", 128, 148), ("stress", 128, 152),
+                                                ("stress", 256, 7)])
+def test_c_scheduler_matches_oracle(L, name, tile_rows, sms):
+    lengths = W.lengths_for(name)
+    H = W.WORKLOADS[name]["H"]
+    for zz in (True, False):
+        sp, tl = jfa.schedule(W.offsets_of(lengths), H, tile_rows, sms, zigzag=zz)
+        rp, rt = S.schedule(list(lengths), H, tile_rows, sms, zigzag=zz)
+        assert sp.tolist() == rp
+        assert [tuple(t) for t in tl.tolist()] == rt
+
+
+def test_c_scheduler_matches_oracle_bcast(L):
+    lengths = W.lengths_for("bcast")
+    off = W.offsets_of(lengths)
+    sp, tl = jfa.schedule(off, 4, 256, 152, fixed_rows=256)
+    rp, rt = S.schedule(list(lengths), 4, 256, 152, fixed_rows=256)
+    assert sp.tolist() == rp and [tuple(t) for t in tl.tolist()] == rt
+    sp, tl = jfa.schedule(off, 4, 128, 152, fixed_work=256)
+    rp, rt = S.schedule(list(lengths), 4, 128, 152, fixed_work=256)
+    assert sp.tolist() == rp and [tuple(t) for t in tl.tolist()] == rt
+
+
+def test_c_scheduler_int32_offsets_and_empty(L):
+    off = np.array([0, 0, 3, 3, 200], dtype=np.int32)
+    sp, tl = jfa.schedule(off, 2, 64, 5)
+    rp, rt = S.schedule([0, 3, 0, 197], 2, 64, 5)
+    assert sp.tolist() == rp and [tuple(t) for t in tl.tolist()] == rt
+    sp, tl = jfa.schedule(np.array([0], dtype=np.int64), 2, 64, 5)
+    assert sp.tolist() == [0] * 6 and tl.shape[0] == 0
