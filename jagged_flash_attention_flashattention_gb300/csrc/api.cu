@@ -283,7 +283,6 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   const int64_t o_rows = Lq > 0 ? B * Lq : q_rows;
   JFA_TRY(map_rows_bf16(&p.tm_q, q, acc_rows, H, D, 64));
   JFA_TRY(map_rows_bf16(&p.tm_do, dout, o_rows, H, D, 64));
-  JFA_TRY(map_rows_bf16(&p.tm_o, o, o_rows, H, D, 64));
   JFA_TRY(map_rows_bf16(&p.tm_k, k, Tk > 0 ? Tk : 1, H, D, 128));
   JFA_TRY(map_rows_bf16(&p.tm_v, v, Tk > 0 ? Tk : 1, H, D, 128));
   JFA_TRY(map_acc_f32(&p.tm_dqacc, acc, acc_rows, H, D));
@@ -292,6 +291,7 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   p.sm_ptr = sm_ptr;
   p.tiles = tiles;
   p.lse = lse;
+  p.o = o;
   p.dk = dk;
   p.dv = dv;
   p.T = Lq > 0 ? Tk : q_rows;

@@ -14,12 +14,14 @@
 //
 // A tile is 128 key rows of one (sequence, head). dK and dV for those rows
 // stay in tensor memory while the kernel walks every 64-row query block of
-// the sequence (or the dense Q for broadcast-Q). Per query block:
+// the sequence (or the dense Q for broadcast-Q); Q and dO blocks stream
+// through a 4-deep ring of shared-memory stages. Per query block:
 //   S^T  = K Q^T        (M=128 keys, N=64 queries, K=D)      -> TMEM
 //   dP^T = V dO^T                                            -> TMEM
 //   P^T, dS^T computed by the compute warps (one key row per thread);
-//   Di for the block's 64 query rows is formed inline from the O and dO
-//   tiles already in shared memory (no separate pass);
+//   LSE and Di = rowsum(dO * O) of the block's 64 query rows are formed
+//   inline, one block ahead, by the dQ warps (O rows read from global
+//   memory, dO from the stage; no separate pass);
 //   dV  += P^T dO       (A = P^T bf16 from TMEM)
 //   dK  += dS^T Q       (A = dS^T bf16 from TMEM)
 //   dQ^T = K^T dS^T     (both operands MN-major in shared memory)  -> TMEM
@@ -31,7 +33,8 @@
 // (broadcast-Q, where dQ is a sum over the whole batch).
 //
 // Roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
-// warps 4-7 compute + dK/dV epilogue, warps 8-11 dQ reduction.
+// warps 4-7 compute + dK/dV epilogue, warps 8-11 LSE/Di staging + dQ
+// reduction.
 // Tensor memory columns: dV [0,128) dK [128,256) S/P [256,320)
 // dP/dS [320,384) dQ^T [384,448).
 #include <cuda_bf16.h>
@@ -47,20 +50,20 @@ using namespace dev;
 template <int D>
 struct BwdCfg {
   static constexpr int KV_TILE = 128 * D * 2;  // 128-row K or V tile
-  static constexpr int QT = 64 * D * 2;        // 64-row Q, dO or O tile
+  static constexpr int QT = 64 * D * 2;        // 64-row Q or dO tile
   static constexpr int QCHUNK = 64 * 128;      // one 64-column box of a 64-row tile
-  static constexpr int NSTAGE = 2;
+  static constexpr int NSTAGE = D == 128 ? 4 : 8;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_TILE;
   static constexpr int OFF_ZERO = 2 * KV_TILE;  // D = 64: zero rows padding K^T to M = 128
   static constexpr int ZERO_BYTES = D == 64 ? 16384 : 0;
-  static constexpr int OFF_STAGE = OFF_ZERO + ZERO_BYTES;
-  static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 3 * QT;  // two 128x64 bf16 dS^T buffers
-  static constexpr int OFF_DQS = OFF_DS + 2 * 16384;          // dQ staging: 4 warps x 2 x 4 KB
-  static constexpr int OFF_LSE = OFF_DQS + 4 * 8192;
-  static constexpr int OFF_DI = OFF_LSE + NSTAGE * 256;
+  static constexpr int OFF_STAGE = OFF_ZERO + ZERO_BYTES;  // NSTAGE x (Q, dO)
+  static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 2 * QT;  // 128x64 bf16 dS^T
+  static constexpr int OFF_DQS = OFF_DS + 16384;               // dQ staging: 4 warps x 4 KB
+  static constexpr int OFF_LSE = OFF_DQS + 16384;              // [NSTAGE][64] log2 units
+  static constexpr int OFF_DI = OFF_LSE + NSTAGE * 256;        // [NSTAGE][64]
   static constexpr int OFF_BAR = OFF_DI + NSTAGE * 256;
-  static constexpr int SMEM = OFF_BAR + 512 + 1024;
+  static constexpr int SMEM = OFF_BAR + 512;
   static constexpr uint32_t KT_LBO = D == 128 ? 16384 : (OFF_ZERO - OFF_K);
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 64, 0, 0);
   static constexpr uint32_t IDESC_G = idesc_bf16(128, D, 0, 1);   // dV, dK
@@ -72,9 +75,8 @@ enum : uint32_t { COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 320, COL_DQ = 
 
 struct BwdBars {
   uint64_t kv_full, kv_empty;
-  uint64_t stage_full[2], stage_empty[2];
-  uint64_t s_full, dp_full, p_ready, ds_ready;
-  uint64_t ds_free[2];
+  uint64_t stage_full[8], stage_empty[8], aux_full[8];
+  uint64_t s_full, dp_full, p_ready, ds_ready, ds_free;
   uint64_t dq_full, dq_free;
   uint64_t dkdv_full, dkdv_free;
   uint64_t drain;
@@ -86,7 +88,7 @@ struct BwdTile {
   int b, h, nq, nkv;  // query blocks to walk; valid key rows in this tile
   int kv_row0;        // first key row (tm_k / tm_v / dK / dV)
   int q_row0;         // first query row of the sequence in tm_q and in the dQ accumulator
-  int o_row0;         // first row of the sequence in tm_o / tm_do
+  int o_row0;         // first row of the sequence in O / dO
   int Lq;             // query rows of the sequence
   int64_t lse0;       // LSE index of query row 0 (jagged: + h*T; bcast: (b*H+h)*Lq)
 };
@@ -119,31 +121,61 @@ __device__ __forceinline__ BwdTile decode_tile(const BwdParams &p, int t) {
   return d;
 }
 
+// Walks the (tile, query block) sequence of one CTA, skipping empty tiles.
+template <bool BCAST>
+struct BlockIter {
+  int t, tend, i;
+  bool valid;
+  BwdTile tl;
+  __device__ __forceinline__ void seek(const BwdParams &p) {
+    valid = false;
+    for (; t < tend; ++t) {
+      tl = decode_tile<BCAST>(p, t);
+      if (tl.nq > 0 && tl.nkv > 0) {
+        valid = true;
+        return;
+      }
+    }
+  }
+  __device__ __forceinline__ void next(const BwdParams &p) {
+    if (++i >= tl.nq) {
+      i = 0;
+      ++t;
+      seek(p);
+    }
+  }
+};
+
+__device__ __forceinline__ uint32_t bit(uint32_t ph, int s) { return (ph >> s) & 1u; }
+
 template <int D, bool BCAST>
 __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   BwdBars &bars = *reinterpret_cast<BwdBars *>(smem + C::OFF_BAR);
-  float *lse_s = reinterpret_cast<float *>(smem + C::OFF_LSE);  // [NSTAGE][64], log2 units
-  float *di_s = reinterpret_cast<float *>(smem + C::OFF_DI);    // [NSTAGE][64]
+  float *lse_s = reinterpret_cast<float *>(smem + C::OFF_LSE);
+  float *di_s = reinterpret_cast<float *>(smem + C::OFF_DI);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled layouts need 1024-byte alignment
+    if (threadIdx.x == 0) p.status[0] = 6;
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.kv_full, 1);
     mbar_init(&bars.kv_empty, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(&bars.stage_full[s], 1);
-      mbar_init(&bars.stage_empty[s], 2);  // MMA commit + compute warps done with O/dO
-      mbar_init(&bars.ds_free[s], 1);
+      mbar_init(&bars.stage_empty[s], 5);  // MMA commit + the four compute warps
+      mbar_init(&bars.aux_full[s], 4);     // LSE and Di of the block, from the dQ warps
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.p_ready, 4);
     mbar_init(&bars.ds_ready, 4);
+    mbar_init(&bars.ds_free, 1);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_free, 4);
     mbar_init(&bars.dkdv_full, 1);
@@ -160,7 +192,6 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_do);
-    prefetch_tmap(&p.tm_o);
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
     prefetch_tmap(&p.tm_dqacc);
@@ -178,7 +209,7 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t kvph = 0, stph[2] = {0, 0};
+      uint32_t kvph = 0, eph = 0;
       int qb = 0;
       for (int t = tbeg; t < tend; ++t) {
         const BwdTile tl = decode_tile<BCAST>(p, t);
@@ -191,18 +222,16 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
           tma_load_3d(smem + C::OFF_V + c * 16384, &p.tm_v, &bars.kv_full, c * 64, tl.h, tl.kv_row0);
         }
         for (int i = 0; i < tl.nq; ++i, ++qb) {
-          const int s = qb & 1;
-          if (!mbar_wait(&bars.stage_empty[s], stph[s] ^ 1, ctl, 2)) goto done;
-          stph[s] ^= 1;
-          mbar_arrive_expect_tx(&bars.stage_full[s], 3 * C::QT);
-          uint8_t *st = smem + C::OFF_STAGE + s * 3 * C::QT;
+          const int s = qb % C::NSTAGE;
+          if (!mbar_wait(&bars.stage_empty[s], bit(eph, s) ^ 1, ctl, 2)) goto done;
+          eph ^= 1u << s;
+          mbar_arrive_expect_tx(&bars.stage_full[s], 2 * C::QT);
+          uint8_t *st = smem + C::OFF_STAGE + s * 2 * C::QT;
           for (int c = 0; c < D / 64; ++c) {
             tma_load_3d(st + c * C::QCHUNK, &p.tm_q, &bars.stage_full[s], c * 64, tl.h,
                         tl.q_row0 + i * 64);
             tma_load_3d(st + C::QT + c * C::QCHUNK, &p.tm_do, &bars.stage_full[s], c * 64, tl.h,
                         tl.o_row0 + i * 64);
-            tma_load_3d(st + 2 * C::QT + c * C::QCHUNK, &p.tm_o, &bars.stage_full[s], c * 64,
-                        tl.h, tl.o_row0 + i * 64);
           }
         }
       }
@@ -210,7 +239,7 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t kvph = 0, stph[2] = {0, 0}, pph = 0, dsph = 0, dqfph = 0, dkdvph = 0;
+      uint32_t kvph = 0, fph = 0, pph = 0, dsph = 0, dqfph = 0, dkdvph = 0;
       int qb = 0;
       const uint32_t k_a = smem_u32(smem + C::OFF_K);
       const uint32_t v_a = smem_u32(smem + C::OFF_V);
@@ -225,7 +254,7 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
                  k > 0);
         }
       };
-      // dV (or dK) += A^T-from-TMEM x Y, Y = dO (or Q) [64 x D] MN-major.
+      // dV (or dK) += A-from-TMEM x Y, Y = dO (or Q) [64 x D] MN-major.
       auto issue_grad = [&](uint32_t dcol, uint32_t acol, uint32_t ya, bool acc) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -238,12 +267,12 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
         if (!mbar_wait(&bars.kv_full, kvph, ctl, 10)) goto done;
         kvph ^= 1;
         for (int i = 0; i < tl.nq; ++i, ++qb) {
-          const int s = qb & 1;
-          const uint32_t q_a = st_a + s * 3 * C::QT;
+          const int s = qb % C::NSTAGE;
+          const uint32_t q_a = st_a + s * 2 * C::QT;
           const uint32_t do_a = q_a + C::QT;
           if (i == 0) {
-            if (!mbar_wait(&bars.stage_full[s], stph[s], ctl, 11)) goto done;
-            stph[s] ^= 1;
+            if (!mbar_wait(&bars.stage_full[s], bit(fph, s), ctl, 11)) goto done;
+            fph ^= 1u << s;
             tc_fence_after();
             issue_xyT(COL_S, k_a, q_a);
             mma_commit(&bars.s_full);
@@ -259,11 +288,11 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
           tc_fence_after();
           issue_grad(COL_DV, COL_S, do_a, i > 0);
           const bool more = i + 1 < tl.nq;
-          const int s2 = (qb + 1) & 1;
-          const uint32_t q2_a = st_a + s2 * 3 * C::QT;
+          const int s2 = (qb + 1) % C::NSTAGE;
+          const uint32_t q2_a = st_a + s2 * 2 * C::QT;
           if (more) {
-            if (!mbar_wait(&bars.stage_full[s2], stph[s2], ctl, 14)) goto done;
-            stph[s2] ^= 1;
+            if (!mbar_wait(&bars.stage_full[s2], bit(fph, s2), ctl, 14)) goto done;
+            fph ^= 1u << s2;
             tc_fence_after();
             issue_xyT(COL_S, k_a, q2_a);
             mma_commit(&bars.s_full);
@@ -276,15 +305,12 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
           if (!mbar_wait(&bars.dq_free, dqfph ^ 1, ctl, 16)) goto done;
           dqfph ^= 1;
           tc_fence_after();
-          {
-            const uint32_t dsb = ds_a + (qb & 1) * 16384;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_ss(tmem + COL_DQ, sdesc_sw128(k_a + k * 2048, C::KT_LBO, 1024),
-                     sdesc_sw128(dsb + k * 2048, 8192, 1024), C::IDESC_Q, k > 0);
-          }
+          for (int k = 0; k < 8; ++k)
+            mma_ss(tmem + COL_DQ, sdesc_sw128(k_a + k * 2048, C::KT_LBO, 1024),
+                   sdesc_sw128(ds_a + k * 2048, 8192, 1024), C::IDESC_Q, k > 0);
           mma_commit(&bars.dq_full);
-          mma_commit(&bars.ds_free[qb & 1]);
+          mma_commit(&bars.ds_free);
           if (more) {
             issue_xyT(COL_DP, v_a, q2_a + C::QT);
             mma_commit(&bars.dp_full);
@@ -300,69 +326,36 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
     const int r = wq * 32 + lane;  // key row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float sl2 = p.scale_log2;
-    uint32_t stph[2] = {0, 0}, sph = 0, dpph = 0, dsfph[2] = {0, 0}, dkdvph = 0;
+    uint32_t aph = 0, sph = 0, dpph = 0, dsfph = 0, dkdvph = 0;
     int qb = 0;
     for (int t = tbeg; t < tend; ++t) {
       const BwdTile tl = decode_tile<BCAST>(p, t);
       if (tl.nq == 0 || tl.nkv <= 0) continue;
       const bool kv_ok = r < tl.nkv;
       for (int i = 0; i < tl.nq; ++i, ++qb) {
-        const int s = qb & 1;
-        const uint8_t *st = smem + C::OFF_STAGE + s * 3 * C::QT;
-        if (!mbar_wait(&bars.stage_full[s], stph[s], ctl, 20)) goto done;
-        stph[s] ^= 1;
-        // LSE (log2 units) and Di = rowsum(dO * O) of the block's query rows.
-        if (r < 64) {
-          const int qrow = i * 64 + r;
-          float lse2 = INFINITY, di = 0.f;
-          if (qrow < tl.Lq) {
-            lse2 = p.lse[tl.lse0 + qrow] * 1.4426950408889634f;
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-              const uint8_t *orow = st + 2 * C::QT + c * C::QCHUNK + r * 128;
-              const uint8_t *drow = st + C::QT + c * C::QCHUNK + r * 128;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const int off = ((j ^ (r & 7)) << 4);
-                const uint4 ov = *reinterpret_cast<const uint4 *>(orow + off);
-                const uint4 dv = *reinterpret_cast<const uint4 *>(drow + off);
-                const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
-                const __nv_bfloat162 *d2 = reinterpret_cast<const __nv_bfloat162 *>(&dv);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float2 of = __bfloat1622float2(o2[e]);
-                  const float2 df = __bfloat1622float2(d2[e]);
-                  di = fmaf(of.x, df.x, di);
-                  di = fmaf(of.y, df.y, di);
-                }
-              }
-            }
-          }
-          lse_s[s * 64 + r] = lse2;
-          di_s[s * 64 + r] = di;
-        }
-        named_bar_sync(1, 128);
-        if (r == 0) mbar_arrive(&bars.stage_empty[s]);
-        // P^T row (this thread's key row against the block's 64 query columns).
+        const int s = qb % C::NSTAGE;
+        if (!mbar_wait(&bars.aux_full[s], bit(aph, s), ctl, 20)) goto done;
+        aph ^= 1u << s;
+        // P^T row: this thread's key row against the block's 64 query columns.
         if (!mbar_wait(&bars.s_full, sph, ctl, 21)) goto done;
         sph ^= 1;
         tc_fence_after();
         float pr[64];
         {
-          uint32_t a[32], b[32];
-          tmem_ld32(tmem + lane_off + COL_S, a);
-          tmem_ld32(tmem + lane_off + COL_S + 32, b);
-          tmem_wait_ld();
           const float4 *l4 = reinterpret_cast<const float4 *>(lse_s + s * 64);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float4 lv = l4[c];
-            const float lv4[4] = {lv.x, lv.y, lv.z, lv.w};
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t a[32];
+            tmem_ld32(tmem + lane_off + COL_S + h2 * 32, a);
+            tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = c * 4 + e;
-              const float sv = __uint_as_float(col < 32 ? a[col] : b[col - 32]);
-              pr[col] = kv_ok ? ex2(fmaf(sv, sl2, -lv4[e])) : 0.f;
+            for (int c = 0; c < 8; ++c) {
+              const float4 lv = l4[h2 * 8 + c];
+              const float lv4[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                pr[h2 * 32 + c * 4 + e] =
+                    kv_ok ? ex2(fmaf(__uint_as_float(a[c * 4 + e]), sl2, -lv4[e])) : 0.f;
             }
           }
           uint32_t pk[32];
@@ -379,20 +372,21 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
         dpph ^= 1;
         tc_fence_after();
         {
-          uint32_t a[32], b[32];
-          tmem_ld32(tmem + lane_off + COL_DP, a);
-          tmem_ld32(tmem + lane_off + COL_DP + 32, b);
-          tmem_wait_ld();
           const float4 *d4 = reinterpret_cast<const float4 *>(di_s + s * 64);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float4 dv = d4[c];
-            const float dv4[4] = {dv.x, dv.y, dv.z, dv.w};
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t a[32];
+            tmem_ld32(tmem + lane_off + COL_DP + h2 * 32, a);
+            tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = c * 4 + e;
-              const float dp = __uint_as_float(col < 32 ? a[col] : b[col - 32]);
-              pr[col] = pr[col] * (dp - dv4[e]);
+            for (int c = 0; c < 8; ++c) {
+              const float4 dv = d4[h2 * 8 + c];
+              const float dv4[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int col = h2 * 32 + c * 4 + e;
+                pr[col] = pr[col] * (__uint_as_float(a[c * 4 + e]) - dv4[e]);
+              }
             }
           }
           uint32_t pk[32];
@@ -400,10 +394,9 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
           for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pr[2 * c], pr[2 * c + 1]);
           tmem_st32(tmem + lane_off + COL_DP, pk);
           // dS^T into shared memory (MN-major operand of the dQ^T product).
-          const int dsb = qb & 1;
-          if (!mbar_wait(&bars.ds_free[dsb], dsfph[dsb] ^ 1, ctl, 23)) goto done;
-          dsfph[dsb] ^= 1;
-          uint8_t *row = smem + C::OFF_DS + dsb * 16384 + r * 128;
+          if (!mbar_wait(&bars.ds_free, dsfph ^ 1, ctl, 23)) goto done;
+          dsfph ^= 1;
+          uint8_t *row = smem + C::OFF_DS + r * 128;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             *reinterpret_cast<uint4 *>(row + ((j ^ (r & 7)) << 4)) =
@@ -413,7 +406,10 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.ds_ready);
+        if (lane == 0) {
+          mbar_arrive(&bars.ds_ready);
+          mbar_arrive(&bars.stage_empty[s]);  // done with this stage's LSE / Di
+        }
       }
       // dK, dV epilogue for this tile's key rows.
       if (!mbar_wait(&bars.dkdv_full, dkdvph, ctl, 24)) goto done;
@@ -449,49 +445,116 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
       if (lane == 0) mbar_arrive(&bars.dkdv_free);
     }
   } else if (warp >= 8) {
-    // ------------------------------------------------------------ dQ reduction
+    // ---------------------------------- LSE / Di staging and dQ reduction
+    // Per query block, ahead of the compute warps: LSE and Di = rowsum(dO * O)
+    // of the block's 64 rows (two threads per row, O read from global memory
+    // one block ahead into registers, dO from the stage). Then, one block
+    // behind the MMA: drain dQ^T from TMEM and TMA reduce-add it.
+    constexpr int ND = D / 2;  // head-dim elements per thread for Di
+    constexpr int NV = ND / 8;
     const int wq = warp & 3;
+    const int rt = threadIdx.x - 256;
+    const int row = rt >> 1, half = rt & 1;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    uint8_t *stg = smem + C::OFF_DQS + wq * 8192;
-    uint32_t dqph = 0;
-    int last_buf = -1;
-    for (int t = tbeg; t < tend; ++t) {
-      const BwdTile tl = decode_tile<BCAST>(p, t);
-      if (tl.nq == 0 || tl.nkv <= 0) continue;
-      for (int i = 0; i < tl.nq; ++i) {
-        if (!mbar_wait(&bars.dq_full, dqph, ctl, 30)) goto done;
-        dqph ^= 1;
-        tc_fence_after();
-        uint32_t v[2][32];
-        tmem_ld32(tmem + lane_off + COL_DQ, v[0]);
-        tmem_ld32(tmem + lane_off + COL_DQ + 32, v[1]);
-        tmem_wait_ld();
-        tc_fence_before();
+    float *stg = reinterpret_cast<float *>(smem + C::OFF_DQS + wq * 4096);
+    const __nv_bfloat16 *obase = static_cast<const __nv_bfloat16 *>(p.o);
+    uint32_t fph = 0, dqph = 0;
+    int qb = 0;
+    uint4 o_r[NV];
+    float lse_r = INFINITY;
+    bool row_ok = false;
+    auto prefetch = [&](const BlockIter<BCAST> &it) {
+      const int qrow = it.i * 64 + row;
+      row_ok = qrow < it.tl.Lq;
+      if (row_ok) {
+        lse_r = p.lse[it.tl.lse0 + qrow];
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            obase + ((int64_t)(it.tl.o_row0 + qrow) * p.H + it.tl.h) * D + half * ND);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) o_r[j] = __ldg(src + j);
+      }
+    };
+    auto reduce_dq = [&](const BwdTile &tl, int i) -> bool {
+      if (!mbar_wait(&bars.dq_full, dqph, ctl, 30)) return false;
+      dqph ^= 1;
+      tc_fence_after();
+      uint32_t v[2][32];
+      tmem_ld32(tmem + lane_off + COL_DQ, v[0]);
+      tmem_ld32(tmem + lane_off + COL_DQ + 32, v[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.dq_free);  // TMEM released before the reduction
+      if (wq * 32 >= D) return true;               // D = 64: lanes 64..127 are padding
+      const int rows = min(64, tl.Lq - i * 64);
+#pragma unroll
+      for (int qc = 0; qc < 2; ++qc) {
+        if (qc * 32 >= rows) break;
+        if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.dq_free);  // TMEM released before the reduction
-        if (wq * 32 >= D) continue;                  // D = 64: lanes 64..127 are padding
-        const int rows = min(64, tl.Lq - i * 64);
 #pragma unroll
-        for (int qc = 0; qc < 2; ++qc) {
-          if (qc * 32 >= rows) break;
-          float *buf = reinterpret_cast<float *>(stg + qc * 4096);
-          if (lane == 0) {
-            if (last_buf == qc) bulk_wait_read<0>();
-            else bulk_wait_read<1>();
-          }
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) buf[j * 32 + lane] = __uint_as_float(v[qc][j]) * p.scale;
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_3d(&p.tm_dqacc, buf, wq * 32, tl.h, tl.q_row0 + i * 64 + qc * 32);
-            bulk_commit();
-          }
-          last_buf = qc;
+        for (int j = 0; j < 32; ++j) stg[j * 32 + lane] = __uint_as_float(v[qc][j]) * p.scale;
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&p.tm_dqacc, stg, wq * 32, tl.h, tl.q_row0 + i * 64 + qc * 32);
+          bulk_commit();
         }
       }
+      return true;
+    };
+    BlockIter<BCAST> cur;
+    cur.t = tbeg;
+    cur.tend = tend;
+    cur.i = 0;
+    cur.seek(p);
+    if (cur.valid) prefetch(cur);
+    bool have_prev = false;
+    BwdTile prev_tl = cur.tl;
+    int prev_i = 0;
+    while (cur.valid) {
+      const int s = qb % C::NSTAGE;
+      if (!mbar_wait(&bars.stage_full[s], bit(fph, s), ctl, 31)) goto done;
+      fph ^= 1u << s;
+      {
+        float di = 0.f;
+        if (row_ok) {
+          const uint8_t *drow = smem + C::OFF_STAGE + s * 2 * C::QT + C::QT +
+                                ((half * ND) / 64) * C::QCHUNK + row * 128;
+          const int j0 = ((half * ND) % 64) / 8;
+#pragma unroll
+          for (int j = 0; j < NV; ++j) {
+            const uint4 dv = *reinterpret_cast<const uint4 *>(drow + (((j0 + j) ^ (row & 7)) << 4));
+            const __nv_bfloat162 *d2 = reinterpret_cast<const __nv_bfloat162 *>(&dv);
+            const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&o_r[j]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 df = __bfloat1622float2(d2[e]);
+              const float2 of = __bfloat1622float2(o2[e]);
+              di = fmaf(of.x, df.x, di);
+              di = fmaf(of.y, df.y, di);
+            }
+          }
+        }
+        di += __shfl_xor_sync(0xffffffffu, di, 1);
+        if (half == 0) {
+          lse_s[s * 64 + row] = row_ok ? lse_r * 1.4426950408889634f : INFINITY;
+          di_s[s * 64 + row] = row_ok ? di : 0.f;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.aux_full[s]);
+      BlockIter<BCAST> nx = cur;
+      nx.next(p);
+      if (nx.valid) prefetch(nx);
+      if (have_prev && !reduce_dq(prev_tl, prev_i)) goto done;
+      prev_tl = cur.tl;
+      prev_i = cur.i;
+      have_prev = true;
+      cur = nx;
+      ++qb;
     }
+    if (have_prev && !reduce_dq(prev_tl, prev_i)) goto done;
     if (lane == 0) bulk_wait<0>();
   }
 done:

@@ -63,7 +63,7 @@ struct FwdBars {
 };
 
 struct FwdTile {
-  int b, h, n_kv, Lk, nrows[2];
+  int b, h, n_kv, Lk, nrows0, nrows1;
   int q_coord;       // row coordinate of the tile's first query row in tm_q
   int kv0;           // first key row in tm_k / tm_v
   int64_t out_row0;  // row of the tile's first query row in O
@@ -86,8 +86,8 @@ __device__ __forceinline__ FwdTile decode_tile(const FwdParams &p, int t) {
   const int row0 = m * 256;
   d.Lk = L;
   d.n_kv = (L + 127) / 128;
-  d.nrows[0] = max(0, min(128, Lq - row0));
-  d.nrows[1] = max(0, min(128, Lq - row0 - 128));
+  d.nrows0 = max(0, min(128, Lq - row0));
+  d.nrows1 = max(0, min(128, Lq - row0 - 128));
   d.kv0 = (int)s0;
   if (BCAST) {
     d.q_coord = row0;
@@ -149,16 +149,17 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t qph[2] = {0, 0};
+      uint32_t qph = 0;
       int slot = 0;
       uint32_t sph = 0;
       for (int t = tbeg; t < tend; ++t) {
         const FwdTile tl = decode_tile<BCAST>(p, t);
         if (tl.n_kv == 0) continue;
+#pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if (tl.nrows[x] == 0) continue;
-          if (!mbar_wait(&bars.q_empty[x], qph[x] ^ 1, ctl, 1)) goto done;
-          qph[x] ^= 1;
+          if ((x ? tl.nrows1 : tl.nrows0) == 0) continue;
+          if (!mbar_wait(&bars.q_empty[x], ((qph >> x) & 1) ^ 1, ctl, 1)) goto done;
+          qph ^= 1u << x;
           mbar_arrive_expect_tx(&bars.q_full[x], C::TILE_BYTES);
           for (int c = 0; c < D / 64; ++c)
             tma_load_3d(smem + C::OFF_Q + x * C::TILE_BYTES + c * 16384, &p.tm_q,
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t qph[2] = {0, 0}, pph[2] = {0, 0}, oph[2] = {0, 0};
+      uint32_t qph = 0, pph = 0, oph = 0;  // phase bit x per half
       int slot = 0;
       uint32_t sph = 0;
       const uint32_t q_addr = smem_u32(smem + C::OFF_Q);
@@ -208,19 +209,21 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       for (int t = tbeg; t < tend; ++t) {
         const FwdTile tl = decode_tile<BCAST>(p, t);
         if (tl.n_kv == 0) continue;
-        const bool has[2] = {tl.nrows[0] > 0, tl.nrows[1] > 0};
+        const uint32_t has = (tl.nrows0 > 0 ? 1u : 0u) | (tl.nrows1 > 0 ? 2u : 0u);
+#pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if (!has[x]) continue;
-          if (!mbar_wait(&bars.q_full[x], qph[x], ctl, 10)) goto done;
-          qph[x] ^= 1;
+          if (!(has >> x & 1)) continue;
+          if (!mbar_wait(&bars.q_full[x], (qph >> x) & 1, ctl, 10)) goto done;
+          qph ^= 1u << x;
         }
         // S_0 for both halves.
         int kslot = slot;
         if (!mbar_wait(&slot_full[kslot], sph, ctl, 11)) goto done;
         if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
         tc_fence_after();
+#pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if (!has[x]) continue;
+          if (!(has >> x & 1)) continue;
           issue_qk(x, kslot);
           mma_commit(&bars.s_full[x]);
           if (tl.n_kv == 1) mma_commit(&bars.q_empty[x]);
@@ -237,13 +240,14 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
             if (!mbar_wait(&slot_full[kslot], sph, ctl, 13)) goto done;
             if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
           }
+#pragma unroll
           for (int x = 0; x < 2; ++x) {
-            if (!has[x]) continue;
-            if (!mbar_wait(&bars.p_ready[x], pph[x], ctl, 14)) goto done;
-            pph[x] ^= 1;
+            if (!(has >> x & 1)) continue;
+            if (!mbar_wait(&bars.p_ready[x], (pph >> x) & 1, ctl, 14)) goto done;
+            pph ^= 1u << x;
             if (j == 1) {  // first PV of the tile overwrites O: epilogue must be done with it
-              if (!mbar_wait(&bars.o_free[x], oph[x] ^ 1, ctl, 15)) goto done;
-              oph[x] ^= 1;
+              if (!mbar_wait(&bars.o_free[x], ((oph >> x) & 1) ^ 1, ctl, 15)) goto done;
+              oph ^= 1u << x;
             }
             tc_fence_after();
             issue_pv(x, vslot, j > 1);
@@ -271,7 +275,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
     __nv_bfloat16 *obase = static_cast<__nv_bfloat16 *>(p.o);
     for (int t = tbeg; t < tend; ++t) {
       const FwdTile tl = decode_tile<BCAST>(p, t);
-      const int nrows = tl.nrows[x];
+      const int nrows = x ? tl.nrows1 : tl.nrows0;
       if (nrows == 0) continue;
       const bool row_ok = r < nrows;
       const int64_t orow = tl.out_row0 + x * 128 + r;

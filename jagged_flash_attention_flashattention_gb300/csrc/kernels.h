@@ -35,7 +35,6 @@ cudaError_t launch_fwd(const FwdParams &p, int D, int num_sms, cudaStream_t st);
 struct BwdParams {
   CUtensorMap tm_q;   // bf16 query rows, box {64, 1, 64}
   CUtensorMap tm_do;  // bf16 dO rows (same row space as O), box {64, 1, 64}
-  CUtensorMap tm_o;   // bf16 O rows, box {64, 1, 64}
   CUtensorMap tm_k;   // bf16 [Tk, H, D], box {64, 1, 128}
   CUtensorMap tm_v;
   CUtensorMap tm_dqacc;  // fp32 [rows, H, D] as {D, H, rows}, box {32, 1, 32}, no swizzle
@@ -44,6 +43,7 @@ struct BwdParams {
   const int32_t *sm_ptr;
   const int32_t *tiles;
   const float *lse;
+  const void *o;  // bf16 O rows (read directly for Di)
   void *dk;  // bf16 [Tk, H, D]
   void *dv;
   int64_t T;
