@@ -111,13 +111,13 @@ __global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_cons
 
   if (warp == 0) {
     if (lane == 0) {
-      uint32_t eph[4] = {0, 0, 0, 0};
+      uint32_t eph = 0;
       int n = 0;
       for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
         const Unit x = unit_of(u, p.H, p.rows);
         const int s = n % C::NSTAGE;
-        if (!mbar_wait(&bars.empty[s], eph[s] ^ 1, ctl, 1)) goto done;
-        eph[s] ^= 1;
+        if (!mbar_wait(&bars.empty[s], bit(eph, s) ^ 1, ctl, 1)) goto done;
+        eph ^= 1u << (s);
         mbar_arrive_expect_tx(&bars.full[s], 3 * C::TILE);
         uint8_t *st = smem + C::OFF_STAGE + s * 3 * C::TILE;
         for (int c = 0; c < D / 64; ++c) {
@@ -129,38 +129,40 @@ __global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_cons
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      uint32_t fph[4] = {0, 0, 0, 0}, pph[2] = {0, 0}, fr[2] = {0, 0};
+      uint32_t fph = 0, pph = 0, fr = 0;
       const uint32_t st0 = smem_u32(smem + C::OFF_STAGE);
+      const uint64_t st_kmaj = sdesc_sw128(st0, 16, 1024);  // k-steps add offset >> 4
+      const uint64_t st_mn = sdesc_sw128(st0, 16384, 1024);
       int n = 0;
       int prev_stage = -1;
       for (int u = blockIdx.x;; u += gridDim.x, ++n) {
         const bool have = u < n_units;
         if (have) {
           const int s = n % C::NSTAGE, ts = n & 1;
-          if (!mbar_wait(&bars.full[s], fph[s], ctl, 10)) goto done;
-          fph[s] ^= 1;
-          if (!mbar_wait(&bars.slot_free[ts], fr[ts] ^ 1, ctl, 11)) goto done;
-          fr[ts] ^= 1;
+          if (!mbar_wait(&bars.full[s], bit(fph, s), ctl, 10)) goto done;
+          fph ^= 1u << (s);
+          if (!mbar_wait(&bars.slot_free[ts], bit(fr, ts) ^ 1, ctl, 11)) goto done;
+          fr ^= 1u << (ts);
           tc_fence_after();
-          const uint32_t qa = st0 + s * 3 * C::TILE, ka = qa + C::TILE;
+          const uint64_t qd = st_kmaj + ((uint32_t)(s * 3 * C::TILE) >> 4);
+          const uint64_t kd = qd + (C::TILE >> 4);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-            mma_ss(tmem + ts * 256, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                   C::IDESC_S, k > 0);
+            const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+            mma_ss(tmem + ts * 256, qd + off, kd + off, C::IDESC_S, k > 0);
           }
           mma_commit(&bars.s_full[ts]);
         }
         if (n > 0) {  // O = P V for the previous unit
           const int pn = n - 1, ts = pn & 1;
-          if (!mbar_wait(&bars.p_ready[ts], pph[ts], ctl, 12)) goto done;
-          pph[ts] ^= 1;
+          if (!mbar_wait(&bars.p_ready[ts], bit(pph, ts), ctl, 12)) goto done;
+          pph ^= 1u << (ts);
           tc_fence_after();
-          const uint32_t va = st0 + prev_stage * 3 * C::TILE + 2 * C::TILE;
+          const uint64_t vd = st_mn + ((uint32_t)(prev_stage * 3 * C::TILE + 2 * C::TILE) >> 4);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + ts * 256 + 128, tmem + ts * 256 + k * 8,
-                   sdesc_sw128(va + k * 2048, 16384, 1024), C::IDESC_O, k > 0);
+            mma_ts(tmem + ts * 256 + 128, tmem + ts * 256 + k * 8, vd + (k * 2048 >> 4), C::IDESC_O,
+                   k > 0);
           mma_commit(&bars.o_full[ts]);
           mma_commit(&bars.empty[prev_stage]);
         }
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_cons
     const int blk = wq >> 1;  // rows 0-63 -> key block 0, rows 64-127 -> key block 1
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float sl2 = p.scale_log2;
-    uint32_t sph[2] = {0, 0}, oph[2] = {0, 0};
+    uint32_t sph = 0, oph = 0;
     float l_prev = 1.f;
     Unit x_prev{0, 0, 0};
     int n = 0;
@@ -184,8 +186,8 @@ __global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_cons
       float l_cur = 1.f;
       if (have) {  // softmax of unit n
         const int ts = n & 1;
-        if (!mbar_wait(&bars.s_full[ts], sph[ts], ctl, 20)) goto done;
-        sph[ts] ^= 1;
+        if (!mbar_wait(&bars.s_full[ts], bit(sph, ts), ctl, 20)) goto done;
+        sph ^= 1u << (ts);
         tc_fence_after();
         const uint32_t tS = tmem + lane_off + ts * 256;
         uint32_t a[32], b[32];
@@ -223,8 +225,8 @@ __global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_cons
       }
       if (n > 0) {  // epilogue of unit n-1
         const int ts = (n - 1) & 1;
-        if (!mbar_wait(&bars.o_full[ts], oph[ts], ctl, 21)) goto done;
-        oph[ts] ^= 1;
+        if (!mbar_wait(&bars.o_full[ts], bit(oph, ts), ctl, 21)) goto done;
+        oph ^= 1u << (ts);
         tc_fence_after();
         const uint32_t tO = tmem + lane_off + ts * 256 + 128;
         const bool row_ok = r < x_prev.nrows;
@@ -341,13 +343,13 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
 
   if (warp == 0) {
     if (lane == 0) {
-      uint32_t eph[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      uint32_t eph = 0;
       int slot = 0;
       for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         const Unit x = unit_of(u, p.H, p.rows);
         for (int t = 0; t < 4; ++t) {
-          if (!mbar_wait(&bars.empty[slot], eph[slot] ^ 1, ctl, 1)) goto done;
-          eph[slot] ^= 1;
+          if (!mbar_wait(&bars.empty[slot], bit(eph, slot) ^ 1, ctl, 1)) goto done;
+          eph ^= 1u << (slot);
           mbar_arrive_expect_tx(&bars.full[slot], C::TILE);
           const CUtensorMap *m = t == T_V ? &p.tm_v : t == T_DO ? &p.tm_do : t == T_Q ? &p.tm_q : &p.tm_k;
           for (int c = 0; c < D / 64; ++c)
@@ -359,24 +361,29 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      uint32_t fph[8] = {0, 0, 0, 0, 0, 0, 0, 0}, psr = 0, psf = 0, gf = 0;
+      uint32_t fph = 0, psr = 0, psf = 0, gf = 0;
       const uint32_t ring = smem_u32(smem + C::OFF_RING);
       const uint32_t pa = smem_u32(smem + C::OFF_P), dsa = smem_u32(smem + C::OFF_DS);
       int slot = 0;
       auto sl = [&](int t) { int s = slot + t; return s >= C::NSLOT ? s - C::NSLOT : s; };
-      auto ta = [&](int t) { return ring + sl(t) * C::TILE; };
       auto wait_full = [&](int t) -> bool {
         const int s = sl(t);
-        if (!mbar_wait(&bars.full[s], fph[s], ctl, 10 + t)) return false;
-        fph[s] ^= 1;
+        if (!mbar_wait(&bars.full[s], bit(fph, s), ctl, 10 + t)) return false;
+        fph ^= 1u << (s);
         return true;
       };
-      auto xyT = [&](uint32_t dcol, uint32_t xa, uint32_t ya) {
+      const uint64_t ring_kmaj = sdesc_sw128(ring, 16, 1024);  // k-steps add offset >> 4
+      const uint64_t ring_mn = sdesc_sw128(ring, 16384, 1024);
+      const uint64_t p_mn = sdesc_sw128(pa, 16384, 1024);
+      const uint64_t ds_mn = sdesc_sw128(dsa, 16384, 1024);
+      const uint64_t ds_kmaj = sdesc_sw128(dsa, 16, 1024);
+      auto tk = [&](int t) { return ring_kmaj + ((uint32_t)(sl(t) * C::TILE) >> 4); };
+      auto tm = [&](int t) { return ring_mn + ((uint32_t)(sl(t) * C::TILE) >> 4); };
+      auto xyT = [&](uint32_t dcol, uint64_t xd, uint64_t yd) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tmem + dcol, sdesc_sw128(xa + off, 16, 1024), sdesc_sw128(ya + off, 16, 1024),
-                 C::IDESC_S, k > 0);
+          const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+          mma_ss(tmem + dcol, xd + off, yd + off, C::IDESC_S, k > 0);
         }
       };
       for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -384,33 +391,40 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
         gf ^= 1;
         if (!wait_full(T_V) || !wait_full(T_DO)) goto done;
         tc_fence_after();
-        xyT(BC_DP, ta(T_DO), ta(T_V));  // dP = dO V^T
+        xyT(BC_DP, tk(T_DO), tk(T_V));  // dP = dO V^T
         mma_commit(&bars.dp_full);
         mma_commit(&bars.empty[sl(T_V)]);
         if (!wait_full(T_Q) || !wait_full(T_K)) goto done;
         tc_fence_after();
-        xyT(BC_S, ta(T_Q), ta(T_K));  // S = Q K^T
+        xyT(BC_S, tk(T_Q), tk(T_K));  // S = Q K^T
         mma_commit(&bars.s_full);
         if (!mbar_wait(&bars.ps_ready, psr, ctl, 21)) goto done;
         psr ^= 1;
         tc_fence_after();
         // dV = P^T dO  (A = P^T: MN-major view of the [q][k] tile; B = dO MN-major)
+        {
+          const uint64_t bd = tm(T_DO);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + BC_S, sdesc_sw128(pa + k * 2048, 16384, 1024),
-                 sdesc_sw128(ta(T_DO) + k * 2048, 16384, 1024), C::IDESC_T, k > 0);
+          for (int k = 0; k < 8; ++k)
+            mma_ss(tmem + BC_S, p_mn + (k * 2048 >> 4), bd + (k * 2048 >> 4), C::IDESC_T, k > 0);
+        }
         mma_commit(&bars.empty[sl(T_DO)]);
         // dK = dS^T Q
+        {
+          const uint64_t bd = tm(T_Q);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + BC_DP, sdesc_sw128(dsa + k * 2048, 16384, 1024),
-                 sdesc_sw128(ta(T_Q) + k * 2048, 16384, 1024), C::IDESC_T, k > 0);
+          for (int k = 0; k < 8; ++k)
+            mma_ss(tmem + BC_DP, ds_mn + (k * 2048 >> 4), bd + (k * 2048 >> 4), C::IDESC_T, k > 0);
+        }
         mma_commit(&bars.empty[sl(T_Q)]);
         // dQ = dS K  (A = dS K-major; B = K MN-major)
+        {
+          const uint64_t bd = tm(T_K);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + BC_DQ, sdesc_sw128(dsa + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                 sdesc_sw128(ta(T_K) + k * 2048, 16384, 1024), C::IDESC_Q, k > 0);
+          for (int k = 0; k < 8; ++k)
+            mma_ss(tmem + BC_DQ, ds_kmaj + (((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                   bd + (k * 2048 >> 4), C::IDESC_Q, k > 0);
+        }
         mma_commit(&bars.empty[sl(T_K)]);
         mma_commit(&bars.g_full);
         mma_commit(&bars.ps_free);

@@ -146,8 +146,6 @@ struct BlockIter {
   }
 };
 
-__device__ __forceinline__ uint32_t bit(uint32_t ph, int s) { return (ph >> s) & 1u; }
-
 template <int D, bool BCAST>
 __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
@@ -245,21 +243,26 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
       const uint32_t v_a = smem_u32(smem + C::OFF_V);
       const uint32_t st_a = smem_u32(smem + C::OFF_STAGE);
       const uint32_t ds_a = smem_u32(smem + C::OFF_DS);
+      // Descriptors are built once per operand; k-steps add offset >> 4 to the
+      // start-address field (keeps the single issuing thread cheap).
+      const uint64_t k_kmaj = sdesc_sw128(k_a, 16, 1024), v_kmaj = sdesc_sw128(v_a, 16, 1024);
+      const uint64_t st_kmaj = sdesc_sw128(st_a, 16, 1024);
+      const uint64_t st_mn = sdesc_sw128(st_a, C::QCHUNK, 1024);
+      const uint64_t kT_mn = sdesc_sw128(k_a, C::KT_LBO, 1024);
+      const uint64_t ds_mn = sdesc_sw128(ds_a, 8192, 1024);
       // S^T (or dP^T) = X Y^T, X = K (or V) [128 x D], Y = Q (or dO) [64 x D], both K-major.
-      auto issue_xyT = [&](uint32_t dcol, uint32_t xa, uint32_t ya) {
+      auto issue_xyT = [&](uint32_t dcol, uint64_t xd, uint64_t yd) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          mma_ss(tmem + dcol, sdesc_sw128(xa + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                 sdesc_sw128(ya + (k >> 2) * C::QCHUNK + (k & 3) * 32, 16, 1024), C::IDESC_S,
-                 k > 0);
-        }
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tmem + dcol, xd + (((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                 yd + (((k >> 2) * C::QCHUNK + (k & 3) * 32) >> 4), C::IDESC_S, k > 0);
       };
       // dV (or dK) += A-from-TMEM x Y, Y = dO (or Q) [64 x D] MN-major.
-      auto issue_grad = [&](uint32_t dcol, uint32_t acol, uint32_t ya, bool acc) {
+      auto issue_grad = [&](uint32_t dcol, uint32_t acol, uint64_t yd, bool acc) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + dcol, tmem + acol + k * 8, sdesc_sw128(ya + k * 2048, C::QCHUNK, 1024),
-                 C::IDESC_G, (acc || k > 0) ? 1u : 0u);
+          mma_ts(tmem + dcol, tmem + acol + k * 8, yd + (k * 2048 >> 4), C::IDESC_G,
+                 (acc || k > 0) ? 1u : 0u);
       };
       for (int t = tbeg; t < tend; ++t) {
         const BwdTile tl = decode_tile<BCAST>(p, t);
@@ -268,15 +271,14 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
         kvph ^= 1;
         for (int i = 0; i < tl.nq; ++i, ++qb) {
           const int s = qb % C::NSTAGE;
-          const uint32_t q_a = st_a + s * 2 * C::QT;
-          const uint32_t do_a = q_a + C::QT;
+          const uint32_t q_off = (uint32_t)(s * 2 * C::QT) >> 4, do_off = q_off + (C::QT >> 4);
           if (i == 0) {
             if (!mbar_wait(&bars.stage_full[s], bit(fph, s), ctl, 11)) goto done;
             fph ^= 1u << s;
             tc_fence_after();
-            issue_xyT(COL_S, k_a, q_a);
+            issue_xyT(COL_S, k_kmaj, st_kmaj + q_off);
             mma_commit(&bars.s_full);
-            issue_xyT(COL_DP, v_a, do_a);
+            issue_xyT(COL_DP, v_kmaj, st_kmaj + do_off);
             mma_commit(&bars.dp_full);
           }
           if (!mbar_wait(&bars.p_ready, pph, ctl, 12)) goto done;
@@ -286,33 +288,33 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
             dkdvph ^= 1;
           }
           tc_fence_after();
-          issue_grad(COL_DV, COL_S, do_a, i > 0);
+          issue_grad(COL_DV, COL_S, st_mn + do_off, i > 0);
           const bool more = i + 1 < tl.nq;
           const int s2 = (qb + 1) % C::NSTAGE;
-          const uint32_t q2_a = st_a + s2 * 2 * C::QT;
+          const uint32_t q2_off = (uint32_t)(s2 * 2 * C::QT) >> 4;
           if (more) {
             if (!mbar_wait(&bars.stage_full[s2], bit(fph, s2), ctl, 14)) goto done;
             fph ^= 1u << s2;
             tc_fence_after();
-            issue_xyT(COL_S, k_a, q2_a);
+            issue_xyT(COL_S, k_kmaj, st_kmaj + q2_off);
             mma_commit(&bars.s_full);
           }
           if (!mbar_wait(&bars.ds_ready, dsph, ctl, 15)) goto done;
           dsph ^= 1;
           tc_fence_after();
-          issue_grad(COL_DK, COL_DP, q_a, i > 0);
+          issue_grad(COL_DK, COL_DP, st_mn + q_off, i > 0);
           mma_commit(&bars.stage_empty[s]);
           if (!mbar_wait(&bars.dq_free, dqfph ^ 1, ctl, 16)) goto done;
           dqfph ^= 1;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + COL_DQ, sdesc_sw128(k_a + k * 2048, C::KT_LBO, 1024),
-                   sdesc_sw128(ds_a + k * 2048, 8192, 1024), C::IDESC_Q, k > 0);
+            mma_ss(tmem + COL_DQ, kT_mn + (k * 2048 >> 4), ds_mn + (k * 2048 >> 4), C::IDESC_Q,
+                   k > 0);
           mma_commit(&bars.dq_full);
           mma_commit(&bars.ds_free);
           if (more) {
-            issue_xyT(COL_DP, v_a, q2_a + C::QT);
+            issue_xyT(COL_DP, v_kmaj, st_kmaj + q2_off + (C::QT >> 4));
             mma_commit(&bars.dp_full);
           }
         }

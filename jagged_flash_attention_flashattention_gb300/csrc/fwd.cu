@@ -189,22 +189,27 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       uint32_t sph = 0;
       const uint32_t q_addr = smem_u32(smem + C::OFF_Q);
       const uint32_t ring = smem_u32(smem + C::OFF_RING);
+      // Descriptors are built once; a k-step only adds its byte offset >> 4 to
+      // the start-address field (a single add keeps the one issuing thread
+      // ahead of the tensor core).
+      const uint64_t q_desc = sdesc_sw128(q_addr, 16, 1024);
+      const uint64_t ring_kdesc = sdesc_sw128(ring, 16, 1024);
+      const uint64_t ring_vdesc = sdesc_sw128(ring, 16384, 1024);
       auto issue_qk = [&](int x, int kslot) {
-        const uint32_t qa = q_addr + x * C::TILE_BYTES;
-        const uint32_t ka = ring + kslot * C::TILE_BYTES;
+        const uint64_t qd = q_desc + (uint64_t)(x * (C::TILE_BYTES >> 4));
+        const uint64_t kd = ring_kdesc + (uint64_t)(kslot * (C::TILE_BYTES >> 4));
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tmem + x * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 C::IDESC_QK, k > 0);
+          const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+          mma_ss(tmem + x * 128, qd + off, kd + off, C::IDESC_QK, k > 0);
         }
       };
       auto issue_pv = [&](int x, int vslot, bool acc) {
-        const uint32_t va = ring + vslot * C::TILE_BYTES;
+        const uint64_t vd = ring_vdesc + (uint64_t)(vslot * (C::TILE_BYTES >> 4));
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8,
-                 sdesc_sw128(va + k * 2048, 16384, 1024), C::IDESC_PV, (acc || k > 0) ? 1u : 0u);
+          mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, vd + (k * 2048 >> 4), C::IDESC_PV,
+                 (acc || k > 0) ? 1u : 0u);
       };
       for (int t = tbeg; t < tend; ++t) {
         const FwdTile tl = decode_tile<BCAST>(p, t);
