@@ -33,8 +33,9 @@
 // (broadcast-Q, where dQ is a sum over the whole batch).
 //
 // Roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
-// warps 4-7 compute + dK/dV epilogue, warps 8-11 LSE/Di staging + dQ
-// reduction.
+// warps 4-7 and 12-15 compute + dK/dV epilogue (two warps per TMEM lane
+// quarter, each on half of the query columns), warps 8-11 LSE/Di staging +
+// dQ reduction.
 // Tensor memory columns: dV [0,128) dK [128,256) S/P [256,320)
 // dP/dS [320,384) dQ^T [384,448).
 #include <cuda_bf16.h>
@@ -147,7 +148,7 @@ struct BlockIter {
 };
 
 template <int D, bool BCAST>
-__global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   BwdBars &bars = *reinterpret_cast<BwdBars *>(smem + C::OFF_BAR);
@@ -166,18 +167,18 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
     mbar_init(&bars.kv_empty, 1);
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(&bars.stage_full[s], 1);
-      mbar_init(&bars.stage_empty[s], 5);  // MMA commit + the four compute warps
+      mbar_init(&bars.stage_empty[s], 9);  // MMA commit + the eight compute warps
       mbar_init(&bars.aux_full[s], 4);     // LSE and Di of the block, from the dQ warps
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.p_ready, 4);
-    mbar_init(&bars.ds_ready, 4);
+    mbar_init(&bars.p_ready, 8);
+    mbar_init(&bars.ds_ready, 8);
     mbar_init(&bars.ds_free, 1);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_free, 4);
     mbar_init(&bars.dkdv_full, 1);
-    mbar_init(&bars.dkdv_free, 4);
+    mbar_init(&bars.dkdv_free, 8);
     mbar_init(&bars.drain, 1);
     bars.abort_flag = 0;
     fence_mbar_init();
@@ -257,12 +258,15 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
           mma_ss(tmem + dcol, xd + (((k >> 2) * 16384 + (k & 3) * 32) >> 4),
                  yd + (((k >> 2) * C::QCHUNK + (k & 3) * 32) >> 4), C::IDESC_S, k > 0);
       };
-      // dV (or dK) += A-from-TMEM x Y, Y = dO (or Q) [64 x D] MN-major.
+      // dV (or dK) += A-from-TMEM x Y, Y = dO (or Q) [64 x D] MN-major. The bf16
+      // A operand of query columns [32h, 32h+32) sits at TMEM columns
+      // [32h, 32h+16) of its region (each compute warp overwrites only its own
+      // scores), so k-step k reads column (k / 2) * 32 + (k % 2) * 8.
       auto issue_grad = [&](uint32_t dcol, uint32_t acol, uint64_t yd, bool acc) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + dcol, tmem + acol + k * 8, yd + (k * 2048 >> 4), C::IDESC_G,
-                 (acc || k > 0) ? 1u : 0u);
+          mma_ts(tmem + dcol, tmem + acol + (k >> 1) * 32 + (k & 1) * 8, yd + (k * 2048 >> 4),
+                 C::IDESC_G, (acc || k > 0) ? 1u : 0u);
       };
       for (int t = tbeg; t < tend; ++t) {
         const BwdTile tl = decode_tile<BCAST>(p, t);
@@ -322,10 +326,14 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
         mma_commit(&bars.kv_empty);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if ((warp >= 4 && warp < 8) || warp >= 12) {
     // ------------------------------------------ compute + dK/dV epilogue
+    // Eight warps: two per TMEM lane quarter, each taking half of the block's
+    // 64 query columns (and half of the head dimension in the epilogue), so
+    // two warps per scheduler hide each other's TMEM / MUFU latency.
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // key row within the tile = TMEM lane
+    const int ch = warp >= 12 ? 1 : 0;  // column half
+    const int r = wq * 32 + lane;       // key row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float sl2 = p.scale_log2;
     uint32_t aph = 0, sph = 0, dpph = 0, dsfph = 0, dkdvph = 0;
@@ -338,70 +346,62 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
         const int s = qb % C::NSTAGE;
         if (!mbar_wait(&bars.aux_full[s], bit(aph, s), ctl, 20)) goto done;
         aph ^= 1u << s;
-        // P^T row: this thread's key row against the block's 64 query columns.
+        // P^T: this thread's key row against 32 of the block's query columns.
         if (!mbar_wait(&bars.s_full, sph, ctl, 21)) goto done;
         sph ^= 1;
         tc_fence_after();
-        float pr[64];
+        float pr[32];
         {
-          const float4 *l4 = reinterpret_cast<const float4 *>(lse_s + s * 64);
+          const float4 *l4 = reinterpret_cast<const float4 *>(lse_s + s * 64 + ch * 32);
+          uint32_t a[32];
+          tmem_ld32(tmem + lane_off + COL_S + ch * 32, a);
+          tmem_wait_ld();
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            uint32_t a[32];
-            tmem_ld32(tmem + lane_off + COL_S + h2 * 32, a);
-            tmem_wait_ld();
+          for (int c = 0; c < 8; ++c) {
+            const float4 lv = l4[c];
+            const float lv4[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const float4 lv = l4[h2 * 8 + c];
-              const float lv4[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                pr[h2 * 32 + c * 4 + e] =
-                    kv_ok ? ex2(fmaf(__uint_as_float(a[c * 4 + e]), sl2, -lv4[e])) : 0.f;
-            }
+            for (int e = 0; e < 4; ++e)
+              pr[c * 4 + e] = kv_ok ? ex2(fmaf(__uint_as_float(a[c * 4 + e]), sl2, -lv4[e])) : 0.f;
           }
-          uint32_t pk[32];
+          uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pr[2 * c], pr[2 * c + 1]);
-          tmem_st32(tmem + lane_off + COL_S, pk);
+          for (int c = 0; c < 16; ++c) pk[c] = pack_bf16(pr[2 * c], pr[2 * c + 1]);
+          // P over this warp's own score columns only (the other half may not be read yet)
+          tmem_st16(tmem + lane_off + COL_S + ch * 32, pk);
           tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.p_ready);
-        // dS^T row = P^T * (dP^T - Di)
+        // dS^T = P^T * (dP^T - Di)
         if (!mbar_wait(&bars.dp_full, dpph, ctl, 22)) goto done;
         dpph ^= 1;
         tc_fence_after();
         {
-          const float4 *d4 = reinterpret_cast<const float4 *>(di_s + s * 64);
+          const float4 *d4 = reinterpret_cast<const float4 *>(di_s + s * 64 + ch * 32);
+          uint32_t a[32];
+          tmem_ld32(tmem + lane_off + COL_DP + ch * 32, a);
+          tmem_wait_ld();
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            uint32_t a[32];
-            tmem_ld32(tmem + lane_off + COL_DP + h2 * 32, a);
-            tmem_wait_ld();
+          for (int c = 0; c < 8; ++c) {
+            const float4 dv = d4[c];
+            const float dv4[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const float4 dv = d4[h2 * 8 + c];
-              const float dv4[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int col = h2 * 32 + c * 4 + e;
-                pr[col] = pr[col] * (__uint_as_float(a[c * 4 + e]) - dv4[e]);
-              }
-            }
+            for (int e = 0; e < 4; ++e)
+              pr[c * 4 + e] = pr[c * 4 + e] * (__uint_as_float(a[c * 4 + e]) - dv4[e]);
           }
-          uint32_t pk[32];
+          uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pr[2 * c], pr[2 * c + 1]);
-          tmem_st32(tmem + lane_off + COL_DP, pk);
+          for (int c = 0; c < 16; ++c) pk[c] = pack_bf16(pr[2 * c], pr[2 * c + 1]);
+          tmem_st16(tmem + lane_off + COL_DP + ch * 32, pk);
           // dS^T into shared memory (MN-major operand of the dQ^T product).
           if (!mbar_wait(&bars.ds_free, dsfph ^ 1, ctl, 23)) goto done;
           dsfph ^= 1;
           uint8_t *row = smem + C::OFF_DS + r * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4 *>(row + ((j ^ (r & 7)) << 4)) =
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4 *>(row + (((ch * 4 + j) ^ (r & 7)) << 4)) =
                 make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
           fence_async_smem();
           tmem_wait_st();
@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
           mbar_arrive(&bars.stage_empty[s]);  // done with this stage's LSE / Di
         }
       }
-      // dK, dV epilogue for this tile's key rows.
+      // dK, dV epilogue for this tile's key rows (this warp's half of D).
       if (!mbar_wait(&bars.dkdv_full, dkdvph, ctl, 24)) goto done;
       dkdvph ^= 1;
       tc_fence_after();
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
           const float mul = which ? p.scale : 1.f;
           uint4 *dst = which ? dkp : dvp;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = ch * (D / 64); c < (ch + 1) * (D / 64); ++c) {
             uint32_t v[32];
             tmem_ld32(tmem + lane_off + (which ? COL_DK : COL_DV) + c * 32, v);
             tmem_wait_ld();
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(384, 1) jfa_bwd_kernel(const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.dkdv_free);
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 12) {
     // ---------------------------------- LSE / Di staging and dQ reduction
     // Per query block, ahead of the compute warps: LSE and Di = rowsum(dO * O)
     // of the block's 64 rows (two threads per row, O read from global memory
@@ -566,7 +566,7 @@ done:
     while (!mbar_try_wait(&bars.drain, 0) && globaltimer() - t0 < p.timeout_ns) {
     }
   }
-  if (warp >= 8 && lane == 0) bulk_wait<0>();
+  if (warp >= 8 && warp < 12 && lane == 0) bulk_wait<0>();
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
@@ -581,7 +581,7 @@ cudaError_t launch_t(const BwdParams &p, int num_sms, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, 384, BwdCfg<D>::SMEM, st>>>(p);
+  kern<<<num_sms, 512, BwdCfg<D>::SMEM, st>>>(p);
   return cudaGetLastError();
 }
 
