@@ -30,6 +30,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 
+# DRAM bytes (read + write) of one GEM backward launch, from an ncu capture of
+# the first 256 sequences (dram__bytes_read.sum + dram__bytes_write.sum)
+# scaled by the processed (key tile, query block) pairs. Reset to None
+# whenever the backward kernel changes until it is measured again.
+BWD_GEM_TRAFFIC = 4.18e9
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -114,15 +121,15 @@ def cpu_baseline(budget_s=12.0, lengths=None, H=4, D=128):
     from jagged_flash_attention_flashattention_gb300 import workloads as W
     from oracle import attention as A
 
-    L = _gem_lengths() if lengths is None else lengths
-    inp = W.jagged_inputs(L[:64], H, D, W.SEEDS["gem"], device="cpu")
+    L = (_gem_lengths() if lengths is None else lengths)[:256]
+    inp = W.jagged_inputs(L, H, D, W.SEEDS["gem"], device="cpu")
     q, k, v, do = (inp[n].double().numpy() for n in ("q", "k", "v", "do"))
-    offs = W.offsets_of(L[:64])
+    offs = W.offsets_of(L)
     s = 1 / np.sqrt(D)
     t0 = time.perf_counter()
     flops = 0.0
     n = 0
-    while n < len(L[:64]) and time.perf_counter() - t0 < budget_s:
+    while n < len(L) and time.perf_counter() - t0 < budget_s:
         a, e = int(offs[n]), int(offs[n + 1])
         for h in range(H):
             A.seq_fwd(q[a:e, h], k[a:e, h], v[a:e, h], s)
@@ -209,7 +216,7 @@ def _setup(name, rank, dev, seqs=0):
 
         st["check"] = lambda: st["plan"].check()
     else:
-        B, L = cfg["B"], cfg["L"]
+        B, L = (seqs or cfg["B"]), cfg["L"]
         inp = W.blockdiag_inputs(B, L, H, D, W.SEEDS[name] + 1000 * rank, device=dev)
         st["fwd_flops"] = W.useful_flops("blockdiag", H=H, D=D, B=B, L=L)
         st["fwd_bytes"] = 4 * B * L * H * D * 2
@@ -306,7 +313,8 @@ def run_ours(args):
         else:
             roof = {"bound": "tensor", "kernel": "jfa_bwd (bwd kernel + dQ cast)",
                     "achieved": round(bwd_tf, 1), "peak": peak, "unit": "TFLOP/s",
-                    "frac": round(bwd_tf / peak, 4), "traffic": None,
+                    "frac": round(bwd_tf / peak, 4),
+                    "traffic": BWD_GEM_TRAFFIC if args.config == "gem" and not args.seqs else None,
                     "peak_source": peak_src + " bf16 burst (cuBLAS)"}
         line = {
             "metric": "useful TFLOP/s fwd+bwd (jagged attention, bf16) and % of GB300 bf16 tensor peak",
@@ -393,7 +401,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seqs", type=int, default=0,
-                    help="jagged workloads: keep only the first N sequences (small profiling case)")
+                    help="keep only the first N sequences (jagged) or N batch rows (block-diagonal): "
+                         "a small profiling case")
     ap.add_argument("--config", default="gem",
                     choices=["gem", "stress", "bcast", "blockdiag", "blockdiag64", "tiny"])
     args = ap.parse_args()

@@ -8,7 +8,7 @@ sorted by their KV workload in descending order and dealt to the SMs in a
 zigzag (boustrophedon) pattern: even passes fill the SMs left to right, odd
 passes right to left.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * a tile is (b, h, m): sequence b, head h, row block m of `tile_rows` rows;
   sequence b has ceil(rows_b / tile_rows) row blocks;
