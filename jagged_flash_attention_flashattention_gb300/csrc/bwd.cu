@@ -20,24 +20,26 @@
 //   dP^T = V dO^T                                            -> TMEM
 //   P^T, dS^T computed by the compute warps (one key row per thread);
 //   LSE and Di = rowsum(dO * O) of the block's 64 query rows are formed
-//   inline, one block ahead, by the dQ warps (O rows read from global
-//   memory, dO from the stage; no separate pass);
+//   inline by the dQ warps, two blocks ahead of their dQ reduction (O rows
+//   read from global memory, dO from the stage; no separate pass);
 //   dV  += P^T dO       (A = P^T bf16 from TMEM)
 //   dK  += dS^T Q       (A = dS^T bf16 from TMEM)
 //   dQ^T = K^T dS^T     (both operands MN-major in shared memory)  -> TMEM
-// The dQ group reads dQ^T out of TMEM (one head-dim lane per thread),
-// releases the TMEM at once, scales, stages 32x32 fp32 boxes in shared
-// memory (two buffers per warp) and adds them into an fp32 accumulator in
-// global memory with TMA reduce-add: a workspace accumulator that a light
-// kernel casts to bf16 at the end (jagged), or the caller's fp32 dQ itself
-// (broadcast-Q, where dQ is a sum over the whole batch).
+// The dQ group reads dQ^T out of TMEM (one head-dim lane per thread; two
+// TMEM buffers, so the next block's dQ^T product does not wait for the
+// reduction), releases the TMEM at once, scales, stages 32x32 fp32 boxes in
+// a 4 KB shared-memory buffer per warp and adds them into an fp32
+// accumulator in global memory with TMA reduce-add: a workspace accumulator
+// that a light kernel casts to bf16 at the end (jagged), or the caller's
+// fp32 dQ itself (broadcast-Q, where dQ is a sum over the whole batch).
+// dK and dV leave TMEM once per tile, written with 32-byte stores.
 //
 // Roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
 // warps 4-7 and 12-15 compute + dK/dV epilogue (two warps per TMEM lane
 // quarter, each on half of the query columns), warps 8-11 LSE/Di staging +
 // dQ reduction.
 // Tensor memory columns: dV [0,128) dK [128,256) S/P [256,320)
-// dP/dS [320,384) dQ^T [384,448).
+// dP/dS [320,384) dQ^T [384,512) (two buffers).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -78,7 +80,7 @@ struct BwdBars {
   uint64_t kv_full, kv_empty;
   uint64_t stage_full[8], stage_empty[8], aux_full[8];
   uint64_t s_full, dp_full, p_ready, ds_ready, ds_free;
-  uint64_t dq_full, dq_free;
+  uint64_t dq_full[2], dq_free[2];  // dQ^T double-buffered in TMEM
   uint64_t dkdv_full, dkdv_free;
   uint64_t drain;
   uint32_t tmem_base;
@@ -175,8 +177,10 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     mbar_init(&bars.p_ready, 8);
     mbar_init(&bars.ds_ready, 8);
     mbar_init(&bars.ds_free, 1);
-    mbar_init(&bars.dq_full, 1);
-    mbar_init(&bars.dq_free, 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars.dq_full[x], 1);
+      mbar_init(&bars.dq_free[x], 4);
+    }
     mbar_init(&bars.dkdv_full, 1);
     mbar_init(&bars.dkdv_free, 8);
     mbar_init(&bars.drain, 1);
@@ -210,8 +214,13 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     if (lane == 0) {
       uint32_t kvph = 0, eph = 0;
       int qb = 0;
+      // The next tile is decoded one tile ahead (its index loads are off the
+      // critical path at the tile switch).
+      BwdTile nxt{};
+      if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
       for (int t = tbeg; t < tend; ++t) {
-        const BwdTile tl = decode_tile<BCAST>(p, t);
+        const BwdTile tl = nxt;
+        if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
         if (tl.nq == 0 || tl.nkv <= 0) continue;
         if (!mbar_wait(&bars.kv_empty, kvph ^ 1, ctl, 1)) goto done;
         kvph ^= 1;
@@ -268,8 +277,13 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
           mma_ts(tmem + dcol, tmem + acol + (k >> 1) * 32 + (k & 1) * 8, yd + (k * 2048 >> 4),
                  C::IDESC_G, (acc || k > 0) ? 1u : 0u);
       };
+      // The next tile is decoded one tile ahead (its index loads are off the
+      // critical path at the tile switch).
+      BwdTile nxt{};
+      if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
       for (int t = tbeg; t < tend; ++t) {
-        const BwdTile tl = decode_tile<BCAST>(p, t);
+        const BwdTile tl = nxt;
+        if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
         if (tl.nq == 0 || tl.nkv <= 0) continue;
         if (!mbar_wait(&bars.kv_full, kvph, ctl, 10)) goto done;
         kvph ^= 1;
@@ -308,14 +322,15 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
           tc_fence_after();
           issue_grad(COL_DK, COL_DP, st_mn + q_off, i > 0);
           mma_commit(&bars.stage_empty[s]);
-          if (!mbar_wait(&bars.dq_free, dqfph ^ 1, ctl, 16)) goto done;
-          dqfph ^= 1;
+          const int qbuf = qb & 1;
+          if (!mbar_wait(&bars.dq_free[qbuf], bit(dqfph, qbuf) ^ 1, ctl, 16)) goto done;
+          dqfph ^= 1u << qbuf;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + COL_DQ, kT_mn + (k * 2048 >> 4), ds_mn + (k * 2048 >> 4), C::IDESC_Q,
-                   k > 0);
-          mma_commit(&bars.dq_full);
+            mma_ss(tmem + COL_DQ + qbuf * 64, kT_mn + (k * 2048 >> 4), ds_mn + (k * 2048 >> 4),
+                   C::IDESC_Q, k > 0);
+          mma_commit(&bars.dq_full[qbuf]);
           mma_commit(&bars.ds_free);
           if (more) {
             issue_xyT(COL_DP, v_kmaj, st_kmaj + q2_off + (C::QT >> 4));
@@ -338,8 +353,13 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     const float sl2 = p.scale_log2;
     uint32_t aph = 0, sph = 0, dpph = 0, dsfph = 0, dkdvph = 0;
     int qb = 0;
+    // The next tile is decoded one tile ahead (its index loads are off the
+    // critical path at the tile switch).
+    BwdTile nxt{};
+    if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
     for (int t = tbeg; t < tend; ++t) {
-      const BwdTile tl = decode_tile<BCAST>(p, t);
+      const BwdTile tl = nxt;
+      if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
       if (tl.nq == 0 || tl.nkv <= 0) continue;
       const bool kv_ok = r < tl.nkv;
       for (int i = 0; i < tl.nq; ++i, ++qb) {
@@ -425,19 +445,22 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
         for (int which = 0; which < 2; ++which) {
           const float mul = which ? p.scale : 1.f;
           uint4 *dst = which ? dkp : dvp;
-#pragma unroll 1
-          for (int c = ch * (D / 64); c < (ch + 1) * (D / 64); ++c) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + (which ? COL_DK : COL_DV) + c * 32, v);
-            tmem_wait_ld();
-            if (kv_ok) {
+          // This warp's half of D: both 32-column chunks in flight at once.
+          uint32_t v[D / 64][32];
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc)
+            tmem_ld32(tmem + lane_off + (which ? COL_DK : COL_DV) + (ch * (D / 64) + cc) * 32, v[cc]);
+          tmem_wait_ld();
+          if (kv_ok) {
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
               uint32_t pk[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                pk[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                dst[c * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                pk[e] = pack_bf16(__uint_as_float(v[cc][2 * e]) * mul, __uint_as_float(v[cc][2 * e + 1]) * mul);
+              const int c = ch * (D / 64) + cc;
+              st_global_v8(dst + c * 4, pk);
+              st_global_v8(dst + c * 4 + 2, pk + 8);
             }
           }
         }
@@ -476,19 +499,24 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
         for (int j = 0; j < NV; ++j) o_r[j] = __ldg(src + j);
       }
     };
-    auto reduce_dq = [&](const BwdTile &tl, int i) -> bool {
-      if (!mbar_wait(&bars.dq_full, dqph, ctl, 30)) return false;
-      dqph ^= 1;
+    // One pending dQ reduction: head, first query row in the accumulator, rows.
+    struct DqJob {
+      int h, row0, rows;
+    };
+    auto reduce_dq = [&](const DqJob &jb, int qbr) -> bool {
+      const int qbuf = qbr & 1;
+      if (!mbar_wait(&bars.dq_full[qbuf], bit(dqph, qbuf), ctl, 30)) return false;
+      dqph ^= 1u << qbuf;
       tc_fence_after();
       uint32_t v[2][32];
-      tmem_ld32(tmem + lane_off + COL_DQ, v[0]);
-      tmem_ld32(tmem + lane_off + COL_DQ + 32, v[1]);
+      tmem_ld32(tmem + lane_off + COL_DQ + qbuf * 64, v[0]);
+      tmem_ld32(tmem + lane_off + COL_DQ + qbuf * 64 + 32, v[1]);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.dq_free);  // TMEM released before the reduction
+      if (lane == 0) mbar_arrive(&bars.dq_free[qbuf]);  // TMEM released before the reduction
       if (wq * 32 >= D) return true;               // D = 64: lanes 64..127 are padding
-      const int rows = min(64, tl.Lq - i * 64);
+      const int rows = jb.rows;
 #pragma unroll
       for (int qc = 0; qc < 2; ++qc) {
         if (qc * 32 >= rows) break;
@@ -499,7 +527,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_3d(&p.tm_dqacc, stg, wq * 32, tl.h, tl.q_row0 + i * 64 + qc * 32);
+          tma_reduce_add_3d(&p.tm_dqacc, stg, wq * 32, jb.h, jb.row0 + qc * 32);
           bulk_commit();
         }
       }
@@ -511,9 +539,10 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     cur.i = 0;
     cur.seek(p);
     if (cur.valid) prefetch(cur);
-    bool have_prev = false;
-    BwdTile prev_tl = cur.tl;
-    int prev_i = 0;
+    // Two blocks in flight between LSE/Di staging and the dQ reduction, so the
+    // staging of block n runs ahead of the reduction of block n - 2.
+    bool have0 = false, have1 = false;
+    DqJob job0{0, 0, 0}, job1{0, 0, 0};
     while (cur.valid) {
       const int s = qb % C::NSTAGE;
       if (!mbar_wait(&bars.stage_full[s], bit(fph, s), ctl, 31)) goto done;
@@ -549,14 +578,16 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       BlockIter<BCAST> nx = cur;
       nx.next(p);
       if (nx.valid) prefetch(nx);
-      if (have_prev && !reduce_dq(prev_tl, prev_i)) goto done;
-      prev_tl = cur.tl;
-      prev_i = cur.i;
-      have_prev = true;
+      if (have0 && !reduce_dq(job0, qb - 2)) goto done;
+      job0 = job1;
+      have0 = have1;
+      job1 = DqJob{cur.tl.h, cur.tl.q_row0 + cur.i * 64, min(64, cur.tl.Lq - cur.i * 64)};
+      have1 = true;
       cur = nx;
       ++qb;
     }
-    if (have_prev && !reduce_dq(prev_tl, prev_i)) goto done;
+    if (have0 && !reduce_dq(job0, qb - 2)) goto done;
+    if (have1 && !reduce_dq(job1, qb - 1)) goto done;
     if (lane == 0) bulk_wait<0>();
   }
 done:

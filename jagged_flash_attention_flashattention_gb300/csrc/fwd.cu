@@ -46,11 +46,12 @@ using namespace dev;
 template <int D>
 struct FwdCfg {
   static constexpr int TILE_BYTES = 128 * D * 2;  // one 128-row Q, K or V tile
-  static constexpr int NSLOT = D == 128 ? 4 : 8;  // K/V ring depth
+  static constexpr int NSLOT = D == 128 ? 5 : 8;  // K/V ring depth
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = 2 * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE_BYTES;
   static constexpr int SMEM = OFF_BAR + 512 + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
   static constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, 0, 0);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, 0, 1);
 };
@@ -152,8 +153,13 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       uint32_t qph = 0;
       int slot = 0;
       uint32_t sph = 0;
+      // The next tile is decoded one tile ahead (its index loads are off the
+      // critical path at the tile switch).
+      FwdTile nxt{};
+      if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
       for (int t = tbeg; t < tend; ++t) {
-        const FwdTile tl = decode_tile<BCAST>(p, t);
+        const FwdTile tl = nxt;
+        if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
         if (tl.n_kv == 0) continue;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
@@ -211,8 +217,13 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, vd + (k * 2048 >> 4), C::IDESC_PV,
                  (acc || k > 0) ? 1u : 0u);
       };
+      // The next tile is decoded one tile ahead (its index loads are off the
+      // critical path at the tile switch).
+      FwdTile nxt{};
+      if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
       for (int t = tbeg; t < tend; ++t) {
-        const FwdTile tl = decode_tile<BCAST>(p, t);
+        const FwdTile tl = nxt;
+        if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
         if (tl.n_kv == 0) continue;
         const uint32_t has = (tl.nrows0 > 0 ? 1u : 0u) | (tl.nrows1 > 0 ? 2u : 0u);
 #pragma unroll
@@ -278,8 +289,13 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
     const float sl2 = p.scale_log2;
     uint32_t sph = 0, oph = 0;
     __nv_bfloat16 *obase = static_cast<__nv_bfloat16 *>(p.o);
+    // The next tile is decoded one tile ahead (its index loads are off the
+    // critical path at the tile switch).
+    FwdTile nxt{};
+    if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
     for (int t = tbeg; t < tend; ++t) {
-      const FwdTile tl = decode_tile<BCAST>(p, t);
+      const FwdTile tl = nxt;
+      if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
       const int nrows = x ? tl.nrows1 : tl.nrows0;
       if (nrows == 0) continue;
       const bool row_ok = r < nrows;
@@ -364,19 +380,22 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       {
         const float inv_l = 1.f / l_run;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
+        for (int c = 0; c < D / 32; c += 2) {  // two 32-column chunks in flight
+          uint32_t o[2][32];
+          tmem_ld32(tO + c * 32, o[0]);
+          tmem_ld32(tO + c * 32 + 32, o[1]);
           tmem_wait_ld();
           if (row_ok) {
-            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l,
-                                __uint_as_float(o[2 * i + 1]) * inv_l);
+            for (int h = 0; h < 2; ++h) {
+              uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              optr[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16(__uint_as_float(o[h][2 * i]) * inv_l,
+                                  __uint_as_float(o[h][2 * i + 1]) * inv_l);
+              st_global_v8(optr + (c + h) * 4, pk);
+              st_global_v8(optr + (c + h) * 4 + 2, pk + 8);
+            }
           }
         }
         if (row_ok) p.lse[tl.lse0 + x * 128 + r] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
