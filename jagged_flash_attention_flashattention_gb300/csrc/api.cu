@@ -53,14 +53,14 @@ jfa_status map_rows_bf16(CUtensorMap *m, const void *base, int64_t rows, int H, 
   return JFA_OK;
 }
 
-// fp32 [rows, H, D] as {D, H, rows}; box {32, 1, 32}, no swizzle.
+// fp32 [rows, H, D] as {D, H, rows}; box {32, 1, 64}, no swizzle.
 jfa_status map_acc_f32(CUtensorMap *m, void *base, int64_t rows, int H, int D) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return fail(JFA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   if (rows < 1) rows = 1;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
-  cuuint32_t box[3] = {32, 1, 32};
+  cuuint32_t box[3] = {32, 1, 64};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

@@ -15,7 +15,8 @@
 // A tile is 128 key rows of one (sequence, head). dK and dV for those rows
 // stay in tensor memory while the kernel walks every 64-row query block of
 // the sequence (or the dense Q for broadcast-Q); Q and dO blocks stream
-// through a 4-deep ring of shared-memory stages. Per query block:
+// through a ring of shared-memory stages (3 deep at D = 128, 7 at D = 64).
+// Per query block:
 //   S^T  = K Q^T        (M=128 keys, N=64 queries, K=D)      -> TMEM
 //   dP^T = V dO^T                                            -> TMEM
 //   P^T, dS^T computed by the compute warps (one key row per thread);
@@ -27,11 +28,12 @@
 //   dQ^T = K^T dS^T     (both operands MN-major in shared memory)  -> TMEM
 // The dQ group reads dQ^T out of TMEM (one head-dim lane per thread; two
 // TMEM buffers, so the next block's dQ^T product does not wait for the
-// reduction), releases the TMEM at once, scales, stages 32x32 fp32 boxes in
-// a 4 KB shared-memory buffer per warp and adds them into an fp32
-// accumulator in global memory with TMA reduce-add: a workspace accumulator
-// that a light kernel casts to bf16 at the end (jagged), or the caller's
-// fp32 dQ itself (broadcast-Q, where dQ is a sum over the whole batch).
+// reduction), releases the TMEM at once, scales, stages its 64 x 32 fp32
+// box in an 8 KB shared-memory buffer and adds it with a single TMA
+// reduce-add (fewer, larger reductions measured faster than 32-row ones)
+// into an fp32 accumulator in global memory: a workspace accumulator that a
+// light kernel casts to bf16 at the end (jagged), or the caller's fp32 dQ
+// itself (broadcast-Q, where dQ is a sum over the whole batch).
 // dK and dV leave TMEM once per tile, written with 32-byte stores.
 //
 // Roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
@@ -55,15 +57,15 @@ struct BwdCfg {
   static constexpr int KV_TILE = 128 * D * 2;  // 128-row K or V tile
   static constexpr int QT = 64 * D * 2;        // 64-row Q or dO tile
   static constexpr int QCHUNK = 64 * 128;      // one 64-column box of a 64-row tile
-  static constexpr int NSTAGE = D == 128 ? 4 : 8;
+  static constexpr int NSTAGE = D == 128 ? 3 : 7;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_TILE;
   static constexpr int OFF_ZERO = 2 * KV_TILE;  // D = 64: zero rows padding K^T to M = 128
   static constexpr int ZERO_BYTES = D == 64 ? 16384 : 0;
   static constexpr int OFF_STAGE = OFF_ZERO + ZERO_BYTES;  // NSTAGE x (Q, dO)
   static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 2 * QT;  // 128x64 bf16 dS^T
-  static constexpr int OFF_DQS = OFF_DS + 16384;               // dQ staging: 4 warps x 4 KB
-  static constexpr int OFF_LSE = OFF_DQS + 16384;              // [NSTAGE][64] log2 units
+  static constexpr int OFF_DQS = OFF_DS + 16384;               // dQ staging: 4 warps x 8 KB
+  static constexpr int OFF_LSE = OFF_DQS + 32768;              // [NSTAGE][64] log2 units
   static constexpr int OFF_DI = OFF_LSE + NSTAGE * 256;        // [NSTAGE][64]
   static constexpr int OFF_BAR = OFF_DI + NSTAGE * 256;
   static constexpr int SMEM = OFF_BAR + 512;
@@ -481,7 +483,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     const int rt = threadIdx.x - 256;
     const int row = rt >> 1, half = rt & 1;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    float *stg = reinterpret_cast<float *>(smem + C::OFF_DQS + wq * 4096);
+    float *stg = reinterpret_cast<float *>(smem + C::OFF_DQS + wq * 8192);
     const __nv_bfloat16 *obase = static_cast<const __nv_bfloat16 *>(p.o);
     uint32_t fph = 0, dqph = 0;
     int qb = 0;
@@ -516,20 +518,18 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.dq_free[qbuf]);  // TMEM released before the reduction
       if (wq * 32 >= D) return true;               // D = 64: lanes 64..127 are padding
-      const int rows = jb.rows;
+      (void)jb.rows;  // rows past the sequence carry zeros (P = 0 there)
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
 #pragma unroll
-      for (int qc = 0; qc < 2; ++qc) {
-        if (qc * 32 >= rows) break;
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
+      for (int qc = 0; qc < 2; ++qc)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) stg[j * 32 + lane] = __uint_as_float(v[qc][j]) * p.scale;
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_3d(&p.tm_dqacc, stg, wq * 32, jb.h, jb.row0 + qc * 32);
-          bulk_commit();
-        }
+        for (int j = 0; j < 32; ++j) stg[(qc * 32 + j) * 32 + lane] = __uint_as_float(v[qc][j]) * p.scale;
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(&p.tm_dqacc, stg, wq * 32, jb.h, jb.row0);
+        bulk_commit();
       }
       return true;
     };

@@ -37,7 +37,7 @@ struct BwdParams {
   CUtensorMap tm_do;  // bf16 dO rows (same row space as O), box {64, 1, 64}
   CUtensorMap tm_k;   // bf16 [Tk, H, D], box {64, 1, 128}
   CUtensorMap tm_v;
-  CUtensorMap tm_dqacc;  // fp32 [rows, H, D] as {D, H, rows}, box {32, 1, 32}, no swizzle
+  CUtensorMap tm_dqacc;  // fp32 [rows, H, D] as {D, H, rows}, box {32, 1, 64}, no swizzle
   const void *offsets;
   int idx64;
   const int32_t *sm_ptr;
