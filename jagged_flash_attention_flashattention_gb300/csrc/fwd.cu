@@ -14,7 +14,8 @@
 // multi-buffered K/V; score, P and softmax state sharing one tensor-memory
 // allocation while the PV accumulator keeps its own):
 //
-//   warp 0       TMA producer: Q halves, then K/V tiles into a ring of slots
+//   warp 0       TMA producer: Q halves, then K/V tiles into a ring of pair
+//                slots (K_j with V_{j-1}: one barrier per K/V step)
 //   warp 1       MMA issuer: S = Q K^T into TMEM, O += P V from TMEM P
 //   warp 2       owns the tensor-memory allocation
 //   warps 4-7    softmax + correction + epilogue for query rows   0..127
@@ -46,10 +47,13 @@ using namespace dev;
 template <int D>
 struct FwdCfg {
   static constexpr int TILE_BYTES = 128 * D * 2;  // one 128-row Q, K or V tile
-  static constexpr int NSLOT = D == 128 ? 5 : 8;  // K/V ring depth
+  // K/V ring of pair slots: the slot of K/V step j holds K_j and V_{j-1},
+  // the two tiles that step j's products read, so one barrier covers both.
+  static constexpr int NSLOT = D == 128 ? 2 : 4;
+  static constexpr int PAIR_BYTES = 2 * TILE_BYTES;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = 2 * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + NSLOT * PAIR_BYTES;
   static constexpr int SMEM = OFF_BAR + 512 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
   static constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, 0, 0);
@@ -171,18 +175,21 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
             tma_load_3d(smem + C::OFF_Q + x * C::TILE_BYTES + c * 16384, &p.tm_q,
                         &bars.q_full[x], c * 64, tl.h, tl.q_coord + x * 128);
         }
-        for (int j = 0; j < tl.n_kv; ++j) {
-          for (int kv = 0; kv < 2; ++kv) {
-            if (!mbar_wait(&slot_empty[slot], sph ^ 1, ctl, 2)) goto done;
-            mbar_arrive_expect_tx(&slot_full[slot], C::TILE_BYTES);
-            for (int c = 0; c < D / 64; ++c)
-              tma_load_3d(smem + C::OFF_RING + slot * C::TILE_BYTES + c * 16384,
-                          kv ? &p.tm_v : &p.tm_k, &slot_full[slot], c * 64, tl.h,
-                          tl.kv0 + j * 128);
-            if (++slot == C::NSLOT) {
-              slot = 0;
-              sph ^= 1;
-            }
+        for (int j = 0; j <= tl.n_kv; ++j) {  // slot of step j: K_j (j < n) and V_{j-1} (j > 0)
+          if (!mbar_wait(&slot_empty[slot], sph ^ 1, ctl, 2)) goto done;
+          const bool k_in = j < tl.n_kv, v_in = j > 0;
+          mbar_arrive_expect_tx(&slot_full[slot], (k_in + v_in) * C::TILE_BYTES);
+          uint8_t *dst = smem + C::OFF_RING + slot * C::PAIR_BYTES;
+          for (int c = 0; c < D / 64; ++c) {
+            if (k_in)
+              tma_load_3d(dst + c * 16384, &p.tm_k, &slot_full[slot], c * 64, tl.h, tl.kv0 + j * 128);
+            if (v_in)
+              tma_load_3d(dst + C::TILE_BYTES + c * 16384, &p.tm_v, &slot_full[slot], c * 64, tl.h,
+                          tl.kv0 + (j - 1) * 128);
+          }
+          if (++slot == C::NSLOT) {
+            slot = 0;
+            sph ^= 1;
           }
         }
       }
@@ -203,7 +210,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       const uint64_t ring_vdesc = sdesc_sw128(ring, 16384, 1024);
       auto issue_qk = [&](int x, int kslot) {
         const uint64_t qd = q_desc + (uint64_t)(x * (C::TILE_BYTES >> 4));
-        const uint64_t kd = ring_kdesc + (uint64_t)(kslot * (C::TILE_BYTES >> 4));
+        const uint64_t kd = ring_kdesc + (uint64_t)(kslot * (C::PAIR_BYTES >> 4));
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
         }
       };
       auto issue_pv = [&](int x, int vslot, bool acc) {
-        const uint64_t vd = ring_vdesc + (uint64_t)(vslot * (C::TILE_BYTES >> 4));
+        const uint64_t vd = ring_vdesc + (uint64_t)((vslot * C::PAIR_BYTES + C::TILE_BYTES) >> 4);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, vd + (k * 2048 >> 4), C::IDESC_PV,
@@ -232,30 +239,24 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           if (!mbar_wait(&bars.q_full[x], (qph >> x) & 1, ctl, 10)) goto done;
           qph ^= 1u << x;
         }
-        // S_0 for both halves.
-        int kslot = slot;
-        if (!mbar_wait(&slot_full[kslot], sph, ctl, 11)) goto done;
-        if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
+        // S_0 for both halves (slot of step 0: K_0 only).
+        if (!mbar_wait(&slot_full[slot], sph, ctl, 11)) goto done;
         tc_fence_after();
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           if (!(has >> x & 1)) continue;
-          issue_qk(x, kslot);
+          issue_qk(x, slot);
           mma_commit(&bars.s_full[x]);
           if (tl.n_kv == 1) mma_commit(&bars.q_empty[x]);
         }
-        mma_commit(&slot_empty[kslot]);
+        mma_commit(&slot_empty[slot]);
+        if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
         for (int j = 1; j <= tl.n_kv; ++j) {
-          // V_{j-1}
-          const int vslot = slot;
-          if (!mbar_wait(&slot_full[vslot], sph, ctl, 12)) goto done;
+          // One slot: V_{j-1}, and K_j unless this is the last step.
+          const int ps = slot;
+          if (!mbar_wait(&slot_full[ps], sph, ctl, 12)) goto done;
           if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
-          kslot = -1;
-          if (j < tl.n_kv) {
-            kslot = slot;
-            if (!mbar_wait(&slot_full[kslot], sph, ctl, 13)) goto done;
-            if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
-          }
+          const bool more = j < tl.n_kv;
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
             if (!(has >> x & 1)) continue;
@@ -266,16 +267,15 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
               oph ^= 1u << x;
             }
             tc_fence_after();
-            issue_pv(x, vslot, j > 1);
+            issue_pv(x, ps, j > 1);
             if (j == tl.n_kv) mma_commit(&bars.o_full[x]);
-            if (kslot >= 0) {
-              issue_qk(x, kslot);
+            if (more) {
+              issue_qk(x, ps);
               mma_commit(&bars.s_full[x]);
               if (j == tl.n_kv - 1) mma_commit(&bars.q_empty[x]);
             }
           }
-          mma_commit(&slot_empty[vslot]);
-          if (kslot >= 0) mma_commit(&slot_empty[kslot]);
+          mma_commit(&slot_empty[ps]);
         }
       }
     }
