@@ -480,8 +480,11 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     constexpr int ND = D / 2;  // head-dim elements per thread for Di
     constexpr int NV = ND / 8;
     const int wq = warp & 3;
-    const int rt = threadIdx.x - 256;
-    const int row = rt >> 1, half = rt & 1;
+    // Two threads per row, the row's halves eight lanes apart: the eight lanes
+    // of a quarter-warp read eight different rows of the swizzled dO tile, so
+    // their 16-byte chunks fall in eight different bank groups.
+    const int row = wq * 16 + (lane & 7) + ((lane >> 4) << 3);
+    const int half = (lane >> 3) & 1;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     float *stg = reinterpret_cast<float *>(smem + C::OFF_DQS + wq * 8192);
     const __nv_bfloat16 *obase = static_cast<const __nv_bfloat16 *>(p.o);
@@ -567,7 +570,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
             }
           }
         }
-        di += __shfl_xor_sync(0xffffffffu, di, 1);
+        di += __shfl_xor_sync(0xffffffffu, di, 8);
         if (half == 0) {
           lse_s[s * 64 + row] = row_ok ? lse_r * 1.4426950408889634f : INFINITY;
           di_s[s * 64 + row] = row_ok ? di : 0.f;
