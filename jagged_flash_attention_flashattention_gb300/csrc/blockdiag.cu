@@ -27,7 +27,10 @@
 // (P^T, dS^T read MN-major) and dQ = dS K (dS read K-major) are fresh
 // products in TMEM. Input tiles go through a 5-slot ring loaded in the order
 // they are released (V after dP, dO after dV, Q after dK, K after dQ), so
-// the next unit's loads start while this unit computes.
+// the next unit's loads start while this unit computes. The epilogue drains
+// dK, dV and dQ in that order and releases each TMEM region as soon as it is
+// read, so the next unit's dP and S products overlap the rest of the stores
+// (32 bytes per lane).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -293,7 +296,8 @@ enum { T_V = 0, T_DO = 1, T_Q = 2, T_K = 3 };  // ring load order = release orde
 
 struct BBars {
   uint64_t full[8], empty[8];
-  uint64_t s_full, dp_full, ps_ready, ps_free, g_full, g_free;
+  uint64_t s_full, dp_full, ps_ready, ps_free, g_full;
+  uint64_t dk_free, dv_free, dq_free;  // epilogue has drained that TMEM region
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -317,7 +321,9 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
     mbar_init(&bars.ps_ready, 4);
     mbar_init(&bars.ps_free, 1);
     mbar_init(&bars.g_full, 1);
-    mbar_init(&bars.g_free, 4);
+    mbar_init(&bars.dk_free, 4);
+    mbar_init(&bars.dv_free, 4);
+    mbar_init(&bars.dq_free, 4);
     mbar_init(&bars.drain, 1);
     bars.abort_flag = 0;
     fence_mbar_init();
@@ -361,7 +367,7 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      uint32_t fph = 0, psr = 0, psf = 0, gf = 0;
+      uint32_t fph = 0, psr = 0, psf = 0, kf = 0, vf = 0, qf = 0;
       const uint32_t ring = smem_u32(smem + C::OFF_RING);
       const uint32_t pa = smem_u32(smem + C::OFF_P), dsa = smem_u32(smem + C::OFF_DS);
       int slot = 0;
@@ -387,13 +393,18 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
         }
       };
       for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        if (!mbar_wait(&bars.g_free, gf ^ 1, ctl, 20)) goto done;  // previous epilogue drained TMEM
-        gf ^= 1;
+        // Each product region is reused as soon as the previous unit's epilogue
+        // has drained it (dK, then dV, then dQ), so this unit's dP and S run
+        // while the rest of the previous epilogue is still being written.
+        if (!mbar_wait(&bars.dk_free, kf ^ 1, ctl, 20)) goto done;
+        kf ^= 1;
         if (!wait_full(T_V) || !wait_full(T_DO)) goto done;
         tc_fence_after();
         xyT(BC_DP, tk(T_DO), tk(T_V));  // dP = dO V^T
         mma_commit(&bars.dp_full);
         mma_commit(&bars.empty[sl(T_V)]);
+        if (!mbar_wait(&bars.dv_free, vf ^ 1, ctl, 22)) goto done;
+        vf ^= 1;
         if (!wait_full(T_Q) || !wait_full(T_K)) goto done;
         tc_fence_after();
         xyT(BC_S, tk(T_Q), tk(T_K));  // S = Q K^T
@@ -417,6 +428,9 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
             mma_ss(tmem + BC_DP, ds_mn + (k * 2048 >> 4), bd + (k * 2048 >> 4), C::IDESC_T, k > 0);
         }
         mma_commit(&bars.empty[sl(T_Q)]);
+        if (!mbar_wait(&bars.dq_free, qf ^ 1, ctl, 23)) goto done;
+        qf ^= 1;
+        tc_fence_after();
         // dQ = dS K  (A = dS K-major; B = K MN-major)
         {
           const uint64_t bd = tm(T_K);
@@ -509,31 +523,38 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
       {
         const bool row_ok = r < x.nrows;
         const int64_t g = ((int64_t)(x.row0 + r) * p.H + x.h) * D;
+        // Drain order dK, dV, dQ: each region is released as soon as it is read.
 #pragma unroll 1
         for (int which = 0; which < 3; ++which) {
-          const uint32_t col = which == 0 ? BC_DQ : which == 1 ? BC_S : BC_DP;
+          const uint32_t col = which == 0 ? BC_DP : which == 1 ? BC_S : BC_DQ;
           const float mul = which == 1 ? 1.f : p.scale;
-          __nv_bfloat16 *base = static_cast<__nv_bfloat16 *>(which == 0 ? p.dq : which == 1 ? p.dv : p.dk);
+          __nv_bfloat16 *base = static_cast<__nv_bfloat16 *>(which == 0 ? p.dk : which == 1 ? p.dv : p.dq);
           uint4 *dst = reinterpret_cast<uint4 *>(base + g);
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + col + c * 32, v);
+          for (int c = 0; c < D / 32; c += 2) {  // two 32-column chunks in flight
+            uint32_t v[2][32];
+            tmem_ld32(tmem + lane_off + col + c * 32, v[0]);
+            tmem_ld32(tmem + lane_off + col + c * 32 + 32, v[1]);
             tmem_wait_ld();
+            if (c + 2 >= D / 32) {  // last chunk pair read: release the region
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(which == 0 ? &bars.dk_free : which == 1 ? &bars.dv_free : &bars.dq_free);
+            }
             if (row_ok) {
-              uint32_t q[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                q[i] = pack_bf16(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+              for (int h = 0; h < 2; ++h) {
+                uint32_t q[16];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) dst[c * 4 + i] = make_uint4(q[4 * i], q[4 * i + 1], q[4 * i + 2], q[4 * i + 3]);
+                for (int i = 0; i < 16; ++i)
+                  q[i] = pack_bf16(__uint_as_float(v[h][2 * i]) * mul, __uint_as_float(v[h][2 * i + 1]) * mul);
+                st_global_v8(dst + (c + h) * 4, q);
+                st_global_v8(dst + (c + h) * 4 + 2, q + 8);
+              }
             }
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.g_free);
     }
   }
 done:
