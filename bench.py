@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 # the first 256 sequences (dram__bytes_read.sum + dram__bytes_write.sum)
 # scaled by the processed (key tile, query block) pairs. Reset to None
 # whenever the backward kernel changes until it is measured again.
-BWD_GEM_TRAFFIC = None
+BWD_GEM_TRAFFIC = 4.22e9
 
 
 def _spin(stream, cycles=2_000_000):
