@@ -1,0 +1,51 @@
+"""GPU edge cases of the jagged path: zero-length sequences between, before
+and after non-empty ones (forward and backward against the fp64 oracle),
+and a batch whose sequences are all empty (nothing to compute: empty
+outputs, no error)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import jagged_flash_attention_flashattention_gb300 as jfa
+from jagged_flash_attention_flashattention_gb300 import workloads as W
+from oracle import attention as A
+from tests._util import assert_close, assert_lse, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_zero_length_sequences(D):
+    lengths = [0, 5, 0, 0, 130, 64, 0, 257, 0]
+    H = 2
+    inp = W.jagged_inputs(lengths, H, D, 23, device="cuda")
+    off = torch.from_numpy(W.offsets_of(lengths)).cuda()
+    plan = jfa.Plan(off, H, D)
+    o, lse = jfa.jfa_fwd(inp["q"], inp["k"], inp["v"], off, plan=plan)
+    grads = jfa.jfa_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], off, plan=plan)
+    plan.check()
+    s = 1 / math.sqrt(D)
+    q, k, v, do = (f64(inp[n]) for n in ("q", "k", "v", "do"))
+    offs = off.cpu().numpy()
+    ref_o, ref_lse = A.jagged_fwd(q, k, v, offs, s)
+    assert_close(o, ref_o, "O", bf16_out=True)
+    assert_lse(lse, ref_lse)
+    for name, g, r in zip(("dQ", "dK", "dV"), grads, A.jagged_bwd(q, k, v, do, offs, s)):
+        assert_close(g, r, name, bf16_out=True)
+
+
+def test_all_empty_batch():
+    lengths = [0, 0, 0]
+    H, D = 2, 128
+    inp = W.jagged_inputs(lengths, H, D, 24, device="cuda")
+    off = torch.from_numpy(W.offsets_of(lengths, np.int32)).cuda()
+    plan = jfa.Plan(off, H, D)
+    assert plan.n_fwd_tiles == 0 and plan.n_bwd_tiles == 0
+    o, lse = jfa.jfa_fwd(inp["q"], inp["k"], inp["v"], off, plan=plan)
+    dq, dk, dv = jfa.jfa_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], off, plan=plan)
+    plan.check()
+    assert tuple(o.shape) == (0, H, D) and tuple(lse.shape) == (H, 0)
+    assert all(tuple(t.shape) == (0, H, D) for t in (dq, dk, dv))
