@@ -132,6 +132,17 @@ jfa_status jfa_workspace_init(void *workspace, size_t ws_bytes, jfa_stream_t str
  * the workspace can be reused). */
 jfa_status jfa_check_status(void *workspace, jfa_stream_t stream);
 
+/* Diagnostic of the failure path above (no counterpart in the pages): one
+ * thread waits, with the same bounded wait as every kernel, on an mbarrier
+ * phase that nothing completes. After `timeout_ns` (1 us .. 1 s) it gives up,
+ * writes JFA_ERR_TIMEOUT with wait site 99 into the workspace status block
+ * and returns, so jfa_check_status() then reports JFA_ERR_TIMEOUT and clears
+ * the block. Nothing faults and the context stays usable. Asynchronous on
+ * `stream`; returns JFA_ERR_WORKSPACE for a missing or too-small workspace
+ * (fewer than 256 bytes) and JFA_ERR_INVALID_ARG for a limit out of range. */
+jfa_status jfa_selftest_wait_timeout(void *workspace, size_t ws_bytes, uint64_t timeout_ns,
+                                     jfa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Jagged forward: for each sequence b and head h,
  *   O = softmax(scale * Q K^T) V,  LSE_i = ln sum_j exp(scale * q_i . k_j)

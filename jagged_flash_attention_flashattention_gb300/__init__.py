@@ -31,6 +31,8 @@ LIB_PATH = os.path.join(_PKG, "libjfa.so")
 JFA_I32, JFA_I64 = 0, 1
 OP_FWD, OP_BWD, OP_BCASTQ_FWD, OP_BCASTQ_BWD, OP_BLOCKDIAG_FWD, OP_BLOCKDIAG_BWD = range(6)
 
+(JFA_OK, JFA_ERR_INVALID_ARG, JFA_ERR_UNSUPPORTED, JFA_ERR_WORKSPACE, JFA_ERR_CUDA,
+ JFA_ERR_TIMEOUT) = range(6)
 _STATUS = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED",
            3: "JFA_ERR_WORKSPACE", 4: "JFA_ERR_CUDA", 5: "JFA_ERR_TIMEOUT"}
 
@@ -38,7 +40,7 @@ EXPORTS = [
     "jfa_status_str", "jfa_last_error", "jfa_sched_size", "jfa_sched_build", "jfa_tile_rows",
     "jfa_num_sms", "jfa_workspace_size", "jfa_workspace_init", "jfa_check_status", "jfa_fwd",
     "jfa_bwd", "jfa_bcastq_fwd", "jfa_bcastq_bwd", "blockdiag_fwd", "blockdiag_bwd",
-    "jfa_bwd_noalloc",
+    "jfa_bwd_noalloc", "jfa_selftest_wait_timeout",
 ]
 
 
@@ -79,6 +81,7 @@ def lib():
         "blockdiag_fwd": ([P, P, P, I64, I64, I, I, F, P, P, SZ, P], I),
         "blockdiag_bwd": ([P, P, P, P, I64, I64, I, I, F, P, P, P, P, SZ, P], I),
         "jfa_bwd_noalloc": ([P, P, P, P, P, P, P, I, I64, I64, I, I, F, P, P, I, P, P, P, P], I),
+        "jfa_selftest_wait_timeout": ([P, SZ, ctypes.c_uint64, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)

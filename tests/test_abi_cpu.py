@@ -132,3 +132,12 @@ def test_c_scheduler_int32_offsets_and_empty(L):
     assert sp.tolist() == rp and [tuple(t) for t in tl.tolist()] == rt
     sp, tl = jfa.schedule(np.array([0], dtype=np.int64), 2, 64, 5)
     assert sp.tolist() == [0] * 6 and tl.shape[0] == 0
+
+
+def test_selftest_rejects_bad_arguments(L):
+    # argument checks happen before any launch (no GPU needed)
+    assert L.jfa_selftest_wait_timeout(None, 256, 1_000_000, None) == jfa.JFA_ERR_WORKSPACE
+    fake = ctypes.c_void_p(0x1000)
+    assert L.jfa_selftest_wait_timeout(fake, 64, 1_000_000, None) == jfa.JFA_ERR_WORKSPACE
+    assert L.jfa_selftest_wait_timeout(fake, 256, 10, None) == jfa.JFA_ERR_INVALID_ARG
+    assert L.jfa_selftest_wait_timeout(fake, 256, 5_000_000_000, None) == jfa.JFA_ERR_INVALID_ARG

@@ -49,3 +49,23 @@ def test_all_empty_batch():
     plan.check()
     assert tuple(o.shape) == (0, H, D) and tuple(lse.shape) == (H, 0)
     assert all(tuple(t.shape) == (0, H, D) for t in (dq, dk, dv))
+
+
+def test_bounded_wait_timeout_reported_and_context_usable():
+    # A wait that nothing completes gives up after 2 ms and reports through the
+    # status block; no fault, and the next computation on the GPU is correct.
+    L = jfa.lib()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    assert L.jfa_selftest_wait_timeout(jfa._ptr(ws), 256, 2_000_000, jfa._stream()) == 0
+    assert L.jfa_check_status(jfa._ptr(ws), jfa._stream()) == jfa.JFA_ERR_TIMEOUT
+    assert b"site 99" in L.jfa_last_error()
+    assert L.jfa_check_status(jfa._ptr(ws), jfa._stream()) == 0  # cleared by the first check
+    lengths, H, D = [70, 200], 2, 128
+    inp = W.jagged_inputs(lengths, H, D, 25, device="cuda")
+    off = torch.from_numpy(W.offsets_of(lengths)).cuda()
+    o, lse = jfa.jfa_fwd(inp["q"], inp["k"], inp["v"], off)
+    jfa.check_status()
+    ref_o, ref_lse = A.jagged_fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), off.cpu().numpy(),
+                                  1 / math.sqrt(D))
+    assert_close(o, ref_o, "O", bf16_out=True)
+    assert_lse(lse, ref_lse)
