@@ -475,8 +475,9 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     // ---------------------------------- LSE / Di staging and dQ reduction
     // Per query block, ahead of the compute warps: LSE and Di = rowsum(dO * O)
     // of the block's 64 rows (two threads per row, O read from global memory
-    // one block ahead into registers, dO from the stage). Then, one block
-    // behind the MMA: drain dQ^T from TMEM and TMA reduce-add it.
+    // one block ahead into registers, dO from the stage). Then the dQ^T of
+    // the block two before this one: drain it from its TMEM buffer, release
+    // the buffer, and TMA reduce-add it.
     constexpr int ND = D / 2;  // head-dim elements per thread for Di
     constexpr int NV = ND / 8;
     const int wq = warp & 3;
