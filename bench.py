@@ -115,6 +115,21 @@ def _dist():
     return ws, rank, local
 
 
+def aggregate_over_ranks(local_flops, local_ms, ws, dev):
+    """Whole-job figures of a weak-scaling run: the useful FLOPs of every rank's
+    own batch summed, and the slowest rank's time. One process per GPU; with
+    ws == 1 the local values are returned unchanged."""
+    if ws == 1:
+        return float(local_flops), float(local_ms)
+    import torch
+    import torch.distributed as dist
+    f = torch.tensor([float(local_flops)], dtype=torch.float64, device=dev)
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=dev)
+    dist.all_reduce(f, op=dist.ReduceOp.SUM)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(f.item()), float(t.item())
+
+
 def _gem_lengths(seed_offset=0):
     from jagged_flash_attention_flashattention_gb300 import workloads as W
     if seed_offset == 0:
@@ -357,13 +372,9 @@ def run_ours(args):
     total_ms = t_start.elapsed_time(t_end)
     fwd_ms = statistics.median(e["e0"].elapsed_time(e["e1"]) for e in evs)
     bwd_ms = statistics.median(e["e1"].elapsed_time(e["e2"]) for e in evs)
-    t_max = total_ms
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    job_flops, t_max = aggregate_over_ranks(fwd_flops + bwd_flops, total_ms, ws, dev)
     ms_per_step = t_max / args.steps
-    value = ws * (fwd_flops + bwd_flops) / (ms_per_step * 1e-3) / 1e12
+    value = job_flops / (ms_per_step * 1e-3) / 1e12
 
     e2e = None
     if args.config == "gem" and not args.seqs:
@@ -484,12 +495,9 @@ def _e2e_gem(args, st, dev, ws):
         comp.wait_event(e)
     a1.record(comp)
     torch.cuda.synchronize()
-    ms = a0.elapsed_time(a1) / n_steps
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    val = ws * (st["fwd_flops"] + st["bwd_flops"]) / (ms * 1e-3) / 1e12
+    job_flops, ms = aggregate_over_ranks(st["fwd_flops"] + st["bwd_flops"],
+                                         a0.elapsed_time(a1) / n_steps, ws, dev)
+    val = job_flops / (ms * 1e-3) / 1e12
     return {"value": round(val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 3),
             "overlap": "h2d of step n+1 and d2h of step n-1 run beside step n's kernels"}
