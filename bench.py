@@ -409,7 +409,7 @@ def run_ours(args):
             "pct_of_peak": round(100 * value / peak, 2),
             "roofline": roof,
             "clocks": clk,
-            "gpu_launches": (3 if st["kind"] == "jagged" else 2) * args.steps,
+            "gpu_launches": (4 if st["kind"] == "jagged" else 2) * args.steps,
         }
         if st["kind"] == "blockdiag":
             line["fwd"]["gbps"] = round(st["fwd_bytes"] / (fwd_ms * 1e-3) / 1e9, 1)
@@ -483,7 +483,7 @@ def _e2e_gem(args, st, dev, ws):
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    n_steps = max(2, min(args.steps, 10))
+    n_steps = max(2, min(args.steps, 20))
     a0 = torch.cuda.Event(enable_timing=True)
     a1 = torch.cuda.Event(enable_timing=True)
     a0.record(comp)

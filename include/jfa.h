@@ -118,9 +118,15 @@ jfa_status jfa_num_sms(int *num_sms);
  * Workspace.
  *
  * Every kernel call takes a device workspace that starts with a 256-byte
- * status block. jfa_bwd also keeps an fp32 dQ accumulator there ([T, H, D]),
- * which the call clears itself. `n` is T for JFA_OP_FWD / JFA_OP_BWD and is
- * ignored for the other ops.
+ * status block. jfa_bwd also keeps an fp32 dQ accumulator there ([T, H, D])
+ * that must start at zero. When jfa_fwd is given a workspace of at least
+ * jfa_workspace_size(JFA_OP_BWD, T, H, D) bytes, its kernel clears that
+ * accumulator on otherwise idle warps and records the cleared size in the
+ * status block; jfa_bwd then skips its own clearing pass, and clears the
+ * accumulator itself in every other case (no forward, a forward of a smaller
+ * batch, a second backward). Calls that share a workspace must be ordered on
+ * one stream. `n` is T for JFA_OP_FWD / JFA_OP_BWD and is ignored for the
+ * other ops.
  * ---------------------------------------------------------------------- */
 size_t jfa_workspace_size(jfa_op op, int64_t n, int H, int D);
 
@@ -154,6 +160,9 @@ jfa_status jfa_selftest_wait_timeout(void *workspace, size_t ws_bytes, uint64_t 
  * d_tiles: device copies of jfa_sched_build() output for
  * tile_rows = jfa_tile_rows(JFA_OP_FWD). num_sms: length of d_sm_ptr - 1
  * (the grid size). o: device bf16 [T, H, D]. lse: device fp32 [H, T].
+ * workspace: >= jfa_workspace_size(JFA_OP_FWD, ...); a workspace sized for
+ * JFA_OP_BWD also gets its dQ accumulator cleared for the backward (see
+ * Workspace above).
  * ---------------------------------------------------------------------- */
 jfa_status jfa_fwd(const void *q, const void *k, const void *v, const void *offsets,
                    jfa_index_t idx, int64_t B, int64_t T, int H, int D, float scale,

@@ -210,6 +210,13 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *o
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = static_cast<uint32_t *>(ws);
   p.timeout_ns = kTimeoutNs;
+  // A workspace sized for the jagged backward: clear its dQ accumulator here,
+  // on the forward kernel's idle warps, instead of in a pass of its own.
+  const size_t acc_bytes = (size_t)q_rows * H * D * sizeof(float);
+  if (Lq == 0 && ws_bytes >= kStatusBytes + round_up(acc_bytes, 256)) {
+    p.acc_zero = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kStatusBytes);
+    p.acc_n16 = (int64_t)(acc_bytes / 16);
+  }
   return cuda_status(launch_fwd(p, D, num_sms, st), "fwd launch");
 }
 
@@ -301,11 +308,15 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = static_cast<uint32_t *>(ws);
   p.timeout_ns = kTimeoutNs;
-  JFA_TRY(cuda_status(cudaMemsetAsync(acc, 0, (size_t)acc_rows * H * D * sizeof(float), st),
-                      "cudaMemsetAsync"));
+  const size_t acc_bytes = (size_t)acc_rows * H * D * sizeof(float);
+  if (Lq > 0)
+    JFA_TRY(cuda_status(cudaMemsetAsync(acc, 0, acc_bytes, st), "cudaMemsetAsync"));
+  else  // skipped on the device when a forward pass has already cleared it
+    JFA_TRY(launch_status(launch_acc_clear(acc, (int64_t)(acc_bytes / 16), p.status, st),
+                          "accumulator clear"));
   if (Tk > 0) JFA_TRY(launch_status(launch_bwd(p, D, num_sms, st), "bwd launch"));
   if (Lq > 0) return JFA_OK;
-  return launch_status(launch_dq_convert(acc, dq, acc_rows, H, D, st), "dq convert");
+  return launch_status(launch_dq_convert(acc, dq, acc_rows, H, D, p.status, st), "dq convert");
 }
 
 }  // namespace

@@ -33,7 +33,10 @@
 // reduce-add (fewer, larger reductions measured faster than 32-row ones)
 // into an fp32 accumulator in global memory: a workspace accumulator that a
 // light kernel casts to bf16 at the end (jagged), or the caller's fp32 dQ
-// itself (broadcast-Q, where dQ is a sum over the whole batch).
+// itself (broadcast-Q, where dQ is a sum over the whole batch). The jagged
+// accumulator starts at zero: a forward pass with the same workspace clears
+// it and records the cleared byte count in the status block; otherwise a
+// clearing kernel does it first, and the cast resets the count.
 // dK and dV leave TMEM once per tile, written with 32-byte stores.
 //
 // Roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
@@ -620,8 +623,23 @@ cudaError_t launch_t(const BwdParams &p, int num_sms, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Clearing of the fp32 accumulator, skipped when a forward pass with this
+// workspace has already zeroed at least n16 units.
+__global__ void acc_clear_kernel(float *acc, int64_t n16, const uint32_t *status) {
+  const uint64_t zeroed =
+      *reinterpret_cast<const volatile uint64_t *>(reinterpret_cast<const uint8_t *>(status) + kAccZeroedOff);
+  if (zeroed >= (uint64_t)n16 * 16) return;
+  uint4 *base = reinterpret_cast<uint4 *>(acc);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
+       i += (int64_t)gridDim.x * blockDim.x)
+    base[i] = make_uint4(0, 0, 0, 0);
+}
+
 // fp32 [rows, H, D] -> bf16 [rows, H, D]; 8 elements per thread.
-__global__ void dq_convert_kernel(const float4 *__restrict__ acc, uint4 *__restrict__ dq, int64_t n8) {
+__global__ void dq_convert_kernel(const float4 *__restrict__ acc, uint4 *__restrict__ dq, int64_t n8,
+                                  uint32_t *status) {
+  if (blockIdx.x == 0 && threadIdx.x == 0)  // the accumulator is dirty until cleared again
+    *reinterpret_cast<volatile uint64_t *>(reinterpret_cast<uint8_t *>(status) + kAccZeroedOff) = 0;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float4 a = acc[2 * i], b = acc[2 * i + 1];
@@ -638,17 +656,25 @@ cudaError_t launch_bwd(const BwdParams &p, int D, int num_sms, cudaStream_t st) 
   return bcast ? launch_t<64, true>(p, num_sms, st) : launch_t<64, false>(p, num_sms, st);
 }
 
-cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, int D,
-                              cudaStream_t st) {
-  const int64_t n8 = rows * H * D / 8;
-  if (n8 == 0) return cudaSuccess;
+static int grid_for(int64_t n) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (n8 + 255) / 256;
-  const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
-  dq_convert_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4 *>(acc),
-                                          static_cast<uint4 *>(dq), n8);
+  const int64_t want = (n + 255) / 256;
+  return (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
+}
+
+cudaError_t launch_acc_clear(float *acc, int64_t n16, const uint32_t *status, cudaStream_t st) {
+  if (n16 == 0) return cudaSuccess;
+  acc_clear_kernel<<<grid_for(n16), 256, 0, st>>>(acc, n16, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, int D,
+                              uint32_t *status, cudaStream_t st) {
+  const int64_t n8 = rows * H * D / 8;
+  dq_convert_kernel<<<grid_for(n8), 256, 0, st>>>(reinterpret_cast<const float4 *>(acc),
+                                                  static_cast<uint4 *>(dq), n8, status);
   return cudaGetLastError();
 }
 

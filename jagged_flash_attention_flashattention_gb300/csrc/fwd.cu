@@ -18,6 +18,10 @@
 //                slots (K_j with V_{j-1}: one barrier per K/V step)
 //   warp 1       MMA issuer: S = Q K^T into TMEM, O += P V from TMEM P
 //   warp 2       owns the tensor-memory allocation
+//   warps 2-3    (jagged, workspace sized for the backward) clear the
+//                backward's fp32 dQ accumulator with coalesced 16-byte
+//                stores, which overlaps that HBM-bound pass with this
+//                tensor-bound kernel
 //   warps 4-7    softmax + correction + epilogue for query rows   0..127
 //   warps 8-11   softmax + correction + epilogue for query rows 128..255
 //
@@ -193,6 +197,20 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           }
         }
       }
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ----------------------------------- backward accumulator pre-clearing
+    // No waits here: the zeroing always runs to completion, so the count that
+    // block 0 records is true once the kernel has finished.
+    if (p.acc_zero != nullptr) {
+      const int64_t per = (p.acc_n16 + gridDim.x - 1) / gridDim.x;
+      const int64_t beg = (int64_t)blockIdx.x * per;
+      const int64_t end = min(p.acc_n16, beg + per);
+      uint4 *base = reinterpret_cast<uint4 *>(p.acc_zero);
+      for (int64_t i = beg + (warp - 2) * 32 + lane; i < end; i += 64) base[i] = make_uint4(0, 0, 0, 0);
+      if (blockIdx.x == 0 && warp == 2 && lane == 0)
+        *reinterpret_cast<volatile uint64_t *>(reinterpret_cast<uint8_t *>(p.status) + kAccZeroedOff) =
+            (uint64_t)p.acc_n16 * 16;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer

@@ -26,7 +26,17 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e)
   uint32_t *status;
   uint64_t timeout_ns;
+  // Jagged only, when the workspace also holds the backward's fp32 dQ
+  // accumulator: the two otherwise idle warps zero it (acc_n16 units of 16
+  // bytes, split evenly over the CTAs) and block 0 records acc_n16 * 16 in the
+  // status block, so the backward that follows skips its own clearing pass.
+  float *acc_zero;
+  int64_t acc_n16;
 };
+
+// Byte offset, in the status block, of the uint64 count of accumulator bytes
+// known to be zero (written by the forward kernel, reset by the dQ cast).
+constexpr size_t kAccZeroedOff = 128;
 
 cudaError_t launch_fwd(const FwdParams &p, int D, int num_sms, cudaStream_t st);
 
@@ -57,9 +67,14 @@ struct BwdParams {
 
 cudaError_t launch_bwd(const BwdParams &p, int D, int num_sms, cudaStream_t st);
 
-// fp32 [rows, H, D] accumulator -> bf16 [rows, H, D]
+// Zeroes the fp32 dQ accumulator (n16 units of 16 bytes) unless the status
+// block already records at least that many zero bytes.
+cudaError_t launch_acc_clear(float *acc, int64_t n16, const uint32_t *status, cudaStream_t st);
+
+// fp32 [rows, H, D] accumulator -> bf16 [rows, H, D]; also resets the status
+// block's zero-accumulator count (the accumulator is dirty from here on).
 cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, int D,
-                              cudaStream_t st);
+                              uint32_t *status, cudaStream_t st);
 
 // Block-diagonal kernels: [B, L, H, D], 64-token blocks, 128-row work units.
 struct BlockdiagParams {

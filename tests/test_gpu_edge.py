@@ -69,3 +69,41 @@ def test_bounded_wait_timeout_reported_and_context_usable():
                                   1 / math.sqrt(D))
     assert_close(o, ref_o, "O", bf16_out=True)
     assert_lse(lse, ref_lse)
+
+
+def test_dq_accumulator_clearing_in_every_call_order():
+    # The jagged forward clears the backward's dQ accumulator when the
+    # workspace holds one, and records how many bytes it cleared; the backward
+    # clears it itself otherwise, and every backward marks it dirty again.
+    # Each order below must give the oracle's gradients.
+    H, D = 2, 128
+    small, large = [70, 200, 5], [300, 129, 64, 250]
+    runs = {}
+    for name, lengths, seed in (("small", small, 26), ("large", large, 27)):
+        inp = W.jagged_inputs(lengths, H, D, seed, device="cuda")
+        off = torch.from_numpy(W.offsets_of(lengths)).cuda()
+        ref = A.jagged_bwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["do"]),
+                           off.cpu().numpy(), 1 / math.sqrt(D))
+        runs[name] = (inp, off, ref)
+    big_plan = jfa.Plan(runs["large"][1], H, D)
+    ws = big_plan.workspace
+    plans = {"large": big_plan, "small": jfa.Plan(runs["small"][1], H, D, workspace=ws)}
+
+    def fwd(name):
+        inp, off, _ = runs[name]
+        return jfa.jfa_fwd(inp["q"], inp["k"], inp["v"], off, plan=plans[name])
+
+    def bwd_check(name, o, lse, tag):
+        inp, off, ref = runs[name]
+        got = jfa.jfa_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], off, plan=plans[name])
+        plans[name].check()
+        for g, r, n in zip(got, ref, ("dQ", "dK", "dV")):
+            assert_close(g, r, "%s %s" % (tag, n), bf16_out=True)
+
+    o_s, l_s = fwd("small")
+    bwd_check("small", o_s, l_s, "fwd then bwd")
+    bwd_check("small", o_s, l_s, "second bwd without a forward")
+    o_l, l_l = fwd("large")
+    o_s, l_s = fwd("small")  # the last forward cleared fewer bytes than "large" needs
+    bwd_check("large", o_l, l_l, "larger bwd after a smaller forward")
+    bwd_check("small", o_s, l_s, "bwd after another batch's bwd")
