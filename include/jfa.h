@@ -214,7 +214,9 @@ jfa_status jfa_bwd_noalloc(const void *q, const void *k, const void *v, const vo
  * sequence of k, v (device bf16 [Tk, H, D], boundaries kv_offsets [B+1]).
  * o: device bf16 [B, Lq, H, D]; lse: device fp32 [B, H, Lq]. A sequence of
  * length 0 gets O = 0 and LSE = -inf. Tiles: jfa_sched_build() with
- * tile_rows = jfa_tile_rows(JFA_OP_BCASTQ_FWD), fixed_rows = Lq. */
+ * tile_rows = jfa_tile_rows(JFA_OP_BCASTQ_FWD), fixed_rows = Lq.
+ * B * Lq must stay below 2^31 - 256 (rows of O are 32-bit indices in the
+ * kernels); larger batches return JFA_ERR_INVALID_ARG and launch nothing. */
 jfa_status jfa_bcastq_fwd(const void *q, const void *k, const void *v, const void *kv_offsets,
                           jfa_index_t idx, int64_t B, int64_t Lq, int64_t Tk, int H, int D,
                           float scale, const int32_t *d_sm_ptr, const int32_t *d_tiles,
@@ -228,7 +230,8 @@ jfa_status jfa_bcastq_fwd(const void *q, const void *k, const void *v, const voi
  * del proceso de Backward y dQ") straight into dq, which is therefore fp32:
  * a sum over the whole batch grows with B and a bf16 result would lose more
  * than the accumulation itself. The call clears dq first. Tiles: tile_rows =
- * jfa_tile_rows(JFA_OP_BCASTQ_BWD) over key blocks, fixed_work = Lq. */
+ * jfa_tile_rows(JFA_OP_BCASTQ_BWD) over key blocks, fixed_work = Lq. Same
+ * B * Lq limit as jfa_bcastq_fwd. */
 jfa_status jfa_bcastq_bwd(const void *q, const void *k, const void *v, const void *o,
                           const float *lse, const void *dout, const void *kv_offsets,
                           jfa_index_t idx, int64_t B, int64_t Lq, int64_t Tk, int H, int D,

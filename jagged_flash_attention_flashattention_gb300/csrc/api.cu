@@ -238,6 +238,8 @@ extern "C" jfa_status jfa_bcastq_fwd(const void *q, const void *k, const void *v
                                      int num_sms, void *o, float *lse, void *workspace,
                                      size_t ws_bytes, jfa_stream_t stream) {
   if (Lq < 0 || Lq >= (1 << 30)) return fail(JFA_ERR_INVALID_ARG, "bad Lq");
+  if (B > 0 && Lq >= ((int64_t(1) << 31) - 256) / B)  // O rows are addressed with 32-bit indices
+    return fail(JFA_ERR_INVALID_ARG, "B * Lq too large");
   if (Lq == 0) return JFA_OK;
   return fwd_common(q, k, v, kv_offsets, idx, B, Lq, Tk, Lq, H, D, scale, d_sm_ptr, d_tiles,
                     num_sms, o, lse, workspace, ws_bytes, (cudaStream_t)stream);
@@ -339,6 +341,8 @@ extern "C" jfa_status jfa_bcastq_bwd(const void *q, const void *k, const void *v
                                      void *dv, void *workspace, size_t ws_bytes,
                                      jfa_stream_t stream) {
   if (Lq < 0 || Lq >= (1 << 30)) return fail(JFA_ERR_INVALID_ARG, "bad Lq");
+  if (B > 0 && Lq >= ((int64_t(1) << 31) - 256) / B)  // O / dO rows use 32-bit indices
+    return fail(JFA_ERR_INVALID_ARG, "B * Lq too large");
   if (Lq == 0) return JFA_OK;
   return bwd_common(q, k, v, o, lse, dout, kv_offsets, idx, B, Lq, Tk, Lq, H, D, scale,
                     d_sm_ptr, d_tiles, num_sms, dq, dk, dv, workspace, ws_bytes,

@@ -141,3 +141,17 @@ def test_selftest_rejects_bad_arguments(L):
     assert L.jfa_selftest_wait_timeout(fake, 64, 1_000_000, None) == jfa.JFA_ERR_WORKSPACE
     assert L.jfa_selftest_wait_timeout(fake, 256, 10, None) == jfa.JFA_ERR_INVALID_ARG
     assert L.jfa_selftest_wait_timeout(fake, 256, 5_000_000_000, None) == jfa.JFA_ERR_INVALID_ARG
+
+
+def test_bcastq_rejects_batches_past_32_bit_row_indices(L):
+    # B * Lq rows of O / dO are addressed with 32-bit row indices in the kernels:
+    # refused on the host, nothing launched.
+    dummy = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(dummy, ctypes.c_void_p)
+    B, Lq = 1 << 20, 1 << 12
+    assert L.jfa_bcastq_fwd(p, p, p, p, 0, B, Lq, 10, 2, 64, 0.1, p, p, 1, p, p, p, 256,
+                            _null()) == 1
+    assert b"B * Lq too large" in L.jfa_last_error()
+    assert L.jfa_bcastq_bwd(p, p, p, p, p, p, p, 0, B, Lq, 10, 2, 64, 0.1, p, p, 1, p, p, p, p,
+                            256, _null()) == 1
+    assert b"B * Lq too large" in L.jfa_last_error()
