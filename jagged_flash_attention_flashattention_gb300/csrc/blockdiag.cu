@@ -30,7 +30,8 @@
 // the next unit's loads start while this unit computes. The epilogue drains
 // dK, dV and dQ in that order and releases each TMEM region as soon as it is
 // read, so the next unit's dP and S products overlap the rest of the stores
-// (32 bytes per lane).
+// (each 128-byte piece of a row stored by four lanes after a shuffle
+// transpose, eight whole lines per store instruction).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -521,17 +522,17 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
       gph ^= 1;
       tc_fence_after();
       {
-        const bool row_ok = r < x.nrows;
-        const int64_t g = ((int64_t)(x.row0 + r) * p.H + x.h) * D;
+        // Each 64-column (128-byte) piece of a row is stored four lanes to a row
+        // (eight whole lines per store instruction, not 32-byte pieces of 32).
+        const int grp = wq * 32 + (lane & ~3);  // first of this lane group's rows
         // Drain order dK, dV, dQ: each region is released as soon as it is read.
 #pragma unroll 1
         for (int which = 0; which < 3; ++which) {
           const uint32_t col = which == 0 ? BC_DP : which == 1 ? BC_S : BC_DQ;
           const float mul = which == 1 ? 1.f : p.scale;
           __nv_bfloat16 *base = static_cast<__nv_bfloat16 *>(which == 0 ? p.dk : which == 1 ? p.dv : p.dq);
-          uint4 *dst = reinterpret_cast<uint4 *>(base + g);
 #pragma unroll 1
-          for (int c = 0; c < D / 32; c += 2) {  // two 32-column chunks in flight
+          for (int c = 0; c < D / 32; c += 2) {  // 64 columns: two 32-column chunks in flight
             uint32_t v[2][32];
             tmem_ld32(tmem + lane_off + col + c * 32, v[0]);
             tmem_ld32(tmem + lane_off + col + c * 32 + 32, v[1]);
@@ -541,17 +542,16 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
               __syncwarp();
               if (lane == 0) mbar_arrive(which == 0 ? &bars.dk_free : which == 1 ? &bars.dv_free : &bars.dq_free);
             }
-            if (row_ok) {
+            uint32_t w[32];  // this lane's row
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                uint32_t q[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  q[i] = pack_bf16(__uint_as_float(v[h][2 * i]) * mul, __uint_as_float(v[h][2 * i + 1]) * mul);
-                st_global_v8(dst + (c + h) * 4, q);
-                st_global_v8(dst + (c + h) * 4 + 2, q + 8);
-              }
+            for (int i = 0; i < 16; ++i) {
+              w[i] = pack_bf16(__uint_as_float(v[0][2 * i]) * mul, __uint_as_float(v[0][2 * i + 1]) * mul);
+              w[16 + i] = pack_bf16(__uint_as_float(v[1][2 * i]) * mul, __uint_as_float(v[1][2 * i + 1]) * mul);
             }
+            store_rows_by_quads(
+                w, lane,
+                [&](int k) { return (void *)(base + ((int64_t)(x.row0 + grp + k) * p.H + x.h) * D + c * 32); },
+                [&](int k) { return grp + k < x.nrows; });
           }
         }
       }

@@ -37,7 +37,9 @@
 // accumulator starts at zero: a forward pass with the same workspace clears
 // it and records the cleared byte count in the status block; otherwise a
 // clearing kernel does it first, and the cast resets the count.
-// dK and dV leave TMEM once per tile, written with 32-byte stores.
+// dK and dV leave TMEM once per tile; at D = 128 each 128-byte half row is
+// stored by four lanes (a shuffle transpose within lane quads), so a store
+// instruction writes eight whole lines.
 //
 // Roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
 // warps 4-7 and 12-15 compute + dK/dV epilogue (two warps per TMEM lane
@@ -456,7 +458,22 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
           for (int cc = 0; cc < D / 64; ++cc)
             tmem_ld32(tmem + lane_off + (which ? COL_DK : COL_DV) + (ch * (D / 64) + cc) * 32, v[cc]);
           tmem_wait_ld();
-          if (kv_ok) {
+          if constexpr (D == 128) {  // 64 columns = one 128-byte line per row: four lanes to a row
+            uint32_t w[32];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              w[e] = pack_bf16(__uint_as_float(v[0][2 * e]) * mul, __uint_as_float(v[0][2 * e + 1]) * mul);
+              w[16 + e] = pack_bf16(__uint_as_float(v[1][2 * e]) * mul, __uint_as_float(v[1][2 * e + 1]) * mul);
+            }
+            const int grp = wq * 32 + (lane & ~3);
+            __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(which ? p.dk : p.dv);
+            store_rows_by_quads(
+                w, lane,
+                [&](int k) {
+                  return (void *)(outp + ((int64_t)(tl.kv_row0 + grp + k) * p.H + tl.h) * D + ch * 64);
+                },
+                [&](int k) { return grp + k < tl.nkv; });
+          } else if (kv_ok) {
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
               uint32_t pk[16];

@@ -146,11 +146,43 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
   }
 }
 
+// One of four words by a 2-bit index, without indexing a register array.
+__device__ __forceinline__ uint32_t sel4(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, int i) {
+  const uint32_t lo = (i & 1) ? x1 : x0, hi = (i & 1) ? x3 : x2;
+  return (i & 2) ? hi : lo;
+}
+
 // 32-byte global store (eight 32-bit words; the address must be 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *w) {
   asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
                "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                : "memory");
+}
+
+// Stores 128 bytes of each lane's row (w: 32 words, lane = row) four lanes
+// to a row: every group of four lanes swaps 32-byte segments of its four
+// rows (a 4 x 4 transpose by shuffles), so one store instruction writes eight
+// whole 128-byte lines. rowp(k) is the address of group row k's 128 bytes
+// (only called when row_ok(k)); every lane of the warp must take part.
+template <typename RowPtr, typename RowOk>
+__device__ __forceinline__ void store_rows_by_quads(const uint32_t (&w)[32], int lane, RowPtr rowp,
+                                                    RowOk row_ok) {
+  const int a = lane & 3;
+  uint32_t rcv[4][8];
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t x = sel4(w[e], w[8 + e], w[16 + e], w[24 + e], a ^ t);
+      rcv[t][e] = t ? __shfl_xor_sync(0xffffffffu, x, t) : x;
+    }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t d[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) d[e] = sel4(rcv[0][e], rcv[1][e], rcv[2][e], rcv[3][e], a ^ k);
+    if (row_ok(k)) st_global_v8(static_cast<uint8_t *>(rowp(k)) + a * 32, d);
+  }
 }
 
 // ---------------------------------------------------------------- TMA
