@@ -470,20 +470,34 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
         tmem_ld32(tmem + lane_off + BC_S + blk * 64, a);
         tmem_ld32(tmem + lane_off + BC_S + blk * 64 + 32, b);
         tmem_wait_ld();
-        float mx = -INFINITY;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(__uint_as_float(a[i]), __uint_as_float(b[i])));
-        const float mo = mx * sl2;
-        float sum = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          pr[i] = ex2(fmaf(__uint_as_float(a[i]), sl2, -mo));
-          pr[32 + i] = ex2(fmaf(__uint_as_float(b[i]), sl2, -mo));
-          sum += pr[i] + pr[32 + i];
+        for (int i = 0; i < 32; i += 2) {
+          mx0 = max3f(mx0, __uint_as_float(a[i]), __uint_as_float(a[i + 1]));
+          mx1 = max3f(mx1, __uint_as_float(b[i]), __uint_as_float(b[i + 1]));
         }
-        const float inv = 1.f / sum;
+        const float mo = fmaxf(mx0, mx1) * sl2;
+        const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-mo, -mo);
+        float2 sum2 = make_float2(0.f, 0.f), sum3 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) pr[i] *= inv;
+        for (int i = 0; i < 32; i += 2) {
+          const float2 xa = fma2(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])), sl2v, negm);
+          const float2 xb = fma2(make_float2(__uint_as_float(b[i]), __uint_as_float(b[i + 1])), sl2v, negm);
+          pr[i] = ex2(xa.x);
+          pr[i + 1] = ex2(xa.y);
+          pr[32 + i] = ex2(xb.x);
+          pr[32 + i + 1] = ex2(xb.y);
+          sum2 = add2(sum2, make_float2(pr[i], pr[i + 1]));
+          sum3 = add2(sum3, make_float2(pr[32 + i], pr[32 + i + 1]));
+        }
+        const float inv = 1.f / ((sum2.x + sum2.y) + (sum3.x + sum3.y));
+        const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float2 q = mul2(make_float2(pr[i], pr[i + 1]), inv2);
+          pr[i] = q.x;
+          pr[i + 1] = q.y;
+        }
       }
       {
         uint32_t a[32], b[32];
@@ -496,15 +510,21 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
           dp[i] = __uint_as_float(a[i]);
           dp[32 + i] = __uint_as_float(b[i]);
         }
+        float2 di2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) di = fmaf(pr[i], dp[i], di);  // Di = rowsum(P * dP)
+        for (int i = 0; i < 64; i += 2)  // Di = rowsum(P * dP)
+          di2 = fma2(make_float2(pr[i], pr[i + 1]), make_float2(dp[i], dp[i + 1]), di2);
+        di = di2.x + di2.y;
         if (!mbar_wait(&bars.ps_free, psf ^ 1, ctl, 32)) goto done;
         psf ^= 1;
         uint32_t pk[32], dk[32];
+        const float2 negdi = make_float2(-di, -di);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           pk[i] = pack_bf16(pr[2 * i], pr[2 * i + 1]);
-          dk[i] = pack_bf16(pr[2 * i] * (dp[2 * i] - di), pr[2 * i + 1] * (dp[2 * i + 1] - di));
+          const float2 ds = mul2(make_float2(pr[2 * i], pr[2 * i + 1]),
+                                 add2(make_float2(dp[2 * i], dp[2 * i + 1]), negdi));
+          dk[i] = pack_bf16(ds.x, ds.y);
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -545,8 +565,8 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
             uint32_t w[32];  // this lane's row
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              w[i] = pack_bf16(__uint_as_float(v[0][2 * i]) * mul, __uint_as_float(v[0][2 * i + 1]) * mul);
-              w[16 + i] = pack_bf16(__uint_as_float(v[1][2 * i]) * mul, __uint_as_float(v[1][2 * i + 1]) * mul);
+              w[i] = pack_bf16_mul(v[0][2 * i], v[0][2 * i + 1], make_float2(mul, mul));
+              w[16 + i] = pack_bf16_mul(v[1][2 * i], v[1][2 * i + 1], make_float2(mul, mul));
             }
             store_rows_by_quads(
                 w, lane,

@@ -70,8 +70,8 @@ struct BwdCfg {
   static constexpr int OFF_STAGE = OFF_ZERO + ZERO_BYTES;  // NSTAGE x (Q, dO)
   static constexpr int OFF_DS = OFF_STAGE + NSTAGE * 2 * QT;  // 128x64 bf16 dS^T
   static constexpr int OFF_DQS = OFF_DS + 16384;               // dQ staging: 4 warps x 8 KB
-  static constexpr int OFF_LSE = OFF_DQS + 32768;              // [NSTAGE][64] log2 units
-  static constexpr int OFF_DI = OFF_LSE + NSTAGE * 256;        // [NSTAGE][64]
+  static constexpr int OFF_LSE = OFF_DQS + 32768;              // [NSTAGE][64] -LSE, log2 units
+  static constexpr int OFF_DI = OFF_LSE + NSTAGE * 256;        // [NSTAGE][64] -Di
   static constexpr int OFF_BAR = OFF_DI + NSTAGE * 256;
   static constexpr int SMEM = OFF_BAR + 512;
   static constexpr uint32_t KT_LBO = D == 128 ? 16384 : (OFF_ZERO - OFF_K);
@@ -383,13 +383,19 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
           uint32_t a[32];
           tmem_ld32(tmem + lane_off + COL_S + ch * 32, a);
           tmem_wait_ld();
+          // (the staged LSE is negated: x = S * scale * log2e - LSE in one packed FMA)
+          const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const float4 lv = l4[c];
-            const float lv4[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              pr[c * 4 + e] = kv_ok ? ex2(fmaf(__uint_as_float(a[c * 4 + e]), sl2, -lv4[e])) : 0.f;
+            const float2 x0 = fma2(make_float2(__uint_as_float(a[c * 4]), __uint_as_float(a[c * 4 + 1])), sl2v,
+                                   make_float2(lv.x, lv.y));
+            const float2 x1 = fma2(make_float2(__uint_as_float(a[c * 4 + 2]), __uint_as_float(a[c * 4 + 3])),
+                                   sl2v, make_float2(lv.z, lv.w));
+            pr[c * 4] = kv_ok ? ex2(x0.x) : 0.f;
+            pr[c * 4 + 1] = kv_ok ? ex2(x0.y) : 0.f;
+            pr[c * 4 + 2] = kv_ok ? ex2(x1.x) : 0.f;
+            pr[c * 4 + 3] = kv_ok ? ex2(x1.y) : 0.f;
           }
           uint32_t pk[16];
 #pragma unroll
@@ -410,13 +416,20 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
           uint32_t a[32];
           tmem_ld32(tmem + lane_off + COL_DP + ch * 32, a);
           tmem_wait_ld();
+          // (the staged Di is negated: dS = P * (dP + (-Di)) in two packed ops per pair)
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const float4 dv = d4[c];
-            const float dv4[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              pr[c * 4 + e] = pr[c * 4 + e] * (__uint_as_float(a[c * 4 + e]) - dv4[e]);
+            const float2 t0 = add2(make_float2(__uint_as_float(a[c * 4]), __uint_as_float(a[c * 4 + 1])),
+                                   make_float2(dv.x, dv.y));
+            const float2 t1 = add2(make_float2(__uint_as_float(a[c * 4 + 2]), __uint_as_float(a[c * 4 + 3])),
+                                   make_float2(dv.z, dv.w));
+            const float2 r0 = mul2(make_float2(pr[c * 4], pr[c * 4 + 1]), t0);
+            const float2 r1 = mul2(make_float2(pr[c * 4 + 2], pr[c * 4 + 3]), t1);
+            pr[c * 4] = r0.x;
+            pr[c * 4 + 1] = r0.y;
+            pr[c * 4 + 2] = r1.x;
+            pr[c * 4 + 3] = r1.y;
           }
           uint32_t pk[16];
 #pragma unroll
@@ -462,8 +475,8 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
             uint32_t w[32];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              w[e] = pack_bf16(__uint_as_float(v[0][2 * e]) * mul, __uint_as_float(v[0][2 * e + 1]) * mul);
-              w[16 + e] = pack_bf16(__uint_as_float(v[1][2 * e]) * mul, __uint_as_float(v[1][2 * e + 1]) * mul);
+              w[e] = pack_bf16_mul(v[0][2 * e], v[0][2 * e + 1], make_float2(mul, mul));
+              w[16 + e] = pack_bf16_mul(v[1][2 * e], v[1][2 * e + 1], make_float2(mul, mul));
             }
             const int grp = wq * 32 + (lane & ~3);
             __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(which ? p.dk : p.dv);
@@ -479,7 +492,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
               uint32_t pk[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                pk[e] = pack_bf16(__uint_as_float(v[cc][2 * e]) * mul, __uint_as_float(v[cc][2 * e + 1]) * mul);
+                pk[e] = pack_bf16_mul(v[cc][2 * e], v[cc][2 * e + 1], make_float2(mul, mul));
               const int c = ch * (D / 64) + cc;
               st_global_v8(dst + c * 4, pk);
               st_global_v8(dst + c * 4 + 2, pk + 8);
@@ -545,10 +558,15 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       (void)jb.rows;  // rows past the sequence carry zeros (P = 0 there)
       if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
+      const float2 sc2 = make_float2(p.scale, p.scale);
 #pragma unroll
       for (int qc = 0; qc < 2; ++qc)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) stg[(qc * 32 + j) * 32 + lane] = __uint_as_float(v[qc][j]) * p.scale;
+        for (int j = 0; j < 32; j += 2) {
+          const float2 x = mul2(make_float2(__uint_as_float(v[qc][j]), __uint_as_float(v[qc][j + 1])), sc2);
+          stg[(qc * 32 + j) * 32 + lane] = x.x;
+          stg[(qc * 32 + j + 1) * 32 + lane] = x.y;
+        }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -572,7 +590,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       if (!mbar_wait(&bars.stage_full[s], bit(fph, s), ctl, 31)) goto done;
       fph ^= 1u << s;
       {
-        float di = 0.f;
+        float2 di2 = make_float2(0.f, 0.f);
         if (row_ok) {
           const uint8_t *drow = smem + C::OFF_STAGE + s * 2 * C::QT + C::QT +
                                 ((half * ND) / 64) * C::QCHUNK + row * 128;
@@ -583,18 +601,14 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
             const __nv_bfloat162 *d2 = reinterpret_cast<const __nv_bfloat162 *>(&dv);
             const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&o_r[j]);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 df = __bfloat1622float2(d2[e]);
-              const float2 of = __bfloat1622float2(o2[e]);
-              di = fmaf(of.x, df.x, di);
-              di = fmaf(of.y, df.y, di);
-            }
+            for (int e = 0; e < 4; ++e) di2 = fma2(__bfloat1622float2(o2[e]), __bfloat1622float2(d2[e]), di2);
           }
         }
+        float di = di2.x + di2.y;
         di += __shfl_xor_sync(0xffffffffu, di, 8);
         if (half == 0) {
-          lse_s[s * 64 + row] = row_ok ? lse_r * 1.4426950408889634f : INFINITY;
-          di_s[s * 64 + row] = row_ok ? di : 0.f;
+          lse_s[s * 64 + row] = row_ok ? -lse_r * 1.4426950408889634f : -INFINITY;  // negated
+          di_s[s * 64 + row] = row_ok ? -di : 0.f;                                  // negated
         }
       }
       __syncwarp();

@@ -349,7 +349,8 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(s[c][i]));
+          for (int i = 0; i < 16; ++i)
+            mx[i & 7] = max3f(mx[i & 7], __uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1]));
         const float m_tile =
             fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
@@ -361,20 +362,22 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           alpha = ex2(m_run - m_tile);
           m_run = m_tile;
         }
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_run, -m_run);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(__uint_as_float(s[c][2 * i]), sl2, -m_run));
-            const float p1 = ex2(fmaf(__uint_as_float(s[c][2 * i + 1]), sl2, -m_run));
-            sum[i & 3] += p0 + p1;
-            pk[i] = pack_bf16(p0, p1);
+            const float2 x = fma2(make_float2(__uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1])),
+                                  sl2v, negm);
+            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            sum2[i & 1] = add2(sum2[i & 1], pp);
+            pk[i] = pack_bf16(pp.x, pp.y);
           }
           tmem_st16(tS + c * 16, pk);
         }
-        l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+        l_run = l_run * alpha + ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
@@ -397,6 +400,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       tc_fence_after();
       {
         const float inv_l = 1.f / l_run;
+        const float2 inv2 = make_float2(inv_l, inv_l);
 #pragma unroll 1
         for (int c = 0; c < D / 32; c += 2) {  // two 32-column chunks in flight
           uint32_t o[2][32];
@@ -408,9 +412,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
             for (int h = 0; h < 2; ++h) {
               uint32_t pk[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                pk[i] = pack_bf16(__uint_as_float(o[h][2 * i]) * inv_l,
-                                  __uint_as_float(o[h][2 * i + 1]) * inv_l);
+              for (int i = 0; i < 16; ++i) pk[i] = pack_bf16_mul(o[h][2 * i], o[h][2 * i + 1], inv2);
               st_global_v8(optr + (c + h) * 4, pk);
               st_global_v8(optr + (c + h) * 4 + 2, pk + 8);
             }

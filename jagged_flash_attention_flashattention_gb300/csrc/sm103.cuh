@@ -30,6 +30,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Three-input maximum (one instruction).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Packed fp32 pair arithmetic (one instruction for two lanes of work).
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   float2 d;
@@ -64,6 +71,12 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half)
   return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// bf16 pair of two fp32 bit patterns, both scaled by s (one packed multiply).
+__device__ __forceinline__ uint32_t pack_bf16_mul(uint32_t lo, uint32_t hi, float2 s) {
+  const float2 v = mul2(make_float2(__uint_as_float(lo), __uint_as_float(hi)), s);
+  return pack_bf16(v.x, v.y);
 }
 
 // Phase bit of slot s in a per-role bitmask of mbarrier phases.
