@@ -369,6 +369,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
       if (tl.nq == 0 || tl.nkv <= 0) continue;
       const bool kv_ok = r < tl.nkv;
+      const bool warp_ok = __all_sync(0xffffffffu, kv_ok);  // uniform: no per-element masking
       for (int i = 0; i < tl.nq; ++i, ++qb) {
         const int s = qb % C::NSTAGE;
         if (!mbar_wait(&bars.aux_full[s], bit(aph, s), ctl, 20)) goto done;
@@ -392,10 +393,14 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
                                    make_float2(lv.x, lv.y));
             const float2 x1 = fma2(make_float2(__uint_as_float(a[c * 4 + 2]), __uint_as_float(a[c * 4 + 3])),
                                    sl2v, make_float2(lv.z, lv.w));
-            pr[c * 4] = kv_ok ? ex2(x0.x) : 0.f;
-            pr[c * 4 + 1] = kv_ok ? ex2(x0.y) : 0.f;
-            pr[c * 4 + 2] = kv_ok ? ex2(x1.x) : 0.f;
-            pr[c * 4 + 3] = kv_ok ? ex2(x1.y) : 0.f;
+            pr[c * 4] = ex2(x0.x);
+            pr[c * 4 + 1] = ex2(x0.y);
+            pr[c * 4 + 2] = ex2(x1.x);
+            pr[c * 4 + 3] = ex2(x1.y);
+          }
+          if (!warp_ok) {  // key rows past the sequence (last tile only) have P = 0
+#pragma unroll
+            for (int i = 0; i < 32; ++i) pr[i] = kv_ok ? pr[i] : 0.f;
           }
           uint32_t pk[16];
 #pragma unroll
