@@ -603,10 +603,10 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
 #pragma unroll
           for (int j = 0; j < NV; ++j) {
             const uint4 dv = *reinterpret_cast<const uint4 *>(drow + (((j0 + j) ^ (row & 7)) << 4));
-            const __nv_bfloat162 *d2 = reinterpret_cast<const __nv_bfloat162 *>(&dv);
-            const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&o_r[j]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) di2 = fma2(__bfloat1622float2(o2[e]), __bfloat1622float2(d2[e]), di2);
+            di2 = fma_bf16x2_f32(o_r[j].x, dv.x, di2);
+            di2 = fma_bf16x2_f32(o_r[j].y, dv.y, di2);
+            di2 = fma_bf16x2_f32(o_r[j].z, dv.z, di2);
+            di2 = fma_bf16x2_f32(o_r[j].w, dv.w, di2);
           }
         }
         float di = di2.x + di2.y;

@@ -73,6 +73,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// acc.x += a.lo * b.lo, acc.y += a.hi * b.hi for two bf16 pairs, with no
+// conversion step: mixed-precision FMA (bf16 sources, fp32 addend and
+// result). A product of two bf16 values is exact in fp32, so this equals
+// widening both and using fp32 FMAs.
+__device__ __forceinline__ float2 fma_bf16x2_f32(uint32_t a, uint32_t b, float2 acc) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(a), "r"(b));
+  return acc;
+}
+
 // bf16 pair of two fp32 bit patterns, both scaled by s (one packed multiply).
 __device__ __forceinline__ uint32_t pack_bf16_mul(uint32_t lo, uint32_t hi, float2 s) {
   const float2 v = mul2(make_float2(__uint_as_float(lo), __uint_as_float(hi)), s);
