@@ -318,7 +318,7 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
                           "accumulator clear"));
   if (Tk > 0) JFA_TRY(launch_status(launch_bwd(p, D, num_sms, st), "bwd launch"));
   if (Lq > 0) return JFA_OK;
-  return launch_status(launch_dq_convert(acc, dq, acc_rows, H, D, p.status, st), "dq convert");
+  return launch_status(launch_dq_convert(acc, dq, acc_rows, H, D, scale, p.status, st), "dq convert");
 }
 
 }  // namespace

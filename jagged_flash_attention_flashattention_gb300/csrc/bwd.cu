@@ -28,8 +28,9 @@
 //   dQ^T = K^T dS^T     (both operands MN-major in shared memory)  -> TMEM
 // The dQ group reads dQ^T out of TMEM (one head-dim lane per thread; two
 // TMEM buffers, so the next block's dQ^T product does not wait for the
-// reduction), releases the TMEM at once, scales, stages its 64 x 32 fp32
-// box in an 8 KB shared-memory buffer and adds it with a single TMA
+// reduction), releases the TMEM at once, stages its 64 x 32 fp32 box in
+// an 8 KB shared-memory buffer (scaled here only for broadcast-Q; the
+// jagged cast applies the scale once to the sum) and adds it with a single TMA
 // reduce-add (fewer, larger reductions measured faster than 32-row ones)
 // into an fp32 accumulator in global memory: a workspace accumulator that a
 // light kernel casts to bf16 at the end (jagged), or the caller's fp32 dQ
@@ -563,15 +564,22 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       (void)jb.rows;  // rows past the sequence carry zeros (P = 0 there)
       if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
-      const float2 sc2 = make_float2(p.scale, p.scale);
+      if constexpr (BCAST) {  // the caller's fp32 dQ is the accumulator: scale each partial
+        const float2 sc2 = make_float2(p.scale, p.scale);
 #pragma unroll
-      for (int qc = 0; qc < 2; ++qc)
+        for (int qc = 0; qc < 2; ++qc)
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float2 x = mul2(make_float2(__uint_as_float(v[qc][j]), __uint_as_float(v[qc][j + 1])), sc2);
-          stg[(qc * 32 + j) * 32 + lane] = x.x;
-          stg[(qc * 32 + j + 1) * 32 + lane] = x.y;
-        }
+          for (int j = 0; j < 32; j += 2) {
+            const float2 x = mul2(make_float2(__uint_as_float(v[qc][j]), __uint_as_float(v[qc][j + 1])), sc2);
+            stg[(qc * 32 + j) * 32 + lane] = x.x;
+            stg[(qc * 32 + j + 1) * 32 + lane] = x.y;
+          }
+      } else {  // jagged: the cast to bf16 applies the scale once, to the sum
+#pragma unroll
+        for (int qc = 0; qc < 2; ++qc)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) stg[(qc * 32 + j) * 32 + lane] = __uint_as_float(v[qc][j]);
+      }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -671,16 +679,16 @@ __global__ void acc_clear_kernel(float *acc, int64_t n16, const uint32_t *status
     base[i] = make_uint4(0, 0, 0, 0);
 }
 
-// fp32 [rows, H, D] -> bf16 [rows, H, D]; 8 elements per thread.
+// scale * fp32 [rows, H, D] -> bf16 [rows, H, D]; 8 elements per thread.
 __global__ void dq_convert_kernel(const float4 *__restrict__ acc, uint4 *__restrict__ dq, int64_t n8,
-                                  uint32_t *status) {
+                                  float scale, uint32_t *status) {
   if (blockIdx.x == 0 && threadIdx.x == 0)  // the accumulator is dirty until cleared again
     *reinterpret_cast<volatile uint64_t *>(reinterpret_cast<uint8_t *>(status) + kAccZeroedOff) = 0;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float4 a = acc[2 * i], b = acc[2 * i + 1];
-    dq[i] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
-                       pack_bf16(b.z, b.w));
+    dq[i] = make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
+                       pack_bf16(b.x * scale, b.y * scale), pack_bf16(b.z * scale, b.w * scale));
   }
 }
 
@@ -706,11 +714,11 @@ cudaError_t launch_acc_clear(float *acc, int64_t n16, const uint32_t *status, cu
   return cudaGetLastError();
 }
 
-cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, int D,
+cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, int D, float scale,
                               uint32_t *status, cudaStream_t st) {
   const int64_t n8 = rows * H * D / 8;
   dq_convert_kernel<<<grid_for(n8), 256, 0, st>>>(reinterpret_cast<const float4 *>(acc),
-                                                  static_cast<uint4 *>(dq), n8, status);
+                                                  static_cast<uint4 *>(dq), n8, scale, status);
   return cudaGetLastError();
 }
 

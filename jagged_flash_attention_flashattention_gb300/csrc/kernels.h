@@ -71,9 +71,10 @@ cudaError_t launch_bwd(const BwdParams &p, int D, int num_sms, cudaStream_t st);
 // block already records at least that many zero bytes.
 cudaError_t launch_acc_clear(float *acc, int64_t n16, const uint32_t *status, cudaStream_t st);
 
-// fp32 [rows, H, D] accumulator -> bf16 [rows, H, D]; also resets the status
-// block's zero-accumulator count (the accumulator is dirty from here on).
-cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, int D,
+// scale * fp32 [rows, H, D] -> bf16 [rows, H, D] (the jagged accumulator
+// holds unscaled dS K sums); also resets the status block's
+// zero-accumulator count (the accumulator is dirty from here on).
+cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, int D, float scale,
                               uint32_t *status, cudaStream_t st);
 
 // Block-diagonal kernels: [B, L, H, D], 64-token blocks, 128-row work units.
