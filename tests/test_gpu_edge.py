@@ -107,3 +107,54 @@ def test_dq_accumulator_clearing_in_every_call_order():
     o_s, l_s = fwd("small")  # the last forward cleared fewer bytes than "large" needs
     bwd_check("large", o_l, l_l, "larger bwd after a smaller forward")
     bwd_check("small", o_s, l_s, "bwd after another batch's bwd")
+
+
+def test_pipelined_steps_sharing_a_workspace_match_single_calls():
+    # The pattern of the end-to-end measurement: two device buffer sets, host
+    # copies on their own streams, plans rebuilt every step on one shared
+    # workspace (so each forward clears the accumulator the next backward uses).
+    # Every step's outputs must equal a fresh single call on the same inputs
+    # (dK, dV, O bit for bit; dQ up to the order of its atomic additions).
+    H, D = 2, 128
+    lengths = [70, 300, 5, 129]
+    comp = torch.cuda.current_stream()
+    batches = [W.jagged_inputs(lengths, H, D, 40 + n, device="cuda") for n in range(3)]
+    host = [{k: v.cpu().pin_memory() for k, v in b.items()} for b in batches]
+    off_host = W.offsets_of(lengths)
+    h_off = torch.from_numpy(off_host).pin_memory()
+    ws = jfa.Plan(torch.from_numpy(off_host).cuda(), H, D).workspace
+    d_in = [{k: torch.empty_like(v) for k, v in batches[0].items()} for _ in range(2)]
+    d_off = [torch.empty_like(h_off, device="cuda") for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    outs = []
+    for n in range(3):
+        b = n & 1
+        with torch.cuda.stream(s_in):
+            if n >= 2:
+                s_in.wait_event(ev_comp[b])
+            for k in d_in[b]:
+                d_in[b][k].copy_(host[n][k], non_blocking=True)
+            d_off[b].copy_(h_off, non_blocking=True)
+        comp.wait_stream(s_in)
+        x = d_in[b]
+        plan = jfa.Plan(d_off[b], H, D, host_offsets=off_host, workspace=ws)
+        o, lse = jfa.jfa_fwd(x["q"], x["k"], x["v"], d_off[b], plan=plan)
+        g = jfa.jfa_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], d_off[b], plan=plan)
+        ev_comp[b].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[b])
+            outs.append([t.to("cpu", non_blocking=True) for t in (o,) + tuple(g)])
+            for t in (o,) + tuple(g):
+                t.record_stream(s_out)
+    torch.cuda.synchronize()
+    jfa.check_status(ws)
+    off = torch.from_numpy(off_host).cuda()
+    for n in range(3):
+        x = batches[n]
+        o, lse = jfa.jfa_fwd(x["q"], x["k"], x["v"], off)
+        ref = (o,) + tuple(jfa.jfa_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], off))
+        got = outs[n]
+        assert torch.equal(got[0], ref[0].cpu()), "O differs at step %d" % n
+        assert torch.equal(got[2], ref[2].cpu()) and torch.equal(got[3], ref[3].cpu()), n
+        assert_close(got[1], ref[1], "dQ step %d" % n, atol=1e-2, rl2=1e-3)
