@@ -19,10 +19,13 @@
 // Per query block:
 //   S^T  = K Q^T        (M=128 keys, N=64 queries, K=D)      -> TMEM
 //   dP^T = V dO^T                                            -> TMEM
-//   P^T, dS^T computed by the compute warps (one key row per thread);
+//   P^T, dS^T computed by the compute warps (one key row per thread, on
+//   packed fp32 pairs; LSE and Di are staged negated so that each of P and
+//   dS is one packed FMA / add per pair);
 //   LSE and Di = rowsum(dO * O) of the block's 64 query rows are formed
 //   inline by the dQ warps, two blocks ahead of their dQ reduction (O rows
-//   read from global memory, dO from the stage; no separate pass);
+//   read from global memory, dO from the stage, bf16 products accumulated
+//   in fp32 by mixed-precision FMAs; no separate pass);
 //   dV  += P^T dO       (A = P^T bf16 from TMEM)
 //   dK  += dS^T Q       (A = dS^T bf16 from TMEM)
 //   dQ^T = K^T dS^T     (both operands MN-major in shared memory)  -> TMEM
