@@ -34,7 +34,11 @@ sys.path.insert(0, ROOT)
 # the first 256 sequences (dram__bytes_read.sum + dram__bytes_write.sum)
 # scaled by the processed (key tile, query block) pairs. Reset to None
 # whenever the backward kernel changes until it is measured again.
-BWD_GEM_TRAFFIC = 4.22e9
+BWD_GEM_TRAFFIC = None
+
+# Nominal dense bf16 tensor peak of one GB300 (NVIDIA's figure without 2:4
+# sparsity), the second denominator reported next to the measured cuBLAS peak.
+SPEC_BF16_TFLOPS = 2250.0
 
 
 def _spin(stream, cycles=2_000_000):
@@ -247,7 +251,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def _setup(name, rank, dev, seqs=0):
+def _setup(name, rank, dev, seqs=0, zigzag=True):
     """Inputs and one hot-path step for a named workload. Returns a dict."""
     import torch
 
@@ -264,12 +268,12 @@ def _setup(name, rank, dev, seqs=0):
         off_host = W.offsets_of(L, cfg["offsets_dtype"])
         inp = W.jagged_inputs(L, H, D, W.SEEDS[name] + 1000 * rank, device=dev)
         off = torch.from_numpy(off_host).to(dev)
-        ws_buf = jfa.Plan(off, H, D, host_offsets=off_host).workspace
+        ws_buf = jfa.Plan(off, H, D, host_offsets=off_host, zigzag=zigzag).workspace
         st["fwd_flops"] = W.useful_flops("jagged", L, H=H, D=D)
         st["desc"] = "%s: B=%d, T=%d, H=%d, D=%d, max len %d" % (name, len(L), int(off_host[-1]), H, D, int(max(L)))
 
         def fwd():
-            st["plan"] = jfa.Plan(off, H, D, host_offsets=off_host, workspace=ws_buf)
+            st["plan"] = jfa.Plan(off, H, D, host_offsets=off_host, workspace=ws_buf, zigzag=zigzag)
             st["o"], st["lse"] = jfa.jfa_fwd(inp["q"], inp["k"], inp["v"], off, plan=st["plan"])
 
         def bwd():
@@ -286,7 +290,7 @@ def _setup(name, rank, dev, seqs=0):
         st["desc"] = "bcast: Lq=%d, B=%d, Tk=%d, H=%d, D=%d" % (Lq, len(L), int(off_host[-1]), H, D)
 
         def fwd():
-            st["plan"] = jfa.Plan(off, H, D, kind="bcast", Lq=Lq, host_offsets=off_host)
+            st["plan"] = jfa.Plan(off, H, D, kind="bcast", Lq=Lq, host_offsets=off_host, zigzag=zigzag)
             st["o"], st["lse"] = jfa.jfa_bcastq_fwd(inp["q"], inp["k"], inp["v"], off, plan=st["plan"])
 
         def bwd():
@@ -315,12 +319,100 @@ def _setup(name, rank, dev, seqs=0):
     return st
 
 
+def _time_steps(st, steps, warmup, stream, sampler=None, barrier=None):
+    """Times `steps` fwd+bwd steps of a set-up workload after `warmup` untimed
+    ones, with CUDA events on `stream`; `barrier` (multi-rank runs) is called
+    on both sides of the timed region. Returns (total ms, median fwd ms,
+    median bwd ms, clocks or None)."""
+    import torch
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        st["fwd"]()
+        if ev is not None:
+            ev[1].record(stream)
+        st["bwd"]()
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(warmup):
+        step()
+    st["check"]()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if barrier is not None:
+        barrier()
+    torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.start()
+    # A short device-side spin before the start event lets the host queue the
+    # timed steps ahead of the GPU, so host launch latency stays out of the
+    # timed region (it holds only the steps' own kernels).
+    _spin(stream)
+    t0.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = sampler.stop() if sampler is not None else None
+    if barrier is not None:
+        barrier()
+    st["check"]()
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+    return t0.elapsed_time(t1), fwd_ms, bwd_ms, clk
+
+
+def _fracs(tflops, peak, spec=SPEC_BF16_TFLOPS):
+    return {"tflops": round(tflops, 1), "frac_of_peak": round(tflops / peak, 4),
+            "frac_of_spec_peak": round(tflops / spec, 4)}
+
+
+def _other_configs(args, dev, peaks):
+    """Every other workload of the method, each timed like the headline one
+    (W warm-up and K timed fwd+bwd steps, CUDA events, median per op), plus the
+    stress workload under the naive tile order for the LPT + zigzag A/B."""
+    import torch
+
+    hbm_peak, tc_peak = peaks
+    stream = torch.cuda.current_stream()
+    steps, warmup = max(3, min(args.steps, 10)), 3
+    out = {}
+    for name in ("stress", "bcast", "blockdiag", "blockdiag64"):
+        st = _setup(name, 0, dev)
+        _, f_ms, b_ms, _ = _time_steps(st, steps, warmup, stream)
+        ff, bf = st["fwd_flops"], st["bwd_flops"]
+        rec = {"workload": st["desc"], "steps": steps,
+               "fwd": dict(ms=round(f_ms, 4), **_fracs(ff / f_ms / 1e9, tc_peak)),
+               "bwd": dict(ms=round(b_ms, 4), **_fracs(bf / b_ms / 1e9, tc_peak))}
+        if st["kind"] == "blockdiag":
+            for op, nbytes, ms in (("fwd", st["fwd_bytes"], f_ms), ("bwd", st["bwd_bytes"], b_ms)):
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                rec[op]["gbps"] = round(gbs, 1)
+                rec[op]["frac_of_hbm_peak"] = round(gbs / hbm_peak, 4)
+            rec["bytes_note"] = ("modelled bytes (inputs read once, outputs written once) over "
+                                 "the measured copy peak")
+        out[name] = rec
+        if name == "stress":
+            nv = _setup(name, 0, dev, zigzag=False)
+            _, nf_ms, nb_ms, _ = _time_steps(nv, steps, warmup, stream)
+            out["schedule_ab"] = {
+                "workload": st["desc"],
+                "fwd_ms_zigzag": round(f_ms, 4), "fwd_ms_naive": round(nf_ms, 4),
+                "bwd_ms_zigzag": round(b_ms, 4), "bwd_ms_naive": round(nb_ms, 4),
+                "fwd_naive_over_zigzag": round(nf_ms / f_ms, 3),
+                "bwd_naive_over_zigzag": round(nb_ms / b_ms, 3)}
+            del nv
+        del st
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
-
-    import jagged_flash_attention_flashattention_gb300 as jfa
-    from jagged_flash_attention_flashattention_gb300 import workloads as W
 
     ws, rank, local = _dist()
     if ws > 1:
@@ -329,56 +421,22 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     hbm_peak, tc_peak, tc_sust, peak_src = _peaks()
 
-    st = _setup(args.config, rank, dev, args.seqs)
+    st = _setup(args.config, rank, dev, args.seqs, zigzag=args.schedule == "zigzag")
     fwd_flops, bwd_flops = st["fwd_flops"], st["bwd_flops"]
     stream = torch.cuda.current_stream()
-
-    def step(timing=None):
-        if timing is not None:
-            timing["e0"].record(stream)
-        st["fwd"]()
-        if timing is not None:
-            timing["e1"].record(stream)
-        st["bwd"]()
-        if timing is not None:
-            timing["e2"].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    st["check"]()
-
-    evs = [{n: torch.cuda.Event(enable_timing=True) for n in ("e0", "e1", "e2")}
-           for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    # A short device-side spin before the start event lets the host queue the
-    # timed steps ahead of the GPU, so host launch latency stays out of the
-    # timed region (it holds only the steps' own kernels).
-    _spin(stream)
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    if ws > 1:
-        dist.barrier()
-    st["check"]()
-    total_ms = t_start.elapsed_time(t_end)
-    fwd_ms = statistics.median(e["e0"].elapsed_time(e["e1"]) for e in evs)
-    bwd_ms = statistics.median(e["e1"].elapsed_time(e["e2"]) for e in evs)
+    total_ms, fwd_ms, bwd_ms, clk = _time_steps(st, args.steps, args.warmup, stream,
+                                                ClockSampler(local),
+                                                dist.barrier if ws > 1 else None)
     job_flops, t_max = aggregate_over_ranks(fwd_flops + bwd_flops, total_ms, ws, dev)
     ms_per_step = t_max / args.steps
     value = job_flops / (ms_per_step * 1e-3) / 1e12
 
-    e2e = None
-    if args.config == "gem" and not args.seqs:
-        e2e = _e2e_gem(args, st, dev, ws)
+    full_gem = args.config == "gem" and not args.seqs
+    e2e = _e2e_gem(args, st, dev, ws, ms_per_step) if full_gem else None
+    configs = None
+    if full_gem and rank == 0 and not args.no_configs:
+        del st["inp"]
+        configs = _other_configs(args, dev, (hbm_peak, tc_peak))
 
     if rank == 0:
         bwd_tf = bwd_flops / (bwd_ms * 1e-3) / 1e12
@@ -388,34 +446,46 @@ def run_ours(args):
             bw = st["bwd_bytes"] / (bwd_ms * 1e-3) / 1e9
             roof = {"bound": "hbm", "kernel": "blockdiag_bwd", "achieved": round(bw, 1),
                     "peak": hbm_peak, "unit": "GB/s", "frac": round(bw / hbm_peak, 4),
-                    "traffic": None, "peak_source": peak_src + " HBM copy"}
+                    "traffic": None, "peak_source": peak_src + " HBM copy",
+                    "achieved_note": "modelled bytes (inputs read once, outputs written once) / "
+                                     "CUDA-event time; the measured copy peak is not a ceiling"}
         else:
             roof = {"bound": "tensor", "kernel": "jfa_bwd (bwd kernel + dQ cast)",
                     "achieved": round(bwd_tf, 1), "peak": peak, "unit": "TFLOP/s",
                     "frac": round(bwd_tf / peak, 4),
-                    "traffic": BWD_GEM_TRAFFIC if args.config == "gem" and not args.seqs else None,
-                    "peak_source": peak_src + " bf16 burst (cuBLAS)"}
+                    "frac_of_spec_peak": round(bwd_tf / SPEC_BF16_TFLOPS, 4),
+                    "traffic": BWD_GEM_TRAFFIC if full_gem else None,
+                    "peak_source": peak_src + " bf16 burst (cuBLAS); spec peak %.0f TFLOP/s"
+                                   % SPEC_BF16_TFLOPS}
         line = {
             "metric": METRIC,
             "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": st["desc"], "parallelism": "replicas (one batch per GPU)",
-                       "l2": "inputs larger than L2 (no flush)"},
-            "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fwd_tf, 1),
-                    "frac_of_peak": round(fwd_tf / peak, 4)},
-            "bwd": {"ms": round(bwd_ms, 4), "tflops": round(bwd_tf, 1),
-                    "frac_of_peak": round(bwd_tf / peak, 4)},
+                       "l2": "inputs larger than L2 (no flush)", "schedule": args.schedule},
+            "fwd": dict(ms=round(fwd_ms, 4), **_fracs(fwd_tf, peak)),
+            "bwd": dict(ms=round(bwd_ms, 4), **_fracs(bwd_tf, peak)),
             "pct_of_peak": round(100 * value / peak, 2),
+            "pct_of_spec_peak": round(100 * value / SPEC_BF16_TFLOPS, 2),
             "roofline": roof,
             "clocks": clk,
             "gpu_launches": (4 if st["kind"] == "jagged" else 2) * args.steps,
         }
+        if full_gem:
+            line["targets"] = {
+                op: {"target_frac": tgt, "frac_of_peak": line[op]["frac_of_peak"],
+                     "frac_of_spec_peak": line[op]["frac_of_spec_peak"],
+                     "met_vs_measured_peak": line[op]["frac_of_peak"] >= tgt,
+                     "met_vs_spec_peak": line[op]["frac_of_spec_peak"] >= tgt}
+                for op, tgt in (("fwd", 0.50), ("bwd", 0.35))}
         if st["kind"] == "blockdiag":
             line["fwd"]["gbps"] = round(st["fwd_bytes"] / (fwd_ms * 1e-3) / 1e9, 1)
             line["bwd"]["gbps"] = round(st["bwd_bytes"] / (bwd_ms * 1e-3) / 1e9, 1)
         if e2e is not None:
             line["e2e"] = e2e
+        if configs is not None:
+            line["configs"] = configs
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
@@ -423,13 +493,78 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def _e2e_gem(args, st, dev, ws):
+def _gpu_local_cpus(dev):
+    """CPUs on the host NUMA node next to the GPU (from sysfs), or None."""
+    import torch
+    bus = None
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except Exception:
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(dev.index or 0), "--query-gpu=pci.bus_id",
+                                "--format=csv,noheader"], capture_output=True, text=True, timeout=10)
+            dom, rest = r.stdout.strip().split(":", 1)
+            bus = "%04x:%s" % (int(dom, 16), rest.lower())
+        except Exception:
+            return None
+    try:
+        with open("/sys/bus/pci/devices/%s/local_cpulist" % bus) as f:
+            text = f.read().strip()
+    except Exception:
+        return None
+    cpus = set()
+    for part in text.split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus or None
+
+
+def _copy_rates(pairs_in, pairs_out, s_in, s_out, reps=3):
+    """Bare pinned copies, no kernels: host-to-device alone, device-to-host
+    alone and both at once, each over every buffer on its own stream. Returns
+    GB/s for each (best of `reps`)."""
+    import torch
+
+    def run(groups):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            cur = torch.cuda.current_stream()
+            a.record(cur)
+            nbytes = 0
+            for pairs, streams in groups:
+                for (dst, src), sj in zip(pairs, streams):
+                    sj.wait_event(a)
+                    with torch.cuda.stream(sj):
+                        dst.copy_(src, non_blocking=True)
+                    nbytes += src.numel() * src.element_size()
+            for pairs, streams in groups:
+                for sj in streams[:len(pairs)]:
+                    cur.wait_stream(sj)
+            b.record(cur)
+            torch.cuda.synchronize()
+            gbs = nbytes / (a.elapsed_time(b) * 1e-3) / 1e9
+            best = gbs if best is None else max(best, gbs)
+        return best
+
+    return (run([(pairs_in, s_in)]), run([(pairs_out, s_out)]),
+            run([(pairs_in, s_in), (pairs_out, s_out)]))
+
+
+def _e2e_gem(args, st, dev, ws, kernel_ms):
     """Same metric through the public API with host (pinned) buffers: every
     step copies q, k, v, dO and the offsets in and O, dQ, dK, dV out. Steps
     are pipelined the way a training input pipeline would run them: the
     host-to-device copy of step n+1 and the device-to-host copy of step n-1
     run on their own streams while step n's kernels run (two device buffer
-    sets; every step still moves all of its own bytes in both directions)."""
+    sets; every step still moves all of its own bytes in both directions).
+    The same run also times the bare copies with no kernels, so the line
+    shows the bound the host link puts on the end-to-end figure."""
     import torch
     import torch.distributed as dist
 
@@ -438,6 +573,22 @@ def _e2e_gem(args, st, dev, ws):
     H, D = st["H"], st["D"]
     inp = st["inp"]
     off_host = st["plan"].host_offsets
+    # Pinned buffers on the host NUMA node next to the GPU when sysfs names one
+    # (pages are placed where the allocating thread runs).
+    affinity = "unchanged"
+    local = _gpu_local_cpus(dev)
+    try:
+        allowed = os.sched_getaffinity(0)
+        if local and (local & allowed) and (local & allowed) != allowed:
+            os.sched_setaffinity(0, local & allowed)
+            affinity = "gpu-local cpus %d of %d" % (len(local & allowed), len(allowed))
+        elif local:
+            affinity = "all %d allowed cpus are gpu-local" % len(allowed) if local >= allowed else \
+                "no gpu-local cpu allowed"
+        else:
+            affinity = "gpu-local cpus unknown"
+    except Exception:
+        pass
     hq, hk, hv, hdo = (inp[n].cpu().pin_memory() for n in ("q", "k", "v", "do"))
     h_off = torch.from_numpy(off_host).pin_memory()
     h_out = [[torch.empty_like(hq).pin_memory() for _ in range(4)] for _ in range(2)]
@@ -453,6 +604,12 @@ def _e2e_gem(args, st, dev, ws):
     ev_in = [[torch.cuda.Event() for _ in range(4)] for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
     ev_out = [[torch.cuda.Event() for _ in range(4)] for _ in range(2)]
+
+    dev_out = [torch.empty_like(hq, device=dev) for _ in range(4)]
+    h2d_gbs, d2h_gbs, both_gbs = _copy_rates(list(zip(d_in[0], (hq, hk, hv, hdo))),
+                                             list(zip(h_out[0], dev_out)), s_in, s_out)
+    del dev_out
+    copy_ms = max(h2d / h2d_gbs, d2h / d2h_gbs, (h2d + d2h) / both_gbs) / 1e6
 
     def e2e_step(n):
         b = n & 1
@@ -498,9 +655,16 @@ def _e2e_gem(args, st, dev, ws):
     job_flops, ms = aggregate_over_ranks(st["fwd_flops"] + st["bwd_flops"],
                                          a0.elapsed_time(a1) / n_steps, ws, dev)
     val = job_flops / (ms * 1e-3) / 1e12
+    hidden = (copy_ms + kernel_ms - ms) / min(copy_ms, kernel_ms)
     return {"value": round(val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 3),
-            "overlap": "h2d of step n+1 and d2h of step n-1 run beside step n's kernels"}
+            "overlap": "h2d of step n+1 and d2h of step n-1 run beside step n's kernels",
+            "copy_gbps": {"h2d": round(h2d_gbs, 1), "d2h": round(d2h_gbs, 1),
+                          "both_directions": round(both_gbs, 1)},
+            "copy_bound_ms": round(copy_ms, 3), "kernel_ms": round(kernel_ms, 3),
+            "hidden_fraction": round(max(0.0, min(1.0, hidden)), 3),
+            "bound": "host link" if copy_ms > kernel_ms else "kernels",
+            "host_buffers": affinity}
 
 
 def main():
@@ -515,6 +679,10 @@ def main():
                          "a small profiling case")
     ap.add_argument("--config", default="gem",
                     choices=["gem", "stress", "bcast", "blockdiag", "blockdiag64", "tiny"])
+    ap.add_argument("--schedule", default="zigzag", choices=["zigzag", "naive"],
+                    help="tile order: host LPT + zigzag deal, or the unsorted round-robin deal")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="with the GEM workload, skip timing the other workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

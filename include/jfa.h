@@ -196,19 +196,27 @@ jfa_status jfa_bwd(const void *q, const void *k, const void *v, const void *o,
  * device, which stays allocated until the process exits on every device
  * that has loaded it. Limit: T * H * D <= 16,777,152; larger problems return
  * JFA_ERR_WORKSPACE with a message and launch nothing. The library
- * allocates and frees nothing here. The first call on each device looks up
- * the array's device address with that device current; make that first call
- * before any stream capture. Every call on a device shares the one array
+ * allocates and frees nothing here. Each call looks up the array's device
+ * address with the calling thread's current device (a host-side query, so a
+ * cudaDeviceReset, which reloads the array, is handled); the first call on a
+ * device may also load the module that holds the array, so make that first
+ * call before any stream capture. Every call on a device shares the one array
  * (each call clears what must start at zero), so calls whose work overlaps
  * on the GPU, e.g. on two streams, race and give wrong results: serialise
- * them. A kernel timeout is not reported by this variant (its status block
- * is cleared at every call); use jfa_bwd and jfa_check_status when that is
- * needed. */
+ * them. A kernel timeout is recorded in the array's status block and stays
+ * there, through later calls, until jfa_noalloc_check_status() reads it. */
 jfa_status jfa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                            const float *lse, const void *dout, const void *offsets,
                            jfa_index_t idx, int64_t B, int64_t T, int H, int D, float scale,
                            const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_sms,
                            void *dq, void *dk, void *dv, jfa_stream_t stream);
+
+/* Status of jfa_bwd_noalloc on the current device (no counterpart in the
+ * paper either): synchronises `stream`, reads the static array's status
+ * block and returns JFA_ERR_TIMEOUT, clearing the block, if a kernel of any
+ * jfa_bwd_noalloc call since the last check gave up waiting; JFA_OK
+ * otherwise. Allocates nothing. */
+jfa_status jfa_noalloc_check_status(jfa_stream_t stream);
 
 /* Broadcast-Q forward: q device bf16 [Lq, H, D] is shared by every
  * sequence of k, v (device bf16 [Tk, H, D], boundaries kv_offsets [B+1]).

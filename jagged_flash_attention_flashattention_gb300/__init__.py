@@ -40,7 +40,7 @@ EXPORTS = [
     "jfa_status_str", "jfa_last_error", "jfa_sched_size", "jfa_sched_build", "jfa_tile_rows",
     "jfa_num_sms", "jfa_workspace_size", "jfa_workspace_init", "jfa_check_status", "jfa_fwd",
     "jfa_bwd", "jfa_bcastq_fwd", "jfa_bcastq_bwd", "blockdiag_fwd", "blockdiag_bwd",
-    "jfa_bwd_noalloc", "jfa_selftest_wait_timeout",
+    "jfa_bwd_noalloc", "jfa_noalloc_check_status", "jfa_selftest_wait_timeout",
 ]
 
 
@@ -81,6 +81,7 @@ def lib():
         "blockdiag_fwd": ([P, P, P, I64, I64, I, I, F, P, P, SZ, P], I),
         "blockdiag_bwd": ([P, P, P, P, I64, I64, I, I, F, P, P, P, P, SZ, P], I),
         "jfa_bwd_noalloc": ([P, P, P, P, P, P, P, I, I64, I64, I, I, F, P, P, I, P, P, P, P], I),
+        "jfa_noalloc_check_status": ([P], I),
         "jfa_selftest_wait_timeout": ([P, SZ, ctypes.c_uint64, P], I),
     }
     for name, (args, res) in sig.items():
@@ -142,6 +143,19 @@ def schedule(offsets_host, H, tile_rows_, n_sms, fixed_rows=0, fixed_work=0, zig
     return sm_ptr, tiles[: n.value]
 
 
+def check_host_offsets(host, n):
+    """Raises unless `host` is a 1-D integer array of n >= 1 offsets starting at 0
+    and non-decreasing (the host copy the scheduler reads must describe the
+    device offsets the kernels read; at least its length is checked here)."""
+    host = np.asarray(host)
+    if host.ndim != 1 or host.size != n or host.size < 1:
+        raise ValueError("host_offsets must be 1-D with as many entries as offsets (%d)" % n)
+    if host.dtype not in (np.int32, np.int64):
+        raise ValueError("offsets must be int32 or int64")
+    if host[0] != 0 or np.any(np.diff(host.astype(np.int64)) < 0):
+        raise ValueError("offsets must start at 0 and be non-decreasing")
+
+
 class Plan:
     """Schedules (on the device) and workspace for one batch layout.
 
@@ -161,6 +175,7 @@ class Plan:
         self.offsets = offsets
         self.idx = JFA_I64 if offsets.dtype == torch.int64 else JFA_I32
         host = np.asarray(host_offsets) if host_offsets is not None else offsets.cpu().numpy()
+        check_host_offsets(host, offsets.numel())
         self.host_offsets = host
         self.B = host.size - 1
         self.T = int(host[-1])
@@ -191,6 +206,18 @@ class Plan:
         """Synchronises and raises if a kernel reported a timeout."""
         _check(lib().jfa_check_status(_ptr(self.workspace), _stream()))
 
+    def validate(self, kind, offsets, rows, H, D, Lq=0):
+        """Raises if this plan was built for another batch layout than the call's:
+        kind, offsets tensor length, packed rows (T for jagged, Tk for
+        broadcast-Q, which must equal the last offset), heads, head dim and
+        broadcast length. The kernels also clamp every sequence to the tensors
+        they are given, so a mismatch that got past this check could give wrong
+        numbers but never touch memory outside the tensors."""
+        want = (kind, offsets.numel() - 1, rows, H, D, int(Lq))
+        have = (self.kind, self.B, self.T, self.H, self.D, self.Lq)
+        if want != have:
+            raise ValueError("plan built for (kind, B, T, H, D, Lq) = %s, call has %s" % (have, want))
+
 
 def _scale(scale, D):
     return 1.0 / math.sqrt(D) if scale is None else float(scale)
@@ -202,6 +229,7 @@ def jfa_fwd(q, k, v, offsets, scale=None, plan=None):
     _need_cuda(q, k, v)
     T, H, D = q.shape
     plan = plan or Plan(offsets, H, D)
+    plan.validate("jagged", offsets, T, H, D)
     o = torch.empty_like(q)
     lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
     sp, tl = plan.fwd_sched
@@ -216,6 +244,7 @@ def jfa_bwd(q, k, v, o, lse, do, offsets, scale=None, plan=None):
     _need_cuda(q, k, v, o, do)
     T, H, D = q.shape
     plan = plan or Plan(offsets, H, D)
+    plan.validate("jagged", offsets, T, H, D)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     sp, tl = plan.bwd_sched
     _check(lib().jfa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(offsets),
@@ -231,6 +260,7 @@ def jfa_bcastq_fwd(q, k, v, kv_offsets, scale=None, plan=None):
     _need_cuda(q, k, v)
     Lq, H, D = q.shape
     plan = plan or Plan(kv_offsets, H, D, kind="bcast", Lq=Lq)
+    plan.validate("bcast", kv_offsets, k.shape[0], H, D, Lq)
     Tk, B = k.shape[0], plan.B
     o = torch.empty((B, Lq, H, D), dtype=q.dtype, device=q.device)
     lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
@@ -248,6 +278,7 @@ def jfa_bcastq_bwd(q, k, v, o, lse, do, kv_offsets, scale=None, plan=None):
     _need_cuda(q, k, v, o, do)
     Lq, H, D = q.shape
     plan = plan or Plan(kv_offsets, H, D, kind="bcast", Lq=Lq)
+    plan.validate("bcast", kv_offsets, k.shape[0], H, D, Lq)
     Tk, B = k.shape[0], plan.B
     dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     dk, dv = torch.empty_like(k), torch.empty_like(v)

@@ -14,7 +14,6 @@ using namespace jfa;
 
 namespace {
 
-constexpr size_t kStatusBytes = 256;
 constexpr uint64_t kTimeoutNs = 4ull * 1000 * 1000 * 1000;  // bounded waits give up after 4 s
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -152,19 +151,25 @@ extern "C" jfa_status jfa_workspace_init(void *workspace, size_t ws_bytes, jfa_s
                      "cudaMemsetAsync");
 }
 
-extern "C" jfa_status jfa_check_status(void *workspace, jfa_stream_t stream) {
-  JFA_TRY(check_ws(workspace, kStatusBytes, kStatusBytes));
+jfa_status jfa::read_status_block(void *status, void *stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   uint32_t st[4] = {0, 0, 0, 0};
-  JFA_TRY(cuda_status(cudaMemcpyAsync(st, workspace, sizeof(st), cudaMemcpyDeviceToHost,
-                                      (cudaStream_t)stream),
+  JFA_TRY(cuda_status(cudaMemcpyAsync(st, status, sizeof(st), cudaMemcpyDeviceToHost, stream),
                       "cudaMemcpyAsync"));
-  JFA_TRY(cuda_status(cudaStreamSynchronize((cudaStream_t)stream), "cudaStreamSynchronize"));
+  JFA_TRY(cuda_status(cudaStreamSynchronize(stream), "cudaStreamSynchronize"));
   if (st[0] != 0) {
-    cudaMemsetAsync(workspace, 0, kStatusBytes, (cudaStream_t)stream);
-    cudaStreamSynchronize((cudaStream_t)stream);
+    // The whole block is cleared; a zero count of cleared accumulator bytes
+    // only makes the next backward clear its accumulator itself.
+    cudaMemsetAsync(status, 0, kStatusBytes, stream);
+    cudaStreamSynchronize(stream);
     return fail(JFA_ERR_TIMEOUT, "kernel wait site %u in block %u gave up", st[1], st[2]);
   }
   return JFA_OK;
+}
+
+extern "C" jfa_status jfa_check_status(void *workspace, jfa_stream_t stream) {
+  JFA_TRY(check_ws(workspace, kStatusBytes, kStatusBytes));
+  return read_status_block(workspace, stream);
 }
 
 // ------------------------------------------------------------------ forward
@@ -204,6 +209,7 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *o
   p.tiles = tiles;
   p.o = o;
   p.lse = lse;
+  p.B = B;
   p.T = Lq > 0 ? Tk : q_rows;
   p.H = H;
   p.Lq = (int)Lq;
@@ -303,6 +309,7 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   p.o = o;
   p.dk = dk;
   p.dv = dv;
+  p.B = B;
   p.T = Lq > 0 ? Tk : q_rows;
   p.H = H;
   p.Lq = (int)Lq;

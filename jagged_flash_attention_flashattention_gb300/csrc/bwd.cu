@@ -117,9 +117,14 @@ __device__ __forceinline__ BwdTile decode_tile(const BwdParams &p, int t) {
   d.b = p.tiles[3 * t];
   d.h = p.tiles[3 * t + 1];
   const int n = p.tiles[3 * t + 2];
-  const int64_t s0 = load_off(p.offsets, p.idx64, d.b);
-  const int L = (int)(load_off(p.offsets, p.idx64, d.b + 1) - s0);
-  d.Lq = BCAST ? p.Lq : L;
+  // A tile outside this batch (a schedule built for another one) is empty,
+  // and sequence bounds are clamped to [0, T]: no row past the tensors is
+  // read or written whatever the tile list or the offsets hold.
+  const bool in = d.b >= 0 && d.b < p.B && d.h >= 0 && d.h < p.H && n >= 0 && n < (1 << 23);
+  const int64_t s0 = in ? min(max(load_off(p.offsets, p.idx64, d.b), (int64_t)0), p.T) : 0;
+  const int64_t e0 = in ? min(max(load_off(p.offsets, p.idx64, d.b + 1), s0), p.T) : 0;
+  const int L = (int)(e0 - s0);
+  d.Lq = BCAST ? (in ? p.Lq : 0) : L;
   d.nq = (d.Lq + 63) / 64;
   d.nkv = min(128, L - n * 128);
   d.kv_row0 = (int)s0 + n * 128;

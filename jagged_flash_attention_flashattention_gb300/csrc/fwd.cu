@@ -89,9 +89,14 @@ __device__ __forceinline__ FwdTile decode_tile(const FwdParams &p, int t) {
   d.b = p.tiles[3 * t];
   d.h = p.tiles[3 * t + 1];
   const int m = p.tiles[3 * t + 2];
-  const int64_t s0 = load_off(p.offsets, p.idx64, d.b);
-  const int L = (int)(load_off(p.offsets, p.idx64, d.b + 1) - s0);
-  const int Lq = BCAST ? p.Lq : L;
+  // A tile outside this batch (a schedule built for another one) is empty,
+  // and sequence bounds are clamped to [0, T]: no row past the tensors is
+  // read or written whatever the tile list or the offsets hold.
+  const bool in = d.b >= 0 && d.b < p.B && d.h >= 0 && d.h < p.H && m >= 0 && m < (1 << 22);
+  const int64_t s0 = in ? min(max(load_off(p.offsets, p.idx64, d.b), (int64_t)0), p.T) : 0;
+  const int64_t e0 = in ? min(max(load_off(p.offsets, p.idx64, d.b + 1), s0), p.T) : 0;
+  const int L = (int)(e0 - s0);
+  const int Lq = BCAST ? (in ? p.Lq : 0) : L;
   const int row0 = m * 256;
   d.Lk = L;
   d.n_kv = (L + 127) / 128;

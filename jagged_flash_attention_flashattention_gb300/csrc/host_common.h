@@ -1,5 +1,6 @@
 // Host-side helpers shared by the C-ABI translation units: status strings,
-// the thread-local detail message and offsets validation.
+// the thread-local detail message, offsets validation and the layout of the
+// status block at the head of every workspace.
 #pragma once
 #include <cstdarg>
 #include <cstdint>
@@ -8,6 +9,17 @@
 #include "jfa.h"
 
 namespace jfa {
+
+// Bytes of the status block at the head of every workspace (and of the
+// static scratch of jfa_bwd_noalloc): word 0 error code (0 = none), word 1
+// wait site, word 2 block index; the uint64 at byte 128 counts accumulator
+// bytes known to be zero.
+constexpr size_t kStatusBytes = 256;
+
+// Synchronises `stream` (a cudaStream_t), reads the status block at device
+// address `status` and returns JFA_ERR_TIMEOUT if a kernel gave up waiting,
+// after clearing the block's error words; JFA_OK otherwise.
+jfa_status read_status_block(void *status, void *stream);
 
 // Records a detail message for jfa_last_error() and returns `s`.
 jfa_status fail(jfa_status s, const char *fmt, ...);

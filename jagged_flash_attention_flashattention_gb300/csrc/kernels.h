@@ -20,7 +20,9 @@ struct FwdParams {
   const int32_t *tiles;
   void *o;      // bf16
   float *lse;   // fp32
-  int64_t T;    // packed length (LSE row stride for the jagged layout)
+  int64_t B;    // sequences: tiles naming b >= B are skipped
+  int64_t T;    // packed K/V length (LSE row stride for the jagged layout);
+                // sequence bounds read from the offsets are clamped to [0, T]
   int H;
   int Lq;       // broadcast-Q: dense query length; 0 for jagged self-attention
   float scale_log2;  // scale * log2(e)
@@ -56,7 +58,8 @@ struct BwdParams {
   const void *o;  // bf16 O rows (read directly for Di)
   void *dk;  // bf16 [Tk, H, D]
   void *dv;
-  int64_t T;
+  int64_t B;  // sequences: tiles naming b >= B are skipped
+  int64_t T;  // packed K/V length; sequence bounds are clamped to [0, T]
   int H;
   int Lq;  // broadcast-Q: dense query length; 0 for jagged
   float scale;

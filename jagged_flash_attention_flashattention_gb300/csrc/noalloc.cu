@@ -16,39 +16,28 @@
 // exits.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "host_common.h"
 #include "jfa.h"
 
 namespace {
 
+using jfa::kStatusBytes;
+
 constexpr size_t kScratchBytes = size_t(64) << 20;  // 64 MiB per device
-constexpr size_t kStatusBytes = 256;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device. The name of the
-// array is only a host-side handle; the address has to be looked up once per
-// device with that device current.
+// Device address of the scratch array in the current device's context. In
+// host code the array's name is only a handle, so the address is looked up
+// with the device current. It is looked up at every call (a host-side query,
+// no allocation) rather than cached, so it stays right after a
+// cudaDeviceReset, which reloads the module and the array with it.
 jfa_status scratch_for_current_device(void **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return jfa::fail(JFA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return jfa::fail(JFA_ERR_UNSUPPORTED, "device %d", dev);
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p)
-      return jfa::fail(JFA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p)
+    return jfa::fail(JFA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+  *out = p;
   return JFA_OK;
 }
 
@@ -71,9 +60,18 @@ extern "C" jfa_status jfa_bwd_noalloc(const void *q, const void *k, const void *
   void *scratch = nullptr;
   jfa_status st = scratch_for_current_device(&scratch);
   if (st != JFA_OK) return st;
-  // The status block must start at zero; jfa_bwd clears the accumulator itself.
-  cudaError_t e = cudaMemsetAsync(scratch, 0, kStatusBytes, (cudaStream_t)stream);
-  if (e != cudaSuccess) return jfa::fail(JFA_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+  // The status block needs no clearing here: the array starts at zero, a
+  // kernel only writes its error words when a wait gives up (they then stay
+  // set until jfa_noalloc_check_status reads and clears them), and the
+  // backward's closing cast resets the cleared-accumulator count, so jfa_bwd
+  // always clears the accumulator itself.
   return jfa_bwd(q, k, v, o, lse, dout, offsets, idx, B, T, H, D, scale, d_sm_ptr, d_tiles,
                  num_sms, dq, dk, dv, scratch, kScratchBytes, stream);
+}
+
+extern "C" jfa_status jfa_noalloc_check_status(jfa_stream_t stream) {
+  void *scratch = nullptr;
+  jfa_status st = scratch_for_current_device(&scratch);
+  if (st != JFA_OK) return st;
+  return jfa::read_status_block(scratch, stream);
 }

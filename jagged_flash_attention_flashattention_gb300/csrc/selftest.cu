@@ -11,7 +11,7 @@
 
 namespace {
 
-constexpr size_t kStatusBytes = 256;
+using jfa::kStatusBytes;
 constexpr int kSite = 99;  // the wait site reported by this probe
 
 __global__ void wait_timeout_probe(uint32_t *status, uint64_t timeout_ns) {

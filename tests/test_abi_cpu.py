@@ -155,3 +155,57 @@ def test_bcastq_rejects_batches_past_32_bit_row_indices(L):
     assert L.jfa_bcastq_bwd(p, p, p, p, p, p, p, 0, B, Lq, 10, 2, 64, 0.1, p, p, 1, p, p, p, p,
                             256, _null()) == 1
     assert b"B * Lq too large" in L.jfa_last_error()
+
+
+def test_noalloc_rejects_oversized_problem_on_host(L):
+    # Refused before any CUDA call, so this runs without a device too.
+    dummy = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(dummy, ctypes.c_void_p)
+    code = L.jfa_bwd_noalloc(p, p, p, p, p, p, p, 0, 1, 40000, 4, 128, 0.1, p, p, 1, p, p, p,
+                             _null())
+    assert code == 3 and b"static buffer" in L.jfa_last_error()
+
+
+def test_noalloc_check_status_without_a_device(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    # No device: the address lookup fails cleanly, nothing crashes.
+    assert L.jfa_noalloc_check_status(_null()) == 4
+
+
+class _FakePlan(jfa.Plan):
+    def __init__(self, kind, B, T, H, D, Lq=0):  # no device work: only the fields validate() reads
+        self.kind, self.B, self.T, self.H, self.D, self.Lq = kind, B, T, H, D, Lq
+
+
+class _Off:
+    def __init__(self, n):
+        self.n = n
+
+    def numel(self):
+        return self.n
+
+
+def test_plan_validate_rejects_another_batch_layout():
+    plan = _FakePlan("jagged", 3, 100, 2, 128)
+    plan.validate("jagged", _Off(4), 100, 2, 128)
+    for args in ((_Off(5), 100, 2, 128), (_Off(4), 99, 2, 128), (_Off(4), 100, 4, 128),
+                 (_Off(4), 100, 2, 64)):
+        with pytest.raises(ValueError):
+            plan.validate("jagged", *args)
+    with pytest.raises(ValueError):
+        plan.validate("bcast", _Off(4), 100, 2, 128, 256)
+    bplan = _FakePlan("bcast", 3, 100, 2, 128, Lq=256)
+    bplan.validate("bcast", _Off(4), 100, 2, 128, 256)
+    with pytest.raises(ValueError):
+        bplan.validate("bcast", _Off(4), 100, 2, 128, 255)
+
+
+def test_host_offsets_checks():
+    jfa.check_host_offsets(np.array([0, 3, 3, 9], dtype=np.int64), 4)
+    jfa.check_host_offsets(np.array([0], dtype=np.int32), 1)
+    for bad, n in ((np.array([0, 3, 2]), 3), (np.array([1, 3]), 2), (np.array([0, 3]), 3),
+                   (np.array([[0, 3]]), 2), (np.array([0.0, 3.0]), 2)):
+        with pytest.raises(ValueError):
+            jfa.check_host_offsets(bad, n)

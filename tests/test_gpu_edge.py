@@ -3,6 +3,7 @@ and after non-empty ones (forward and backward against the fp64 oracle),
 and a batch whose sequences are all empty (nothing to compute: empty
 outputs, no error)."""
 
+import ctypes
 import math
 
 import numpy as np
@@ -158,3 +159,69 @@ def test_pipelined_steps_sharing_a_workspace_match_single_calls():
         assert torch.equal(got[0], ref[0].cpu()), "O differs at step %d" % n
         assert torch.equal(got[2], ref[2].cpu()) and torch.equal(got[3], ref[3].cpu()), n
         assert_close(got[1], ref[1], "dQ step %d" % n, atol=1e-2, rl2=1e-3)
+
+
+def _raw_fwd_bwd(q, k, v, do, off_dev, idx, B, T, H, D, plan, o, lse, dq, dk, dv):
+    """jfa_fwd then jfa_bwd through the C ABI with explicit sizes and the given
+    plan's tile lists (bypassing the binding's plan validation)."""
+    L, P, s = jfa.lib(), jfa._ptr, ctypes.c_float(D ** -0.5)
+    ws = plan.workspace
+    fsp, ftl = plan.fwd_sched
+    bsp, btl = plan.bwd_sched
+    assert L.jfa_fwd(P(q), P(k), P(v), P(off_dev), idx, B, T, H, D, s, P(fsp), P(ftl), plan.n_sms,
+                     P(o), P(lse), P(ws), ws.numel(), jfa._stream()) == 0, L.jfa_last_error()
+    assert L.jfa_bwd(P(q), P(k), P(v), P(o), P(lse), P(do), P(off_dev), idx, B, T, H, D, s, P(bsp),
+                     P(btl), plan.n_sms, P(dq), P(dk), P(dv), P(ws), ws.numel(),
+                     jfa._stream()) == 0, L.jfa_last_error()
+    plan.check()
+
+
+def test_mismatched_schedule_or_offsets_never_write_past_the_tensors():
+    # The kernels skip tiles naming a sequence or head outside the call and
+    # clamp every sequence to [0, T]. Outputs are views at the start of larger
+    # buffers whose tails hold a sentinel: nothing may change it. Every access
+    # stays inside allocated memory even if a guard were missing (the buffers
+    # are as large as the larger batch), so no case here can fault.
+    H, D = 2, 128
+    big, small = [300, 129, 700, 64], [70, 200]
+    Tb, Ts = sum(big), sum(small)
+    off_big = torch.from_numpy(W.offsets_of(big)).cuda()
+    off_small = torch.from_numpy(W.offsets_of(small)).cuda()
+    plan_big = jfa.Plan(off_big, H, D)
+    inp = W.jagged_inputs(small, H, D, 81, device="cuda")
+    sentinel = 7.0
+
+    def buffers():
+        o = torch.full((Tb, H, D), sentinel, dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((H * Tb,), sentinel, dtype=torch.float32, device="cuda")
+        g = [torch.full((Tb, H, D), sentinel, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        return o, lse, g
+
+    def untouched(o, lse, g):
+        assert bool((o[Ts:] == sentinel).all()) and bool((lse[H * Ts:] == sentinel).all())
+        for t in g:
+            assert bool((t[Ts:] == sentinel).all())
+
+    # (a) tile lists of a larger batch with the call's own offsets: tiles of
+    # sequences 2 and 3 are skipped, and the ones the small batch needs are in
+    # the list, so the results are also right.
+    o, lse, g = buffers()
+    _raw_fwd_bwd(inp["q"], inp["k"], inp["v"], inp["do"], off_small, jfa.JFA_I64, 2, Ts, H, D,
+                 plan_big, o, lse, *g)
+    untouched(o, lse, g)
+    s = 1 / math.sqrt(D)
+    q, k, v, do = (f64(inp[n]) for n in ("q", "k", "v", "do"))
+    offs = W.offsets_of(small)
+    ref_o, ref_lse = A.jagged_fwd(q, k, v, offs, s)
+    assert_close(o[:Ts], ref_o, "O", bf16_out=True)
+    assert_lse(lse[:H * Ts].view(H, Ts), ref_lse)
+    for name, got, r in zip(("dQ", "dK", "dV"), g, A.jagged_bwd(q, k, v, do, offs, s)):
+        assert_close(got[:Ts], r, name, bf16_out=True)
+
+    # (b) device offsets of the larger batch (ending past T) with the small
+    # tensors: sequences are clamped to T, values are unspecified, but no row
+    # at or past T is written and no kernel gives up.
+    o, lse, g = buffers()
+    _raw_fwd_bwd(inp["q"], inp["k"], inp["v"], inp["do"], off_big, jfa.JFA_I64, 4, Ts, H, D,
+                 plan_big, o, lse, *g)
+    untouched(o, lse, g)

@@ -53,6 +53,9 @@ def test_noalloc_matches_jfa_bwd_twice():
         got = _noalloc(inp, o, lse, off, plan, H, D)
         for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
             assert_close(g, r, name + " (no-alloc vs jfa_bwd)")
+    # No kernel of either call gave up waiting: the static status block says so.
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert jfa.lib().jfa_noalloc_check_status(stream) == 0, jfa.lib().jfa_last_error().decode()
 
 
 def test_noalloc_rejects_oversized_problem():
