@@ -37,6 +37,24 @@ per sequence and per head, with no blocking, fusion or online rescaling:
   64-token blocks and each query block attends only to its own key/value
   block, i.e. the definition above applied to every block independently.
 
+* masked and cross (varlen) attention ([JFA-GEM] "Impacto en el desarrollo
+  de modelos generativos": causal, sliding-window and block-sparse masks as
+  the natural extensions of the jagged kernels; "Optimización del proceso de
+  Backward y dQ": the peeled, masked last K/V block). The pages give no
+  formula; the plain reading used here is the usual band mask. Query i of a
+  sequence sees key j iff
+
+      (left < 0  or  j >= i + shift - left)  and
+      (right < 0 or  j <= i + shift + right),   shift = Lk - Lq,
+
+  i.e. a window of `left` keys before and `right` keys after the key aligned
+  with the query (bottom-right alignment, so a causal mask, left = -1 and
+  right = 0, lets the last query see every key when Lq != Lk). Masked scores
+  are -inf before the softmax; a query that sees no key gets O = 0 and
+  LSE = -inf and contributes nothing to the gradients. Cross attention takes
+  separate query and key/value offsets: sequence b pairs query rows
+  q_offsets[b]:q_offsets[b+1] with key rows kv_offsets[b]:kv_offsets[b+1].
+
 Inputs are NumPy arrays. Callers pass the bf16 values already widened to
 float64 (exactly); all arithmetic here is float64. Query rows are processed
 in chunks only to bound memory: every row's softmax is still taken over all
@@ -71,12 +89,41 @@ def softmax_rows(S):
     return e / l, (m + np.log(l))[:, 0]
 
 
-def seq_fwd(Q, K, V, scale):
+def band_visible(rows, Lq, Lk, window):
+    """Boolean [len(rows), Lk]: which keys each query row of `rows` sees under
+    the band mask `window` = (left, right) (see the module docstring; -1 is
+    unbounded, (-1, -1) sees every key)."""
+    left, right = window
+    i = np.asarray(rows, dtype=np.int64)[:, None] + (Lk - Lq)
+    j = np.arange(Lk, dtype=np.int64)[None, :]
+    ok = np.ones((i.shape[0], Lk), dtype=bool)
+    if left >= 0:
+        ok &= j >= i - left
+    if right >= 0:
+        ok &= j <= i + right
+    return ok
+
+
+def masked_softmax_rows(S, ok):
+    """Row softmax of S over the entries where `ok` holds; P is 0 elsewhere.
+    Rows with no such entry get P = 0 and LSE = -inf."""
+    S = np.where(ok, S, -np.inf)
+    any_ = ok.any(axis=1)
+    m = np.where(any_, S.max(axis=1), 0.0)[:, None]
+    e = np.where(ok, np.exp(S - m), 0.0)
+    l = e.sum(axis=1, keepdims=True)
+    P = np.where(any_[:, None], e / np.where(l > 0, l, 1.0), 0.0)
+    lse = np.where(any_, (m + np.log(np.where(l > 0, l, 1.0)))[:, 0], -np.inf)
+    return P, lse
+
+
+def seq_fwd(Q, K, V, scale, window=None):
     """Attention forward for one sequence and one head.
 
     Q [Lq, D], K [Lk, D], V [Lk, Dv] (fp64). Returns O [Lq, Dv] and
     LSE [Lq]. With Lk = 0 the output is 0 and the LSE is -inf (no keys:
     the empty sum), the reading used for broadcast-Q sequences of length 0.
+    `window` = (left, right) applies the band mask of the module docstring.
     """
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     Lq, Lk = Q.shape[0], K.shape[0]
@@ -87,16 +134,20 @@ def seq_fwd(Q, K, V, scale):
     for r0 in range(0, Lq, ROW_CHUNK):
         r1 = min(Lq, r0 + ROW_CHUNK)
         S = scale * (Q[r0:r1] @ K.T)
-        P, lse[r0:r1] = softmax_rows(S)
+        if window is None:
+            P, lse[r0:r1] = softmax_rows(S)
+        else:
+            P, lse[r0:r1] = masked_softmax_rows(S, band_visible(range(r0, r1), Lq, Lk, window))
         O[r0:r1] = P @ V
     return O, lse
 
 
-def seq_bwd(Q, K, V, dO, scale, O=None):
+def seq_bwd(Q, K, V, dO, scale, O=None, window=None):
     """Attention backward for one sequence and one head.
 
     Q [Lq, D], K [Lk, D], V [Lk, D], dO [Lq, D] (fp64). O is the oracle's
     own forward output (recomputed when not given). Returns dQ, dK, dV.
+    `window` = (left, right) applies the band mask of the module docstring.
     """
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
     Lq, Lk = Q.shape[0], K.shape[0]
@@ -106,11 +157,14 @@ def seq_bwd(Q, K, V, dO, scale, O=None):
     if Lq == 0 or Lk == 0:
         return dQ, dK, dV
     if O is None:
-        O, _ = seq_fwd(Q, K, V, scale)
+        O, _ = seq_fwd(Q, K, V, scale, window)
     for r0 in range(0, Lq, ROW_CHUNK):
         r1 = min(Lq, r0 + ROW_CHUNK)
         S = scale * (Q[r0:r1] @ K.T)
-        P, _ = softmax_rows(S)
+        if window is None:
+            P, _ = softmax_rows(S)
+        else:
+            P, _ = masked_softmax_rows(S, band_visible(range(r0, r1), Lq, Lk, window))
         dV += P.T @ dO[r0:r1]
         dP = dO[r0:r1] @ V.T
         Di = np.sum(dO[r0:r1] * O[r0:r1], axis=1, keepdims=True)
@@ -149,6 +203,33 @@ def jagged_bwd(q, k, v, do, offsets, scale):
         for h in range(H):
             dq[s:e, h], dk[s:e, h], dv[s:e, h] = seq_bwd(
                 q[s:e, h], k[s:e, h], v[s:e, h], do[s:e, h], scale)
+    return dq, dk, dv
+
+
+def varlen_fwd(q, k, v, q_offsets, kv_offsets, scale, window=(-1, -1)):
+    """Cross (or self) attention over packed sequences with separate query and
+    key/value offsets and an optional band mask. q [Tq, H, D]; k, v [Tk, H, D].
+    Returns O [Tq, H, D] and LSE [H, Tq] (fp64)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Tq, H, _ = q.shape
+    o = np.zeros((Tq, H, v.shape[2]))
+    lse = np.full((H, Tq), -np.inf)
+    for (qs, qe), (ks, ke) in zip(_bounds(q_offsets), _bounds(kv_offsets)):
+        for h in range(H):
+            o[qs:qe, h], lse[h, qs:qe] = seq_fwd(q[qs:qe, h], k[ks:ke, h], v[ks:ke, h], scale,
+                                                 tuple(window))
+    return o, lse
+
+
+def varlen_bwd(q, k, v, do, q_offsets, kv_offsets, scale, window=(-1, -1)):
+    """Backward of :func:`varlen_fwd`. Returns dQ [Tq, H, D], dK, dV [Tk, H, D]."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    H = q.shape[1]
+    for (qs, qe), (ks, ke) in zip(_bounds(q_offsets), _bounds(kv_offsets)):
+        for h in range(H):
+            dq[qs:qe, h], dk[ks:ke, h], dv[ks:ke, h] = seq_bwd(
+                q[qs:qe, h], k[ks:ke, h], v[ks:ke, h], do[qs:qe, h], scale, window=tuple(window))
     return dq, dk, dv
 
 

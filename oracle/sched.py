@@ -24,6 +24,21 @@ Readings where the pages are silent:
 
 Output is CSR: ``sm_ptr[S+1]`` and ``tiles`` as a list of (b, h, m), each
 SM's tiles in the order they were dealt.
+
+Masked and cross (varlen) attention (the band mask of ``oracle.attention``:
+query i sees key j iff j - i - (Lk - Lq) lies in [-left, right], -1 meaning
+unbounded) reuse the same sort and deal; only a tile's rows and work change:
+
+* forward tile (b, h, m) covers query rows [256 m, min(Lq, 256 m + 256)) and
+  its work is the length of the key range those rows can see,
+  [max(0, r0 + shift - left), min(Lk, r1 - 1 + shift + right + 1)), or 0 when
+  that range is empty (the tile still runs: its rows get O = 0);
+* backward tile (b, h, n) covers keys [128 n, min(Lk, 128 n + 128)) and its
+  work is the number of query rows that can see them,
+  [max(0, k0 - shift - right), min(Lq, k1 - 1 - shift + left + 1)), or 0
+  (the tile still runs: its keys get dK = dV = 0).
+
+Without a mask and with equal offsets this is the jagged schedule above.
 """
 
 
@@ -69,3 +84,72 @@ def makespan(sm_ptr, tiles, lengths, fixed_work=0):
             tot += fixed_work if fixed_work > 0 else lengths[b]
         best = max(best, tot)
     return best
+
+
+FWD_ROWS, BWD_ROWS = 256, 128
+
+
+def fwd_key_range(r0, r1, Lq, Lk, window):
+    """Keys [lo, hi) that query rows [r0, r1) can see under the band mask."""
+    left, right = window
+    shift = Lk - Lq
+    lo = 0 if left < 0 else max(0, r0 + shift - left)
+    hi = Lk if right < 0 else min(Lk, r1 - 1 + shift + right + 1)
+    return lo, max(lo, hi)
+
+
+def bwd_query_range(k0, k1, Lq, Lk, window):
+    """Query rows [lo, hi) that can see some key of [k0, k1) under the band mask."""
+    left, right = window
+    shift = Lk - Lq
+    lo = 0 if right < 0 else max(0, k0 - shift - right)
+    hi = Lq if left < 0 else min(Lq, k1 - 1 - shift + left + 1)
+    return lo, max(lo, hi)
+
+
+def enumerate_varlen_tiles(q_lengths, kv_lengths, H, op, window=(-1, -1)):
+    """Tiles (b, h, m, work) of the masked / cross attention forward
+    (op = "fwd") or backward (op = "bwd"), in enumeration order."""
+    out = []
+    for b, (Lq, Lk) in enumerate(zip(q_lengths, kv_lengths)):
+        if op == "fwd":
+            n_m = -(-Lq // FWD_ROWS)
+            works = []
+            for m in range(n_m):
+                r0, r1 = m * FWD_ROWS, min(Lq, m * FWD_ROWS + FWD_ROWS)
+                lo, hi = fwd_key_range(r0, r1, Lq, Lk, window)
+                works.append(hi - lo)
+        else:
+            n_m = -(-Lk // BWD_ROWS)
+            works = []
+            for n in range(n_m):
+                k0, k1 = n * BWD_ROWS, min(Lk, n * BWD_ROWS + BWD_ROWS)
+                lo, hi = bwd_query_range(k0, k1, Lq, Lk, window)
+                works.append(hi - lo)
+        for h in range(H):
+            for m in range(n_m):
+                out.append((b, h, m, works[m]))
+    return out
+
+
+def schedule_varlen(q_lengths, kv_lengths, H, op, num_sms, window=(-1, -1), zigzag=True):
+    """LPT + zigzag (or naive) deal of the varlen tiles. Returns (sm_ptr, tiles)."""
+    return _deal(enumerate_varlen_tiles(q_lengths, kv_lengths, H, op, window), num_sms, zigzag)
+
+
+def _deal(tiles, num_sms, zigzag):
+    if zigzag:
+        order = sorted(range(len(tiles)), key=lambda i: -tiles[i][3])  # stable
+    else:
+        order = list(range(len(tiles)))
+    per_sm = [[] for _ in range(num_sms)]
+    for i, t in enumerate(order):
+        p, j = divmod(i, num_sms)
+        sm = j if (not zigzag or p % 2 == 0) else num_sms - 1 - j
+        per_sm[sm].append(tiles[t][:3])
+    sm_ptr = [0]
+    flat = []
+    for lst in per_sm:
+        flat.extend(lst)
+        sm_ptr.append(len(flat))
+    return sm_ptr, flat

@@ -92,7 +92,7 @@ def _bwd_with(ds_rule=None, dq_rule=None, dk_rule=None, dv_rule=None):
     """A copy of the oracle's per-sequence backward with one step replaced;
     each rule gets every intermediate by name."""
 
-    def seq_bwd(Q, K, V, dO, scale, O=None):
+    def seq_bwd(Q, K, V, dO, scale, O=None, window=None):  # window: unused by these pins
         Q, K, V, dO = (np.asarray(x, dtype=np.float64) for x in (Q, K, V, dO))
         if O is None:
             O, _ = A.seq_fwd(Q, K, V, scale)
@@ -112,7 +112,7 @@ def _bwd_with(ds_rule=None, dq_rule=None, dk_rule=None, dv_rule=None):
 def _fwd_with(scores=None, softmax_axis=1):
     """A copy of the oracle's per-sequence forward with one step replaced."""
 
-    def seq_fwd(Q, K, V, scale):
+    def seq_fwd(Q, K, V, scale, window=None):  # window: unused by these pins
         Q, K, V = (np.asarray(x, dtype=np.float64) for x in (Q, K, V))
         S = scores(Q, K, scale) if scores else scale * (Q @ K.T)
         m = S.max(axis=softmax_axis, keepdims=True)
