@@ -280,6 +280,31 @@ def _setup(name, rank, dev, seqs=0, zigzag=True):
             jfa.jfa_bwd(inp["q"], inp["k"], inp["v"], st["o"], st["lse"], inp["do"], off, plan=st["plan"])
 
         st["check"] = lambda: st["plan"].check()
+    elif cfg["kind"] == "varlen":
+        L = _gem_lengths(rank) if cfg["lengths"] == "gem" else W.lengths_for(cfg["lengths"])
+        if seqs:
+            L = L[:seqs]
+        off_host = W.offsets_of(L, cfg["offsets_dtype"])
+        win, det = cfg["window"], cfg["deterministic"]
+        inp = W.jagged_inputs(L, H, D, W.SEEDS[cfg["lengths"]] + 1000 * rank, device=dev)
+        off = torch.from_numpy(off_host).to(dev)
+        ws_buf = jfa.Plan(off, H, D, kind="varlen", host_offsets=off_host, window=win,
+                          deterministic=det).workspace
+        st["fwd_flops"] = W.useful_flops("varlen", L, H=H, D=D, window=win)
+        st["desc"] = "%s: B=%d, T=%d, H=%d, D=%d, window %s, %s dQ" % (
+            name, len(L), int(off_host[-1]), H, D, tuple(win), "ordered" if det else "atomic")
+
+        def fwd():
+            st["plan"] = jfa.Plan(off, H, D, kind="varlen", host_offsets=off_host, window=win,
+                                  deterministic=det, workspace=ws_buf, zigzag=zigzag)
+            st["o"], st["lse"] = jfa.jfa_varlen_fwd(inp["q"], inp["k"], inp["v"], off, off,
+                                                    window=win, plan=st["plan"])
+
+        def bwd():
+            jfa.jfa_varlen_bwd(inp["q"], inp["k"], inp["v"], st["o"], st["lse"], inp["do"], off, off,
+                               window=win, deterministic=det, plan=st["plan"])
+
+        st["check"] = lambda: st["plan"].check()
     elif cfg["kind"] == "bcast":
         L = W.lengths_for(name)
         Lq = cfg["Lq"]
@@ -379,7 +404,7 @@ def _other_configs(args, dev, peaks):
     stream = torch.cuda.current_stream()
     steps, warmup = max(3, min(args.steps, 10)), 3
     out = {}
-    for name in ("stress", "bcast", "blockdiag", "blockdiag64"):
+    for name in ("stress", "bcast", "blockdiag", "blockdiag64", "gem_causal", "gem_det"):
         st = _setup(name, 0, dev)
         _, f_ms, b_ms, _ = _time_steps(st, steps, warmup, stream)
         ff, bf = st["fwd_flops"], st["bwd_flops"]
@@ -470,7 +495,7 @@ def run_ours(args):
             "pct_of_spec_peak": round(100 * value / SPEC_BF16_TFLOPS, 2),
             "roofline": roof,
             "clocks": clk,
-            "gpu_launches": (4 if st["kind"] == "jagged" else 2) * args.steps,
+            "gpu_launches": (4 if st["kind"] in ("jagged", "varlen") else 2) * args.steps,
         }
         if full_gem:
             line["targets"] = {
@@ -678,7 +703,8 @@ def main():
                     help="keep only the first N sequences (jagged) or N batch rows (block-diagonal): "
                          "a small profiling case")
     ap.add_argument("--config", default="gem",
-                    choices=["gem", "stress", "bcast", "blockdiag", "blockdiag64", "tiny"])
+                    choices=["gem", "stress", "bcast", "blockdiag", "blockdiag64", "tiny",
+                             "gem_causal", "gem_det"])
     ap.add_argument("--schedule", default="zigzag", choices=["zigzag", "naive"],
                     help="tile order: host LPT + zigzag deal, or the unsorted round-robin deal")
     ap.add_argument("--no-configs", action="store_true",

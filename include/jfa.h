@@ -108,6 +108,24 @@ jfa_status jfa_sched_build(int64_t B, int H, int tile_rows, int num_sms,
                            const void *host_offsets, jfa_index_t idx, int64_t fixed_rows,
                            int64_t fixed_work, int zigzag, int32_t *sm_ptr, int32_t *tiles);
 
+/* Scheduler for jfa_varlen_fwd / jfa_varlen_bwd (op = JFA_OP_FWD or
+ * JFA_OP_BWD): separate query and key/value offsets (host arrays of B+1
+ * entries; host_q_offsets NULL means the same as host_kv_offsets) and the
+ * band mask (window_left, window_right) of jfa_varlen_fwd. Forward tiles
+ * are 256 query rows of one (sequence, head); their work is the length of
+ * the key range those rows can see. Backward tiles are 128 keys; their work
+ * is the length of the query range that can see them. Tiles with no work
+ * are still emitted (their rows get O = 0, or their keys dK = dV = 0). Sort,
+ * tie order and deal are those of jfa_sched_build; without a window and with
+ * equal offsets the output equals jfa_sched_build's for the same op. */
+jfa_status jfa_sched_size_varlen(int64_t B, int H, jfa_op op, const void *host_q_offsets,
+                                 const void *host_kv_offsets, jfa_index_t idx, int64_t *n_tiles);
+
+jfa_status jfa_sched_build_varlen(int64_t B, int H, jfa_op op, int num_sms,
+                                  const void *host_q_offsets, const void *host_kv_offsets,
+                                  jfa_index_t idx, int window_left, int window_right, int zigzag,
+                                  int32_t *sm_ptr, int32_t *tiles);
+
 /* Rows per tile that the kernels of `op` expect from the scheduler. */
 jfa_status jfa_tile_rows(jfa_op op, int D, int *tile_rows);
 
@@ -184,6 +202,67 @@ jfa_status jfa_bwd(const void *q, const void *k, const void *v, const void *o,
                    int64_t B, int64_t T, int H, int D, float scale, const int32_t *d_sm_ptr,
                    const int32_t *d_tiles, int num_sms, void *dq, void *dk, void *dv,
                    void *workspace, size_t ws_bytes, jfa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Masked and cross (varlen) attention.
+ *
+ * "Desarrollo de Jagged Flash Attention para el modelo GEM", section
+ * "Impacto en el desarrollo de modelos generativos": causal, sliding-window
+ * and block-sparse masks as the extensions of the jagged kernels, built on
+ * the masked last K/V block of "Optimización del proceso de Backward y dQ".
+ * The pages give no formula; the band mask used is the usual one. In
+ * sequence b (Lq = query rows, Lk = keys, shift = Lk - Lq) query i sees key
+ * j iff
+ *   (window_left  < 0 || j >= i + shift - window_left) &&
+ *   (window_right < 0 || j <= i + shift + window_right),
+ * so (-1, -1) is no mask, (-1, 0) causal, (w - 1, 0) a causal window of w
+ * keys, with the diagonal aligned to the last query and the last key
+ * (bottom-right). A query that sees no key gets O = 0, LSE = -inf and
+ * contributes no gradient; keys that no query sees get dK = dV = 0.
+ *
+ * Queries and keys have separate offsets (jagged cross attention; pass the
+ * same array twice for self-attention): q, o, dout, dq are [Tq, H, D] bf16
+ * with q_offsets [B+1], k, v, dk, dv are [Tk, H, D] bf16 with kv_offsets
+ * [B+1], LSE is fp32 [H, Tq]. Tiles: jfa_sched_build_varlen with the same
+ * offsets and window.
+ * ---------------------------------------------------------------------- */
+jfa_status jfa_varlen_fwd(const void *q, const void *k, const void *v, const void *q_offsets,
+                          const void *kv_offsets, jfa_index_t idx, int64_t B, int64_t Tq,
+                          int64_t Tk, int H, int D, float scale, int window_left,
+                          int window_right, const int32_t *d_sm_ptr, const int32_t *d_tiles,
+                          int num_sms, void *o, float *lse, void *workspace, size_t ws_bytes,
+                          jfa_stream_t stream);
+
+/* Backward of jfa_varlen_fwd. deterministic = 0: dQ is summed in an fp32
+ * accumulator by TMA reduce-adds from every key block, so the order of the
+ * additions, and the last bits of dQ, can change from run to run (as in
+ * jfa_bwd). deterministic = 1: every key block stores its own fp32 partial
+ * of each query block it walks, and a closing pass sums a query block's
+ * partials in key-block order, so dQ is bit-identical across runs (reading
+ * of "Optimización del proceso de Backward y dQ": per-block fp32 partials and
+ * an ordered final sum); it needs a larger workspace and one more pass over
+ * the partials. workspace >= jfa_varlen_workspace_size(...) for the same
+ * offsets and mode; a workspace too small for the device offsets is reported
+ * by jfa_check_status as JFA_ERR_WORKSPACE (dQ is then wrong, and nothing is
+ * written outside the workspace and the outputs). */
+jfa_status jfa_varlen_bwd(const void *q, const void *k, const void *v, const void *o,
+                          const float *lse, const void *dout, const void *q_offsets,
+                          const void *kv_offsets, jfa_index_t idx, int64_t B, int64_t Tq,
+                          int64_t Tk, int H, int D, float scale, int window_left,
+                          int window_right, int deterministic, const int32_t *d_sm_ptr,
+                          const int32_t *d_tiles, int num_sms, void *dq, void *dk, void *dv,
+                          void *workspace, size_t ws_bytes, jfa_stream_t stream);
+
+/* Workspace bytes of jfa_varlen_bwd (and enough for jfa_varlen_fwd) from
+ * host copies of the offsets (host_q_offsets NULL = host_kv_offsets):
+ * non-deterministic, the 256-byte status block and an fp32 [Tq, H, D] dQ
+ * accumulator; deterministic, the status block, two [B+1] int64 tables and
+ * sum over b of ceil(Lk_b / 128) * round_up(Lq_b, 64) fp32 partial rows of
+ * H * D. The forward clears the accumulator when given a non-deterministic
+ * workspace of this size, as jfa_fwd does. */
+jfa_status jfa_varlen_workspace_size(int64_t B, const void *host_q_offsets,
+                                     const void *host_kv_offsets, jfa_index_t idx, int H, int D,
+                                     int deterministic, size_t *bytes);
 
 /* jfa_bwd without a workspace argument. The paper has no counterpart: this
  * entry point exists for callers that cannot allocate device memory when

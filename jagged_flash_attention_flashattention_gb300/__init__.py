@@ -13,6 +13,9 @@ Functions mirror the C entry points:
   ``[T, H, D]`` bf16 tensors and an offsets tensor ``[B+1]``;
 * :func:`jfa_bcastq_fwd`, :func:`jfa_bcastq_bwd` -- one dense Q
   ``[Lq, H, D]`` shared by every jagged K/V sequence;
+* :func:`jfa_varlen_fwd`, :func:`jfa_varlen_bwd` -- separate query and
+  key/value offsets (jagged cross attention), an optional band mask
+  (causal, sliding window) and an optional deterministic dQ reduction;
 * :func:`blockdiag_fwd`, :func:`blockdiag_bwd` -- 64-token block-diagonal
   attention on ``[B, L, H, D]``;
 * :func:`schedule` -- the host LPT + zigzag tile scheduler.
@@ -41,6 +44,8 @@ EXPORTS = [
     "jfa_num_sms", "jfa_workspace_size", "jfa_workspace_init", "jfa_check_status", "jfa_fwd",
     "jfa_bwd", "jfa_bcastq_fwd", "jfa_bcastq_bwd", "blockdiag_fwd", "blockdiag_bwd",
     "jfa_bwd_noalloc", "jfa_noalloc_check_status", "jfa_selftest_wait_timeout",
+    "jfa_sched_size_varlen", "jfa_sched_build_varlen", "jfa_varlen_fwd", "jfa_varlen_bwd",
+    "jfa_varlen_workspace_size",
 ]
 
 
@@ -82,6 +87,13 @@ def lib():
         "blockdiag_bwd": ([P, P, P, P, I64, I64, I, I, F, P, P, P, P, SZ, P], I),
         "jfa_bwd_noalloc": ([P, P, P, P, P, P, P, I, I64, I64, I, I, F, P, P, I, P, P, P, P], I),
         "jfa_noalloc_check_status": ([P], I),
+        "jfa_sched_size_varlen": ([I64, I, I, P, P, I, P], I),
+        "jfa_sched_build_varlen": ([I64, I, I, I, P, P, I, I, I, I, P, P], I),
+        "jfa_varlen_fwd": ([P, P, P, P, P, I, I64, I64, I64, I, I, F, I, I, P, P, I, P, P, P, SZ,
+                            P], I),
+        "jfa_varlen_bwd": ([P, P, P, P, P, P, P, P, I, I64, I64, I64, I, I, F, I, I, I, P, P, I, P,
+                            P, P, P, SZ, P], I),
+        "jfa_varlen_workspace_size": ([I64, P, P, I, I, I, I, P], I),
         "jfa_selftest_wait_timeout": ([P, SZ, ctypes.c_uint64, P], I),
     }
     for name, (args, res) in sig.items():
@@ -156,20 +168,44 @@ def check_host_offsets(host, n):
         raise ValueError("offsets must start at 0 and be non-decreasing")
 
 
+def schedule_varlen(q_offsets_host, kv_offsets_host, H, op, n_sms, window=(-1, -1), zigzag=True):
+    """Host LPT + zigzag schedule of the masked / cross attention tiles
+    (op = OP_FWD or OP_BWD). Returns (sm_ptr, tiles) int32 numpy."""
+    qo = np.ascontiguousarray(q_offsets_host)
+    ko = np.ascontiguousarray(kv_offsets_host)
+    if qo.dtype != ko.dtype or ko.dtype not in (np.int32, np.int64):
+        raise ValueError("offsets must both be int32 or both int64")
+    idx = JFA_I64 if ko.dtype == np.int64 else JFA_I32
+    B = ko.size - 1
+    n = ctypes.c_int64(0)
+    L = lib()
+    _check(L.jfa_sched_size_varlen(B, H, op, qo.ctypes.data, ko.ctypes.data, idx, ctypes.byref(n)))
+    sm_ptr = np.zeros(n_sms + 1, dtype=np.int32)
+    tiles = np.zeros((max(n.value, 1), 3), dtype=np.int32)
+    _check(L.jfa_sched_build_varlen(B, H, op, n_sms, qo.ctypes.data, ko.ctypes.data, idx,
+                                    int(window[0]), int(window[1]), 1 if zigzag else 0,
+                                    sm_ptr.ctypes.data, tiles.ctypes.data))
+    return sm_ptr, tiles[: n.value]
+
+
 class Plan:
     """Schedules (on the device) and workspace for one batch layout.
 
-    kind: "jagged" (offsets of the packed Q/K/V) or "bcast" (offsets of the
-    packed K/V, dense Q of length Lq). The scheduler runs on the host, so it
-    reads host offsets: pass them as `host_offsets` (numpy) when the caller
-    already has them, otherwise they are copied from `offsets` once. Tile
-    lists are copied to the device asynchronously from pinned memory.
-    `workspace` (uint8 CUDA tensor) may be shared between plans; it is
-    allocated when absent or too small.
+    kind: "jagged" (offsets of the packed Q/K/V), "bcast" (offsets of the
+    packed K/V, dense Q of length Lq) or "varlen" (`offsets` of the packed
+    K/V and `q_offsets` of the packed queries, which may be the same tensor;
+    band mask `window` = (left, right), -1 unbounded; `deterministic` sizes
+    the workspace for the ordered dQ reduction). The scheduler runs on the
+    host, so it reads host offsets: pass them as `host_offsets` /
+    `host_q_offsets` (numpy) when the caller already has them, otherwise they
+    are copied from the device once. Tile lists are copied to the device
+    asynchronously from pinned memory. `workspace` (uint8 CUDA tensor) may be
+    shared between plans; it is allocated when absent or too small.
     """
 
     def __init__(self, offsets, H, D, kind="jagged", Lq=0, zigzag=True, host_offsets=None,
-                 workspace=None):
+                 workspace=None, q_offsets=None, host_q_offsets=None, window=(-1, -1),
+                 deterministic=False):
         if not offsets.is_cuda:
             raise ValueError("offsets must be a CUDA tensor")
         self.offsets = offsets
@@ -180,9 +216,29 @@ class Plan:
         self.B = host.size - 1
         self.T = int(host[-1])
         self.H, self.D, self.kind, self.Lq = H, D, kind, int(Lq)
+        self.window = (int(window[0]), int(window[1]))
+        self.deterministic = bool(deterministic)
         self.n_sms = num_sms()
         dev = offsets.device
-        if kind == "jagged":
+        if kind == "varlen":
+            self.q_offsets = offsets if q_offsets is None else q_offsets
+            if self.q_offsets.dtype != offsets.dtype:
+                raise ValueError("q_offsets and offsets must have the same dtype")
+            if host_q_offsets is not None:
+                hq = np.asarray(host_q_offsets)
+            elif q_offsets is None:
+                hq = host
+            else:
+                hq = self.q_offsets.cpu().numpy()
+            check_host_offsets(hq, self.q_offsets.numel())
+            self.host_q_offsets = hq
+            self.Tq = int(hq[-1])
+        if kind == "varlen":
+            fwd = schedule_varlen(self.host_q_offsets, host, H, OP_FWD, self.n_sms, self.window,
+                                  zigzag)
+            bwd = schedule_varlen(self.host_q_offsets, host, H, OP_BWD, self.n_sms, self.window,
+                                  zigzag)
+        elif kind == "jagged":
             fwd = schedule(host, H, tile_rows(OP_FWD, D), self.n_sms, zigzag=zigzag)
             bwd = schedule(host, H, tile_rows(OP_BWD, D), self.n_sms, zigzag=zigzag)
         else:
@@ -194,9 +250,18 @@ class Plan:
         d = [t.to(dev, non_blocking=True) for t in self._pinned]
         self.fwd_sched, self.bwd_sched = (d[0], d[1]), (d[2], d[3])
         self.n_fwd_tiles, self.n_bwd_tiles = fwd[1].shape[0], bwd[1].shape[0]
-        rows = self.T if kind == "jagged" else self.Lq
-        op = OP_BWD if kind == "jagged" else OP_BCASTQ_BWD
-        nbytes = lib().jfa_workspace_size(op, rows, H, D)
+        if kind == "varlen":
+            sz = ctypes.c_size_t(0)
+            hq = np.ascontiguousarray(self.host_q_offsets)
+            hk = np.ascontiguousarray(host)
+            _check(lib().jfa_varlen_workspace_size(self.B, hq.ctypes.data, hk.ctypes.data, self.idx,
+                                                   H, D, 1 if self.deterministic else 0,
+                                                   ctypes.byref(sz)))
+            nbytes = sz.value
+        else:
+            rows = self.T if kind == "jagged" else self.Lq
+            op = OP_BWD if kind == "jagged" else OP_BCASTQ_BWD
+            nbytes = lib().jfa_workspace_size(op, rows, H, D)
         if workspace is None or workspace.numel() < nbytes:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
             _check(lib().jfa_workspace_init(_ptr(workspace), nbytes, _stream()))
@@ -217,6 +282,18 @@ class Plan:
         have = (self.kind, self.B, self.T, self.H, self.D, self.Lq)
         if want != have:
             raise ValueError("plan built for (kind, B, T, H, D, Lq) = %s, call has %s" % (have, want))
+
+
+def _check_varlen_plan(plan, q_offsets, kv_offsets, Tq, Tk, H, D, window):
+    if plan.kind != "varlen":
+        raise ValueError("a varlen call needs a plan of kind 'varlen'")
+    if (plan.B, plan.T, plan.Tq, plan.H, plan.D) != (kv_offsets.numel() - 1, Tk, Tq, H, D):
+        raise ValueError("plan built for (B, Tk, Tq, H, D) = %s, call has %s" % (
+            (plan.B, plan.T, plan.Tq, plan.H, plan.D), (kv_offsets.numel() - 1, Tk, Tq, H, D)))
+    if q_offsets.numel() != kv_offsets.numel():
+        raise ValueError("q_offsets and kv_offsets must have the same length")
+    if tuple(window) != plan.window:
+        raise ValueError("plan built for window %s, call has %s" % (plan.window, tuple(window)))
 
 
 def _scale(scale, D):
@@ -251,6 +328,52 @@ def jfa_bwd(q, k, v, o, lse, do, offsets, scale=None, plan=None):
                          plan.idx, plan.B, T, H, D, _scale(scale, D), _ptr(sp), _ptr(tl),
                          plan.n_sms, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(plan.workspace),
                          plan.workspace.numel(), _stream()))
+    return dq, dk, dv
+
+
+def jfa_varlen_fwd(q, k, v, q_offsets, kv_offsets, scale=None, window=(-1, -1), plan=None):
+    """Masked / cross attention forward. q [Tq, H, D], k, v [Tk, H, D] bf16 CUDA;
+    q_offsets, kv_offsets [B+1] (same dtype; the same tensor twice for
+    self-attention); window = (left, right) band mask, (-1, -1) none, (-1, 0)
+    causal. Returns (o [Tq, H, D] bf16, lse [H, Tq] fp32)."""
+    _need_cuda(q, k, v)
+    Tq, H, D = q.shape
+    Tk = k.shape[0]
+    plan = plan or Plan(kv_offsets, H, D, kind="varlen", q_offsets=q_offsets, window=window)
+    _check_varlen_plan(plan, q_offsets, kv_offsets, Tq, Tk, H, D, window)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device)
+    sp, tl = plan.fwd_sched
+    # a deterministic plan's workspace holds no accumulator for the forward to clear
+    ws_bytes = 256 if plan.deterministic else plan.workspace.numel()
+    _check(lib().jfa_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(q_offsets), _ptr(kv_offsets),
+                                plan.idx, plan.B, Tq, Tk, H, D, _scale(scale, D), int(window[0]),
+                                int(window[1]), _ptr(sp), _ptr(tl), plan.n_sms, _ptr(o), _ptr(lse),
+                                _ptr(plan.workspace), ws_bytes, _stream()))
+    return o, lse
+
+
+def jfa_varlen_bwd(q, k, v, o, lse, do, q_offsets, kv_offsets, scale=None, window=(-1, -1),
+                   deterministic=False, plan=None):
+    """Backward of :func:`jfa_varlen_fwd`. With deterministic=True the dQ
+    reduction runs in a fixed order (bit-identical dQ from run to run); the
+    plan must then be built with deterministic=True. Returns (dq, dk, dv) bf16."""
+    _need_cuda(q, k, v, o, do)
+    Tq, H, D = q.shape
+    Tk = k.shape[0]
+    plan = plan or Plan(kv_offsets, H, D, kind="varlen", q_offsets=q_offsets, window=window,
+                        deterministic=deterministic)
+    _check_varlen_plan(plan, q_offsets, kv_offsets, Tq, Tk, H, D, window)
+    if deterministic and not plan.deterministic:
+        raise ValueError("deterministic=True needs a plan built with deterministic=True")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    sp, tl = plan.bwd_sched
+    _check(lib().jfa_varlen_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                _ptr(q_offsets), _ptr(kv_offsets), plan.idx, plan.B, Tq, Tk, H, D,
+                                _scale(scale, D), int(window[0]), int(window[1]),
+                                1 if deterministic else 0, _ptr(sp), _ptr(tl), plan.n_sms,
+                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(plan.workspace),
+                                plan.workspace.numel(), _stream()))
     return dq, dk, dv
 
 

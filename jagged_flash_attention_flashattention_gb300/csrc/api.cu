@@ -162,7 +162,13 @@ jfa_status jfa::read_status_block(void *status, void *stream_) {
     // only makes the next backward clear its accumulator itself.
     cudaMemsetAsync(status, 0, kStatusBytes, stream);
     cudaStreamSynchronize(stream);
-    return fail(JFA_ERR_TIMEOUT, "kernel wait site %u in block %u gave up", st[1], st[2]);
+    if (st[0] == JFA_ERR_TIMEOUT)
+      return fail(JFA_ERR_TIMEOUT, "kernel wait site %u in block %u gave up", st[1], st[2]);
+    if (st[0] == JFA_ERR_WORKSPACE)
+      return fail(JFA_ERR_WORKSPACE,
+                  "the deterministic dQ partials need more rows than the workspace holds "
+                  "(size it with jfa_varlen_workspace_size for the same offsets)");
+    return fail(JFA_ERR_CUDA, "a kernel reported device status %u", st[0]);
   }
   return JFA_OK;
 }
@@ -176,17 +182,29 @@ extern "C" jfa_status jfa_check_status(void *workspace, jfa_stream_t stream) {
 
 namespace {
 
-jfa_status fwd_common(const void *q, const void *k, const void *v, const void *offsets,
-                      jfa_index_t idx, int64_t B, int64_t q_rows, int64_t Tk, int64_t Lq, int H,
-                      int D, float scale, const int32_t *sm_ptr, const int32_t *tiles,
-                      int num_sms, void *o, float *lse, void *ws, size_t ws_bytes,
-                      cudaStream_t st) {
+jfa_status check_window(int left, int right) {
+  if (left < -1 || right < -1)
+    return fail(JFA_ERR_INVALID_ARG, "window (%d, %d): bounds must be >= -1", left, right);
+  return JFA_OK;
+}
+
+// Shared by every forward entry point. kv_offsets bound the K/V sequences;
+// q_offsets the query sequences (jagged, may equal kv_offsets), or NULL with
+// Lq > 0 for broadcast-Q (one dense Q of Lq rows); q_rows = rows of q.
+jfa_status fwd_common(const void *q, const void *k, const void *v, const void *kv_offsets,
+                      const void *q_offsets, jfa_index_t idx, int64_t B, int64_t q_rows,
+                      int64_t Tk, int64_t Lq, int H, int D, float scale, int win_left,
+                      int win_right, const int32_t *sm_ptr, const int32_t *tiles, int num_sms,
+                      void *o, float *lse, void *ws, size_t ws_bytes, cudaStream_t st) {
   JFA_TRY(check_dims(B, Tk, H, D));
+  JFA_TRY(check_dims(B, q_rows, H, D));
+  JFA_TRY(check_window(win_left, win_right));
   if (idx != JFA_I32 && idx != JFA_I64) return fail(JFA_ERR_INVALID_ARG, "bad index type");
   if (!(scale > 0.f)) return fail(JFA_ERR_INVALID_ARG, "scale must be > 0");
   JFA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
   if (num_sms < 1) return fail(JFA_ERR_INVALID_ARG, "num_sms = %d < 1", num_sms);
-  JFA_TRY(need_ptr(offsets, "offsets"));
+  JFA_TRY(need_ptr(kv_offsets, "kv_offsets"));
+  if (Lq == 0) JFA_TRY(need_ptr(q_offsets, "q_offsets"));
   if (B == 0 || q_rows == 0) return JFA_OK;
   JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
   JFA_TRY(need_ptr(q, "q"));
@@ -196,21 +214,25 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *o
     JFA_TRY(need_ptr(k, "k"));
     JFA_TRY(need_ptr(v, "v"));
   } else {
-    k = v = q;  // never read: every sequence is empty
+    k = v = q;  // never read: every K/V sequence is empty
   }
   FwdParams p;
   memset(&p, 0, sizeof(p));
   JFA_TRY(map_rows_bf16(&p.tm_q, q, q_rows, H, D, 128));
   JFA_TRY(map_rows_bf16(&p.tm_k, k, Tk > 0 ? Tk : q_rows, H, D, 128));
   JFA_TRY(map_rows_bf16(&p.tm_v, v, Tk > 0 ? Tk : q_rows, H, D, 128));
-  p.offsets = offsets;
+  p.offsets = kv_offsets;
+  p.q_offsets = Lq > 0 ? kv_offsets : q_offsets;
   p.idx64 = idx == JFA_I64;
   p.sm_ptr = sm_ptr;
   p.tiles = tiles;
   p.o = o;
   p.lse = lse;
   p.B = B;
-  p.T = Lq > 0 ? Tk : q_rows;
+  p.T = Tk;
+  p.Tq = q_rows;
+  p.win_left = win_left;
+  p.win_right = win_right;
   p.H = H;
   p.Lq = (int)Lq;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -233,8 +255,20 @@ extern "C" jfa_status jfa_fwd(const void *q, const void *k, const void *v, const
                               const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_sms,
                               void *o, float *lse, void *workspace, size_t ws_bytes,
                               jfa_stream_t stream) {
-  return fwd_common(q, k, v, offsets, idx, B, T, T, 0, H, D, scale, d_sm_ptr, d_tiles, num_sms,
-                    o, lse, workspace, ws_bytes, (cudaStream_t)stream);
+  return fwd_common(q, k, v, offsets, offsets, idx, B, T, T, 0, H, D, scale, -1, -1, d_sm_ptr,
+                    d_tiles, num_sms, o, lse, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" jfa_status jfa_varlen_fwd(const void *q, const void *k, const void *v,
+                                     const void *q_offsets, const void *kv_offsets,
+                                     jfa_index_t idx, int64_t B, int64_t Tq, int64_t Tk, int H,
+                                     int D, float scale, int window_left, int window_right,
+                                     const int32_t *d_sm_ptr, const int32_t *d_tiles,
+                                     int num_sms, void *o, float *lse, void *workspace,
+                                     size_t ws_bytes, jfa_stream_t stream) {
+  return fwd_common(q, k, v, kv_offsets, q_offsets, idx, B, Tq, Tk, 0, H, D, scale, window_left,
+                    window_right, d_sm_ptr, d_tiles, num_sms, o, lse, workspace, ws_bytes,
+                    (cudaStream_t)stream);
 }
 
 extern "C" jfa_status jfa_bcastq_fwd(const void *q, const void *k, const void *v,
@@ -247,8 +281,8 @@ extern "C" jfa_status jfa_bcastq_fwd(const void *q, const void *k, const void *v
   if (B > 0 && Lq >= ((int64_t(1) << 31) - 256) / B)  // O rows are addressed with 32-bit indices
     return fail(JFA_ERR_INVALID_ARG, "B * Lq too large");
   if (Lq == 0) return JFA_OK;
-  return fwd_common(q, k, v, kv_offsets, idx, B, Lq, Tk, Lq, H, D, scale, d_sm_ptr, d_tiles,
-                    num_sms, o, lse, workspace, ws_bytes, (cudaStream_t)stream);
+  return fwd_common(q, k, v, kv_offsets, nullptr, idx, B, Lq, Tk, Lq, H, D, scale, -1, -1,
+                    d_sm_ptr, d_tiles, num_sms, o, lse, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
 // ------------------------------------------------------------------ backward
@@ -260,29 +294,38 @@ jfa_status launch_status(cudaError_t e, const char *what) {
   return cuda_status(e, what);
 }
 
+// Bytes of the deterministic workspace header: the status block, then the
+// per-sequence partial-row and query-block prefix sums ([B+1] int64 each).
+size_t det_header_bytes(int64_t B) {
+  return kStatusBytes + round_up(2 * (size_t)(B + 1) * sizeof(int64_t), 256);
+}
+
+// Shared by every backward entry point (see fwd_common for the offsets).
 jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o,
-                      const float *lse, const void *dout, const void *offsets, jfa_index_t idx,
-                      int64_t B, int64_t q_rows, int64_t Tk, int64_t Lq, int H, int D,
-                      float scale, const int32_t *sm_ptr, const int32_t *tiles, int num_sms,
-                      void *dq, void *dk, void *dv, void *ws, size_t ws_bytes, cudaStream_t st) {
+                      const float *lse, const void *dout, const void *kv_offsets,
+                      const void *q_offsets, jfa_index_t idx, int64_t B, int64_t q_rows,
+                      int64_t Tk, int64_t Lq, int H, int D, float scale, int win_left,
+                      int win_right, int det, const int32_t *sm_ptr, const int32_t *tiles,
+                      int num_sms, void *dq, void *dk, void *dv, void *ws, size_t ws_bytes,
+                      cudaStream_t st) {
   JFA_TRY(check_dims(B, Tk, H, D));
+  JFA_TRY(check_dims(B, q_rows, H, D));
+  JFA_TRY(check_window(win_left, win_right));
   if (idx != JFA_I32 && idx != JFA_I64) return fail(JFA_ERR_INVALID_ARG, "bad index type");
   if (!(scale > 0.f)) return fail(JFA_ERR_INVALID_ARG, "scale must be > 0");
+  if (det && Lq > 0) return fail(JFA_ERR_UNSUPPORTED, "deterministic dQ is for the jagged layouts");
   const int64_t acc_rows = Lq > 0 ? Lq : q_rows;
-  // Jagged: fp32 accumulator in the workspace, cast to bf16 at the end.
+  // Jagged: fp32 accumulator in the workspace, cast to bf16 at the end (or,
+  // deterministic, per-key-block partials summed in order by the cast).
   // Broadcast-Q: the caller's fp32 dq is the accumulator itself.
   const size_t need =
-      kStatusBytes + (Lq > 0 ? 0 : round_up((size_t)acc_rows * H * D * sizeof(float), 256));
+      det ? det_header_bytes(B)
+          : kStatusBytes + (Lq > 0 ? 0 : round_up((size_t)acc_rows * H * D * sizeof(float), 256));
   JFA_TRY(check_ws(ws, ws_bytes, need));
   if (num_sms < 1) return fail(JFA_ERR_INVALID_ARG, "num_sms = %d < 1", num_sms);
-  JFA_TRY(need_ptr(offsets, "offsets"));
-  if (B == 0 || q_rows == 0) return JFA_OK;
-  JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
-  JFA_TRY(need_ptr(q, "q"));
-  JFA_TRY(need_ptr(o, "o"));
-  JFA_TRY(need_ptr(lse, "lse"));
-  JFA_TRY(need_ptr(dout, "dout"));
-  JFA_TRY(need_ptr(dq, "dq"));
+  JFA_TRY(need_ptr(kv_offsets, "kv_offsets"));
+  if (Lq == 0) JFA_TRY(need_ptr(q_offsets, "q_offsets"));
+  if (B == 0 || (q_rows == 0 && Tk == 0)) return JFA_OK;
   if (Tk > 0) {
     JFA_TRY(need_ptr(k, "k"));
     JFA_TRY(need_ptr(v, "v"));
@@ -291,8 +334,19 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   } else {
     k = v = q;
   }
-  float *acc = Lq > 0 ? static_cast<float *>(dq)
-                      : reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kStatusBytes);
+  if (q_rows == 0) {  // keys that no query sees: dK = dV = 0
+    const size_t kv_bytes = (size_t)Tk * H * D * 2;
+    JFA_TRY(cuda_status(cudaMemsetAsync(dk, 0, kv_bytes, st), "cudaMemsetAsync"));
+    return cuda_status(cudaMemsetAsync(dv, 0, kv_bytes, st), "cudaMemsetAsync");
+  }
+  JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
+  JFA_TRY(need_ptr(q, "q"));
+  JFA_TRY(need_ptr(o, "o"));
+  JFA_TRY(need_ptr(lse, "lse"));
+  JFA_TRY(need_ptr(dout, "dout"));
+  JFA_TRY(need_ptr(dq, "dq"));
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  float *acc = Lq > 0 ? static_cast<float *>(dq) : reinterpret_cast<float *>(wsb + kStatusBytes);
   BwdParams p;
   memset(&p, 0, sizeof(p));
   const int64_t o_rows = Lq > 0 ? B * Lq : q_rows;
@@ -300,8 +354,24 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   JFA_TRY(map_rows_bf16(&p.tm_do, dout, o_rows, H, D, 64));
   JFA_TRY(map_rows_bf16(&p.tm_k, k, Tk > 0 ? Tk : 1, H, D, 128));
   JFA_TRY(map_rows_bf16(&p.tm_v, v, Tk > 0 ? Tk : 1, H, D, 128));
-  JFA_TRY(map_acc_f32(&p.tm_dqacc, acc, acc_rows, H, D));
-  p.offsets = offsets;
+  float *part = nullptr;
+  int64_t *det_base = nullptr, *qb_base = nullptr;
+  if (det) {
+    det_base = reinterpret_cast<int64_t *>(wsb + kStatusBytes);
+    qb_base = det_base + (B + 1);
+    part = reinterpret_cast<float *>(wsb + det_header_bytes(B));
+    p.det = 1;
+    p.det_base = det_base;
+    // Partial rows are 32-bit TMA coordinates: at most 2^31 - 64 of them.
+    p.det_rows = (int64_t)((ws_bytes - det_header_bytes(B)) / ((size_t)H * D * sizeof(float)));
+    if (p.det_rows > (int64_t(1) << 31) - 64) p.det_rows = (int64_t(1) << 31) - 64;
+    JFA_TRY(map_acc_f32(&p.tm_dqpart, part, p.det_rows > 0 ? p.det_rows : 1, H, D));
+    JFA_TRY(map_acc_f32(&p.tm_dqacc, part, p.det_rows > 0 ? p.det_rows : 1, H, D));  // unused
+  } else {
+    JFA_TRY(map_acc_f32(&p.tm_dqacc, acc, acc_rows, H, D));
+  }
+  p.offsets = kv_offsets;
+  p.q_offsets = Lq > 0 ? kv_offsets : q_offsets;
   p.idx64 = idx == JFA_I64;
   p.sm_ptr = sm_ptr;
   p.tiles = tiles;
@@ -310,13 +380,21 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   p.dk = dk;
   p.dv = dv;
   p.B = B;
-  p.T = Lq > 0 ? Tk : q_rows;
+  p.T = Tk;
+  p.Tq = q_rows;
+  p.win_left = win_left;
+  p.win_right = win_right;
   p.H = H;
   p.Lq = (int)Lq;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = static_cast<uint32_t *>(ws);
   p.timeout_ns = kTimeoutNs;
+  if (det) {
+    JFA_TRY(launch_status(launch_det_layout(p, det_base, qb_base, st), "deterministic layout"));
+    if (Tk > 0) JFA_TRY(launch_status(launch_bwd(p, D, num_sms, st), "bwd launch"));
+    return launch_status(launch_det_cast(p, part, qb_base, dq, D, num_sms, st), "dq sum");
+  }
   const size_t acc_bytes = (size_t)acc_rows * H * D * sizeof(float);
   if (Lq > 0)
     JFA_TRY(cuda_status(cudaMemsetAsync(acc, 0, acc_bytes, st), "cudaMemsetAsync"));
@@ -336,8 +414,45 @@ extern "C" jfa_status jfa_bwd(const void *q, const void *k, const void *v, const
                               const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_sms,
                               void *dq, void *dk, void *dv, void *workspace, size_t ws_bytes,
                               jfa_stream_t stream) {
-  return bwd_common(q, k, v, o, lse, dout, offsets, idx, B, T, T, 0, H, D, scale, d_sm_ptr,
-                    d_tiles, num_sms, dq, dk, dv, workspace, ws_bytes, (cudaStream_t)stream);
+  return bwd_common(q, k, v, o, lse, dout, offsets, offsets, idx, B, T, T, 0, H, D, scale, -1, -1,
+                    0, d_sm_ptr, d_tiles, num_sms, dq, dk, dv, workspace, ws_bytes,
+                    (cudaStream_t)stream);
+}
+
+extern "C" jfa_status jfa_varlen_bwd(const void *q, const void *k, const void *v, const void *o,
+                                     const float *lse, const void *dout, const void *q_offsets,
+                                     const void *kv_offsets, jfa_index_t idx, int64_t B,
+                                     int64_t Tq, int64_t Tk, int H, int D, float scale,
+                                     int window_left, int window_right, int deterministic,
+                                     const int32_t *d_sm_ptr, const int32_t *d_tiles,
+                                     int num_sms, void *dq, void *dk, void *dv, void *workspace,
+                                     size_t ws_bytes, jfa_stream_t stream) {
+  return bwd_common(q, k, v, o, lse, dout, kv_offsets, q_offsets, idx, B, Tq, Tk, 0, H, D, scale,
+                    window_left, window_right, deterministic ? 1 : 0, d_sm_ptr, d_tiles, num_sms,
+                    dq, dk, dv, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" jfa_status jfa_varlen_workspace_size(int64_t B, const void *host_q_offsets,
+                                                const void *host_kv_offsets, jfa_index_t idx,
+                                                int H, int D, int deterministic, size_t *bytes) {
+  if (!bytes) return fail(JFA_ERR_INVALID_ARG, "bytes is NULL");
+  if (H < 1 || D < 1) return fail(JFA_ERR_INVALID_ARG, "bad H or D");
+  if (!host_q_offsets) host_q_offsets = host_kv_offsets;
+  JFA_TRY(check_host_offsets(host_kv_offsets, idx, B, -1));
+  JFA_TRY(check_host_offsets(host_q_offsets, idx, B, -1));
+  const int64_t Tq = offset_at(host_q_offsets, idx, B);
+  if (!deterministic) {
+    *bytes = kStatusBytes + round_up((size_t)Tq * H * D * sizeof(float), 256);
+    return JFA_OK;
+  }
+  size_t rows = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t Lq = offset_at(host_q_offsets, idx, b + 1) - offset_at(host_q_offsets, idx, b);
+    const int64_t Lk = offset_at(host_kv_offsets, idx, b + 1) - offset_at(host_kv_offsets, idx, b);
+    rows += (size_t)((Lk + 127) / 128) * (size_t)((Lq + 63) / 64 * 64);
+  }
+  *bytes = det_header_bytes(B) + rows * H * D * sizeof(float);
+  return JFA_OK;
 }
 
 extern "C" jfa_status jfa_bcastq_bwd(const void *q, const void *k, const void *v, const void *o,
@@ -351,8 +466,8 @@ extern "C" jfa_status jfa_bcastq_bwd(const void *q, const void *k, const void *v
   if (B > 0 && Lq >= ((int64_t(1) << 31) - 256) / B)  // O / dO rows use 32-bit indices
     return fail(JFA_ERR_INVALID_ARG, "B * Lq too large");
   if (Lq == 0) return JFA_OK;
-  return bwd_common(q, k, v, o, lse, dout, kv_offsets, idx, B, Lq, Tk, Lq, H, D, scale,
-                    d_sm_ptr, d_tiles, num_sms, dq, dk, dv, workspace, ws_bytes,
+  return bwd_common(q, k, v, o, lse, dout, kv_offsets, nullptr, idx, B, Lq, Tk, Lq, H, D, scale,
+                    -1, -1, 0, d_sm_ptr, d_tiles, num_sms, dq, dk, dv, workspace, ws_bytes,
                     (cudaStream_t)stream);
 }
 

@@ -53,6 +53,7 @@
 // dP/dS [320,384) dQ^T [384,512) (two buffers).
 #include <cuda_bf16.h>
 
+#include "band.h"
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -100,18 +101,23 @@ struct BwdBars {
 
 struct BwdTile {
   int b, h, nq, nkv;  // query blocks to walk; valid key rows in this tile
+  int qb0;            // first query block walked (blocks of 64 rows)
   int kv_row0;        // first key row (tm_k / tm_v / dK / dV)
+  int qdiag0;         // query index aligned with the tile's first key (band mask)
   int q_row0;         // first query row of the sequence in tm_q and in the dQ accumulator
   int o_row0;         // first row of the sequence in O / dO
   int Lq;             // query rows of the sequence
-  int64_t lse0;       // LSE index of query row 0 (jagged: + h*T; bcast: (b*H+h)*Lq)
+  int64_t lse0;       // LSE index of query row 0 (jagged: + h*Tq; bcast: (b*H+h)*Lq)
+  int prow0;          // deterministic dQ: partial row of query row 0 for this key block
 };
 
 __device__ __forceinline__ int64_t load_off(const void *off, int idx64, int i) {
   return idx64 ? static_cast<const int64_t *>(off)[i] : (int64_t) static_cast<const int *>(off)[i];
 }
 
-template <bool BCAST>
+// GEN: the band mask and the deterministic dQ store are compiled in
+// (jfa_varlen_bwd); without them every key sees all of its sequence's queries.
+template <bool BCAST, bool GEN>
 __device__ __forceinline__ BwdTile decode_tile(const BwdParams &p, int t) {
   BwdTile d;
   d.b = p.tiles[3 * t];
@@ -124,24 +130,36 @@ __device__ __forceinline__ BwdTile decode_tile(const BwdParams &p, int t) {
   const int64_t s0 = in ? min(max(load_off(p.offsets, p.idx64, d.b), (int64_t)0), p.T) : 0;
   const int64_t e0 = in ? min(max(load_off(p.offsets, p.idx64, d.b + 1), s0), p.T) : 0;
   const int L = (int)(e0 - s0);
-  d.Lq = BCAST ? (in ? p.Lq : 0) : L;
-  d.nq = (d.Lq + 63) / 64;
+  int64_t qs = 0;
+  if (BCAST) {
+    d.Lq = in ? p.Lq : 0;
+  } else {
+    qs = in ? min(max(load_off(p.q_offsets, p.idx64, d.b), (int64_t)0), p.Tq) : 0;
+    d.Lq = (int)(in ? min(max(load_off(p.q_offsets, p.idx64, d.b + 1), qs), p.Tq) - qs : 0);
+  }
   d.nkv = min(128, L - n * 128);
+  d.qdiag0 = n * 128 - (L - d.Lq);
+  d.qb0 = 0;
+  d.nq = 0;
+  if (d.nkv > 0)
+    bwd_query_blocks(n, d.Lq, L, GEN ? p.win_left : -1, GEN ? p.win_right : -1, &d.qb0, &d.nq);
   d.kv_row0 = (int)s0 + n * 128;
+  d.prow0 = 0;
   if (BCAST) {
     d.q_row0 = 0;
     d.o_row0 = d.b * p.Lq;
     d.lse0 = ((int64_t)d.b * p.H + d.h) * p.Lq;
   } else {
-    d.q_row0 = (int)s0;
-    d.o_row0 = (int)s0;
-    d.lse0 = (int64_t)d.h * p.T + s0;
+    d.q_row0 = (int)qs;
+    d.o_row0 = (int)qs;
+    d.lse0 = (int64_t)d.h * p.Tq + qs;
+    if (GEN && p.det && d.nq > 0) d.prow0 = (int)(p.det_base[d.b] + (int64_t)n * ((d.Lq + 63) / 64 * 64));
   }
   return d;
 }
 
 // Walks the (tile, query block) sequence of one CTA, skipping empty tiles.
-template <bool BCAST>
+template <bool BCAST, bool GEN>
 struct BlockIter {
   int t, tend, i;
   bool valid;
@@ -149,7 +167,7 @@ struct BlockIter {
   __device__ __forceinline__ void seek(const BwdParams &p) {
     valid = false;
     for (; t < tend; ++t) {
-      tl = decode_tile<BCAST>(p, t);
+      tl = decode_tile<BCAST, GEN>(p, t);
       if (tl.nq > 0 && tl.nkv > 0) {
         valid = true;
         return;
@@ -165,7 +183,7 @@ struct BlockIter {
   }
 };
 
-template <int D, bool BCAST>
+template <int D, bool BCAST, bool GEN>
 __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -233,10 +251,10 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       // The next tile is decoded one tile ahead (its index loads are off the
       // critical path at the tile switch).
       BwdTile nxt{};
-      if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
+      if (tbeg < tend) nxt = decode_tile<BCAST, GEN>(p, tbeg);
       for (int t = tbeg; t < tend; ++t) {
         const BwdTile tl = nxt;
-        if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
+        if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
         if (tl.nq == 0 || tl.nkv <= 0) continue;
         if (!mbar_wait(&bars.kv_empty, kvph ^ 1, ctl, 1)) goto done;
         kvph ^= 1;
@@ -247,15 +265,16 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
         }
         for (int i = 0; i < tl.nq; ++i, ++qb) {
           const int s = qb % C::NSTAGE;
+          const int qr = (tl.qb0 + i) * 64;  // first query row of the block in the sequence
           if (!mbar_wait(&bars.stage_empty[s], bit(eph, s) ^ 1, ctl, 2)) goto done;
           eph ^= 1u << s;
           mbar_arrive_expect_tx(&bars.stage_full[s], 2 * C::QT);
           uint8_t *st = smem + C::OFF_STAGE + s * 2 * C::QT;
           for (int c = 0; c < D / 64; ++c) {
             tma_load_3d(st + c * C::QCHUNK, &p.tm_q, &bars.stage_full[s], c * 64, tl.h,
-                        tl.q_row0 + i * 64);
+                        tl.q_row0 + qr);
             tma_load_3d(st + C::QT + c * C::QCHUNK, &p.tm_do, &bars.stage_full[s], c * 64, tl.h,
-                        tl.o_row0 + i * 64);
+                        tl.o_row0 + qr);
           }
         }
       }
@@ -296,10 +315,10 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       // The next tile is decoded one tile ahead (its index loads are off the
       // critical path at the tile switch).
       BwdTile nxt{};
-      if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
+      if (tbeg < tend) nxt = decode_tile<BCAST, GEN>(p, tbeg);
       for (int t = tbeg; t < tend; ++t) {
         const BwdTile tl = nxt;
-        if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
+        if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
         if (tl.nq == 0 || tl.nkv <= 0) continue;
         if (!mbar_wait(&bars.kv_full, kvph, ctl, 10)) goto done;
         kvph ^= 1;
@@ -372,13 +391,31 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     // The next tile is decoded one tile ahead (its index loads are off the
     // critical path at the tile switch).
     BwdTile nxt{};
-    if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
+    if (tbeg < tend) nxt = decode_tile<BCAST, GEN>(p, tbeg);
     for (int t = tbeg; t < tend; ++t) {
       const BwdTile tl = nxt;
-      if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
-      if (tl.nq == 0 || tl.nkv <= 0) continue;
+      if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
+      if (tl.nkv <= 0) continue;
       const bool kv_ok = r < tl.nkv;
+      if (tl.nq == 0) {  // keys that no query sees (band mask, or no queries): dK = dV = 0
+        if (kv_ok) {
+          const int64_t grow = (int64_t)(tl.kv_row0 + r) * p.H + tl.h;
+          uint4 *dvp = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dv) + grow * D);
+          uint4 *dkp = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dk) + grow * D);
+          for (int c = ch * (D / 16); c < (ch + 1) * (D / 16); ++c) {
+            dvp[c] = make_uint4(0, 0, 0, 0);
+            dkp[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        continue;
+      }
       const bool warp_ok = __all_sync(0xffffffffu, kv_ok);  // uniform: no per-element masking
+      // Queries that see this thread's key (band mask; every query without one).
+      const int kq = tl.qdiag0 + r;
+      const int vq_lo =
+          (!GEN || p.win_right < 0) ? 0 : (int)max((int64_t)kq - p.win_right, (int64_t)-1);
+      const int vq_hi = (!GEN || p.win_left < 0) ? (1 << 30)  // (rows past Lq already have P = 0)
+                                       : (int)min((int64_t)kq + p.win_left, (int64_t)1 << 30);
       for (int i = 0; i < tl.nq; ++i, ++qb) {
         const int s = qb % C::NSTAGE;
         if (!mbar_wait(&bars.aux_full[s], bit(aph, s), ctl, 20)) goto done;
@@ -410,6 +447,14 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
           if (!warp_ok) {  // key rows past the sequence (last tile only) have P = 0
 #pragma unroll
             for (int i = 0; i < 32; ++i) pr[i] = kv_ok ? pr[i] : 0.f;
+          }
+          {  // band edges: P = 0 for the queries of these 32 columns that cannot see this key
+            const int cb = (tl.qb0 + i) * 64 + ch * 32;
+            const int lo_rel = vq_lo - cb, hi_rel = vq_hi - cb;
+            if (__any_sync(0xffffffffu, lo_rel > 0 || hi_rel < 31)) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) pr[c] = (c < lo_rel || c > hi_rel) ? 0.f : pr[c];
+            }
           }
           uint32_t pk[16];
 #pragma unroll
@@ -541,8 +586,8 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     uint4 o_r[NV];
     float lse_r = INFINITY;
     bool row_ok = false;
-    auto prefetch = [&](const BlockIter<BCAST> &it) {
-      const int qrow = it.i * 64 + row;
+    auto prefetch = [&](const BlockIter<BCAST, GEN> &it) {
+      const int qrow = (it.tl.qb0 + it.i) * 64 + row;
       row_ok = qrow < it.tl.Lq;
       if (row_ok) {
         lse_r = p.lse[it.tl.lse0 + qrow];
@@ -555,6 +600,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     // One pending dQ reduction: head, first query row in the accumulator, rows.
     struct DqJob {
       int h, row0, rows;
+      int prow;  // deterministic: partial row of the block's first query row
     };
     auto reduce_dq = [&](const DqJob &jb, int qbr) -> bool {
       const int qbuf = qbr & 1;
@@ -591,12 +637,15 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_reduce_add_3d(&p.tm_dqacc, stg, wq * 32, jb.h, jb.row0);
+        if (GEN && p.det)  // deterministic: this key block's own partial, summed in order later
+          tma_store_3d(&p.tm_dqpart, stg, wq * 32, jb.h, jb.prow);
+        else
+          tma_reduce_add_3d(&p.tm_dqacc, stg, wq * 32, jb.h, jb.row0);
         bulk_commit();
       }
       return true;
     };
-    BlockIter<BCAST> cur;
+    BlockIter<BCAST, GEN> cur;
     cur.t = tbeg;
     cur.tend = tend;
     cur.i = 0;
@@ -605,7 +654,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     // Two blocks in flight between LSE/Di staging and the dQ reduction, so the
     // staging of block n runs ahead of the reduction of block n - 2.
     bool have0 = false, have1 = false;
-    DqJob job0{0, 0, 0}, job1{0, 0, 0};
+    DqJob job0{0, 0, 0, 0}, job1{0, 0, 0, 0};
     while (cur.valid) {
       const int s = qb % C::NSTAGE;
       if (!mbar_wait(&bars.stage_full[s], bit(fph, s), ctl, 31)) goto done;
@@ -627,20 +676,23 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
         }
         float di = di2.x + di2.y;
         di += __shfl_xor_sync(0xffffffffu, di, 8);
-        if (half == 0) {
-          lse_s[s * 64 + row] = row_ok ? -lse_r * 1.4426950408889634f : -INFINITY;  // negated
-          di_s[s * 64 + row] = row_ok ? -di : 0.f;                                  // negated
+        if (half == 0) {  // negated; a row that saw no key (LSE = -inf) gets P = 0
+          lse_s[s * 64 + row] = row_ok && lse_r > -INFINITY ? -lse_r * 1.4426950408889634f : -INFINITY;
+          di_s[s * 64 + row] = row_ok ? -di : 0.f;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.aux_full[s]);
-      BlockIter<BCAST> nx = cur;
+      BlockIter<BCAST, GEN> nx = cur;
       nx.next(p);
       if (nx.valid) prefetch(nx);
       if (have0 && !reduce_dq(job0, qb - 2)) goto done;
       job0 = job1;
       have0 = have1;
-      job1 = DqJob{cur.tl.h, cur.tl.q_row0 + cur.i * 64, min(64, cur.tl.Lq - cur.i * 64)};
+      {
+        const int qr = (cur.tl.qb0 + cur.i) * 64;
+        job1 = DqJob{cur.tl.h, cur.tl.q_row0 + qr, min(64, cur.tl.Lq - qr), cur.tl.prow0 + qr};
+      }
       have1 = true;
       cur = nx;
       ++qb;
@@ -665,9 +717,9 @@ done:
   }
 }
 
-template <int D, bool BCAST>
+template <int D, bool BCAST, bool GEN>
 cudaError_t launch_t(const BwdParams &p, int num_sms, cudaStream_t st) {
-  auto kern = jfa_bwd_kernel<D, BCAST>;
+  auto kern = jfa_bwd_kernel<D, BCAST, GEN>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
@@ -700,12 +752,151 @@ __global__ void dq_convert_kernel(const float4 *__restrict__ acc, uint4 *__restr
   }
 }
 
+// Sequence bounds exactly as decode_tile reads them (clamped to the tensors).
+__device__ __forceinline__ void seq_bounds(const BwdParams &p, int64_t b, int64_t *qs, int64_t *Lq,
+                                           int64_t *Lk) {
+  const int64_t s0 = min(max(load_off(p.offsets, p.idx64, (int)b), (int64_t)0), p.T);
+  const int64_t e0 = min(max(load_off(p.offsets, p.idx64, (int)b + 1), s0), p.T);
+  *qs = min(max(load_off(p.q_offsets, p.idx64, (int)b), (int64_t)0), p.Tq);
+  *Lq = min(max(load_off(p.q_offsets, p.idx64, (int)b + 1), *qs), p.Tq) - *qs;
+  *Lk = e0 - s0;
+}
+
+// First partial row of key block n of sequence b (deterministic dQ).
+__device__ __forceinline__ int64_t det_base_row(const BwdParams &p, int64_t b, int n,
+                                                int64_t lqpad) {
+  return p.det_base[b] + (int64_t)n * lqpad;
+}
+
+// Deterministic dQ layout (one CTA of 1024 threads): per sequence, the
+// partial rows (ceil(Lk / 128) key blocks x Lq rounded up to 64) and the
+// 64-row query blocks, as exclusive prefix sums over the batch.
+__global__ void __launch_bounds__(1024) det_layout_kernel(const BwdParams p, int64_t *det_base,
+                                                          int64_t *qb_base) {
+  __shared__ int64_t s_rows[1024], s_qb[1024];
+  const int t = threadIdx.x;
+  const int64_t chunk = (p.B + 1023) / 1024;
+  const int64_t b0 = min(p.B, (int64_t)t * chunk), b1 = min(p.B, b0 + chunk);
+  int64_t rows = 0, qbs = 0;
+  for (int64_t b = b0; b < b1; ++b) {
+    int64_t qs, Lq, Lk;
+    seq_bounds(p, b, &qs, &Lq, &Lk);
+    rows += (Lk + 127) / 128 * ((Lq + 63) / 64 * 64);
+    qbs += (Lq + 63) / 64;
+  }
+  s_rows[t] = rows;
+  s_qb[t] = qbs;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive scan
+    const int64_t a = t >= off ? s_rows[t - off] : 0, q = t >= off ? s_qb[t - off] : 0;
+    __syncthreads();
+    s_rows[t] += a;
+    s_qb[t] += q;
+    __syncthreads();
+  }
+  int64_t br = s_rows[t] - rows, bq = s_qb[t] - qbs;
+  for (int64_t b = b0; b < b1; ++b) {
+    int64_t qs, Lq, Lk;
+    seq_bounds(p, b, &qs, &Lq, &Lk);
+    det_base[b] = br;
+    qb_base[b] = bq;
+    br += (Lk + 127) / 128 * ((Lq + 63) / 64 * 64);
+    bq += (Lq + 63) / 64;
+  }
+  if (t == 1023) {
+    det_base[p.B] = s_rows[1023];
+    qb_base[p.B] = s_qb[1023];
+    if (s_rows[1023] > p.det_rows) atomicCAS(p.status, 0u, 3u);  // JFA_ERR_WORKSPACE
+  }
+}
+
+// Deterministic dQ: one 64-row query block per iteration of the grid-stride
+// loop; its rows sum, in key-block order, the partials of the key blocks that
+// walked that query block (a contiguous range of key blocks, since the band's
+// query range grows with the key block), scale, and store bf16.
+template <int D>
+__global__ void __launch_bounds__(256, 4) det_cast_kernel(const BwdParams p, const float *part,
+                                                       const int64_t *qb_base, __nv_bfloat16 *dq) {
+  __shared__ int s_na, s_nb;
+  __shared__ int64_t s_b;
+  const int64_t total = qb_base[p.B];
+  const int HD8 = p.H * D / 8;
+  for (int64_t g = blockIdx.x; g < total; g += gridDim.x) {
+    if (threadIdx.x == 0) {  // the sequence of block g: the last b with qb_base[b] <= g
+      int64_t lo = 0, hi = p.B;
+      while (hi - lo > 1) {
+        const int64_t mid = (lo + hi) / 2;
+        if (qb_base[mid] <= g) lo = mid; else hi = mid;
+      }
+      s_b = lo;
+      s_na = 1 << 30;
+      s_nb = -1;
+    }
+    __syncthreads();
+    const int64_t b = s_b;
+    const int qb = (int)(g - qb_base[b]);
+    int64_t qs, Lq, Lk;
+    seq_bounds(p, b, &qs, &Lq, &Lk);
+    const int nkt = (int)((Lk + 127) / 128);
+    for (int n = threadIdx.x; n < nkt; n += blockDim.x) {
+      int qb0, nq;
+      bwd_query_blocks(n, Lq, Lk, p.win_left, p.win_right, &qb0, &nq);
+      if (qb >= qb0 && qb < qb0 + nq) {
+        atomicMin(&s_na, n);
+        atomicMax(&s_nb, n);
+      }
+    }
+    __syncthreads();
+    const int na = s_na, nb = s_nb;
+    const int64_t lqpad = (Lq + 63) / 64 * 64;
+    const int rows = (int)min((int64_t)64, Lq - (int64_t)qb * 64);
+    for (int e = threadIdx.x; e < rows * HD8; e += blockDim.x) {
+      const int row = e / HD8, rem = e - row * HD8;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int n = na; n <= nb; ++n) {
+        const int64_t prow = det_base_row(p, b, n, lqpad) + (int64_t)qb * 64 + row;
+        if (prow >= p.det_rows) continue;  // (only with a workspace too small: reported)
+        const float4 *src = reinterpret_cast<const float4 *>(part + prow * p.H * D) + rem * 2;
+        const float4 x = src[0], y = src[1];
+        acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
+        acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
+      }
+      const float sc = p.scale;
+      reinterpret_cast<uint4 *>(dq + (qs + (int64_t)qb * 64 + row) * p.H * D)[rem] =
+          make_uint4(pack_bf16(acc[0] * sc, acc[1] * sc), pack_bf16(acc[2] * sc, acc[3] * sc),
+                     pack_bf16(acc[4] * sc, acc[5] * sc), pack_bf16(acc[6] * sc, acc[7] * sc));
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_det_layout(const BwdParams &p, int64_t *det_base, int64_t *qb_base,
+                              cudaStream_t st) {
+  det_layout_kernel<<<1, 1024, 0, st>>>(p, det_base, qb_base);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_det_cast(const BwdParams &p, const float *part, const int64_t *qb_base,
+                            void *dq, int D, int num_sms, cudaStream_t st) {
+  auto *out = static_cast<__nv_bfloat16 *>(dq);
+  if (D == 128)
+    det_cast_kernel<128><<<num_sms * 8, 256, 0, st>>>(p, part, qb_base, out);
+  else
+    det_cast_kernel<64><<<num_sms * 8, 256, 0, st>>>(p, part, qb_base, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bwd(const BwdParams &p, int D, int num_sms, cudaStream_t st) {
   const bool bcast = p.Lq > 0;
-  if (D == 128) return bcast ? launch_t<128, true>(p, num_sms, st) : launch_t<128, false>(p, num_sms, st);
-  return bcast ? launch_t<64, true>(p, num_sms, st) : launch_t<64, false>(p, num_sms, st);
+  const bool gen = !bcast && (p.win_left >= 0 || p.win_right >= 0 || p.det);
+  if (D == 128) {
+    if (bcast) return launch_t<128, true, false>(p, num_sms, st);
+    return gen ? launch_t<128, false, true>(p, num_sms, st) : launch_t<128, false, false>(p, num_sms, st);
+  }
+  if (bcast) return launch_t<64, true, false>(p, num_sms, st);
+  return gen ? launch_t<64, false, true>(p, num_sms, st) : launch_t<64, false, false>(p, num_sms, st);
 }
 
 static int grid_for(int64_t n) {

@@ -40,6 +40,7 @@
 //   [256,256+D) O of half A   [384,384+D) O of half B
 #include <cuda_bf16.h>
 
+#include "band.h"
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -72,9 +73,11 @@ struct FwdBars {
 };
 
 struct FwdTile {
-  int b, h, n_kv, Lk, nrows0, nrows1;
+  int b, h, n_kv, nrows0, nrows1;
+  int kv_len;        // keys from the first loaded key to the end of the sequence
+  int diag0;         // key (counted from the first loaded key) aligned with the tile's first query row
   int q_coord;       // row coordinate of the tile's first query row in tm_q
-  int kv0;           // first key row in tm_k / tm_v
+  int kv0;           // first key row loaded, in tm_k / tm_v
   int64_t out_row0;  // row of the tile's first query row in O
   int64_t lse0;      // index of that row's LSE
 };
@@ -83,7 +86,9 @@ __device__ __forceinline__ int64_t load_off(const void *off, int idx64, int i) {
   return idx64 ? static_cast<const int64_t *>(off)[i] : (int64_t) static_cast<const int *>(off)[i];
 }
 
-template <bool BCAST>
+// GEN: the band mask is compiled in (jfa_varlen_fwd with a window); without
+// it every row sees all of its sequence's keys.
+template <bool BCAST, bool GEN>
 __device__ __forceinline__ FwdTile decode_tile(const FwdParams &p, int t) {
   FwdTile d;
   d.b = p.tiles[3 * t];
@@ -96,26 +101,41 @@ __device__ __forceinline__ FwdTile decode_tile(const FwdParams &p, int t) {
   const int64_t s0 = in ? min(max(load_off(p.offsets, p.idx64, d.b), (int64_t)0), p.T) : 0;
   const int64_t e0 = in ? min(max(load_off(p.offsets, p.idx64, d.b + 1), s0), p.T) : 0;
   const int L = (int)(e0 - s0);
-  const int Lq = BCAST ? (in ? p.Lq : 0) : L;
+  int64_t qs = 0;
+  int Lq;
+  if (BCAST) {
+    Lq = in ? p.Lq : 0;
+  } else {
+    qs = in ? min(max(load_off(p.q_offsets, p.idx64, d.b), (int64_t)0), p.Tq) : 0;
+    Lq = (int)(in ? min(max(load_off(p.q_offsets, p.idx64, d.b + 1), qs), p.Tq) - qs : 0);
+  }
   const int row0 = m * 256;
-  d.Lk = L;
-  d.n_kv = (L + 127) / 128;
   d.nrows0 = max(0, min(128, Lq - row0));
   d.nrows1 = max(0, min(128, Lq - row0 - 128));
-  d.kv0 = (int)s0;
+  // Keys the tile's rows can see (all of them without a band mask), in
+  // 128-key tiles: K/V tiles j0 .. j0 + n_kv - 1 of the sequence.
+  int64_t lo = 0, hi = 0;
+  if (d.nrows0 > 0)
+    fwd_key_range(row0, row0 + d.nrows0 + d.nrows1, Lq, L, GEN ? p.win_left : -1,
+                  GEN ? p.win_right : -1, &lo, &hi);
+  const int j0 = (int)(lo / 128);
+  d.n_kv = hi > lo ? (int)((hi + 127) / 128) - j0 : 0;
+  d.kv_len = L - j0 * 128;
+  d.diag0 = row0 + (L - Lq) - j0 * 128;
+  d.kv0 = (int)s0 + j0 * 128;
   if (BCAST) {
     d.q_coord = row0;
     d.out_row0 = (int64_t)d.b * Lq + row0;
     d.lse0 = ((int64_t)d.b * p.H + d.h) * Lq + row0;
   } else {
-    d.q_coord = (int)s0 + row0;
-    d.out_row0 = s0 + row0;
-    d.lse0 = (int64_t)d.h * p.T + s0 + row0;
+    d.q_coord = (int)qs + row0;
+    d.out_row0 = qs + row0;
+    d.lse0 = (int64_t)d.h * p.Tq + qs + row0;
   }
   return d;
 }
 
-template <int D, bool BCAST>
+template <int D, bool BCAST, bool GEN>
 __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -169,10 +189,10 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       // The next tile is decoded one tile ahead (its index loads are off the
       // critical path at the tile switch).
       FwdTile nxt{};
-      if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
+      if (tbeg < tend) nxt = decode_tile<BCAST, GEN>(p, tbeg);
       for (int t = tbeg; t < tend; ++t) {
         const FwdTile tl = nxt;
-        if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
+        if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
         if (tl.n_kv == 0) continue;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
@@ -250,10 +270,10 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       // The next tile is decoded one tile ahead (its index loads are off the
       // critical path at the tile switch).
       FwdTile nxt{};
-      if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
+      if (tbeg < tend) nxt = decode_tile<BCAST, GEN>(p, tbeg);
       for (int t = tbeg; t < tend; ++t) {
         const FwdTile tl = nxt;
-        if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
+        if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
         if (tl.n_kv == 0) continue;
         const uint32_t has = (tl.nrows0 > 0 ? 1u : 0u) | (tl.nrows1 > 0 ? 2u : 0u);
 #pragma unroll
@@ -315,22 +335,31 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
     // The next tile is decoded one tile ahead (its index loads are off the
     // critical path at the tile switch).
     FwdTile nxt{};
-    if (tbeg < tend) nxt = decode_tile<BCAST>(p, tbeg);
+    if (tbeg < tend) nxt = decode_tile<BCAST, GEN>(p, tbeg);
     for (int t = tbeg; t < tend; ++t) {
       const FwdTile tl = nxt;
-      if (t + 1 < tend) nxt = decode_tile<BCAST>(p, t + 1);
+      if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
       const int nrows = x ? tl.nrows1 : tl.nrows0;
       if (nrows == 0) continue;
       const bool row_ok = r < nrows;
       const int64_t orow = tl.out_row0 + x * 128 + r;
       uint4 *optr = reinterpret_cast<uint4 *>(obase + (orow * p.H + tl.h) * D);
-      if (tl.n_kv == 0) {  // broadcast-Q sequence with no keys: O = 0, LSE = -inf
+      if (tl.n_kv == 0) {  // rows that see no key (no keys, or outside the band): O = 0, LSE = -inf
         if (row_ok) {
           for (int i = 0; i < D / 8; ++i) optr[i] = make_uint4(0, 0, 0, 0);
           p.lse[tl.lse0 + x * 128 + r] = -INFINITY;
         }
         continue;
       }
+      // This row's visible keys [vis_lo, vis_hi], counted from the tile's
+      // first loaded key: all of them, or the band (the last K/V tile is
+      // masked past the sequence end).
+      const int dg = tl.diag0 + x * 128 + r;
+      const int vis_lo =
+          (!GEN || p.win_left < 0) ? 0 : (int)max((int64_t)dg - p.win_left, (int64_t)-1);
+      const int vis_hi = (!GEN || p.win_right < 0)
+                             ? tl.kv_len - 1
+                             : (int)min((int64_t)dg + p.win_right, (int64_t)tl.kv_len - 1);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < tl.n_kv; ++j) {
         if (!mbar_wait(&bars.s_full[x], sph, ctl, 20 + x)) goto done;
@@ -340,13 +369,15 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
         tmem_wait_ld();
-        const int valid = tl.Lk - j * 128;
-        if (valid < 128) {  // peeled tail: mask keys past the sequence end
+        // Masked columns only where some row of the warp needs them: the
+        // peeled tail past the sequence end and the edges of a band.
+        const int lo_rel = vis_lo - j * 128, hi_rel = vis_hi - j * 128;
+        if (__any_sync(0xffffffffu, lo_rel > 0 || hi_rel < 127)) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (c * 32 + i >= valid) s[c][i] = __float_as_uint(-INFINITY);
+              if (c * 32 + i < lo_rel || c * 32 + i > hi_rel) s[c][i] = __float_as_uint(-INFINITY);
         }
         float mx[8];
 #pragma unroll
@@ -363,12 +394,15 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
         float alpha = 1.f;
         if (j == 0) {
           m_run = m_tile;
-        } else if (m_tile > m_run + 8.f) {
+        } else if (m_tile > m_run + 8.f) {  // also when every earlier key was masked (m_run = -inf)
           alpha = ex2(m_run - m_tile);
           m_run = m_tile;
         }
+        // A row with every key so far masked keeps m_run = -inf; its
+        // exponentials are then exp2(-inf - 0) = 0, not NaN.
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;
         float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_run, -m_run);
+        const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_use, -m_use);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
@@ -404,7 +438,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       oph ^= 1;
       tc_fence_after();
       {
-        const float inv_l = 1.f / l_run;
+        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;  // a row that saw no key: O = 0
         const float2 inv2 = make_float2(inv_l, inv_l);
 #pragma unroll 1
         for (int c = 0; c < D / 32; c += 2) {  // two 32-column chunks in flight
@@ -423,7 +457,9 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
             }
           }
         }
-        if (row_ok) p.lse[tl.lse0 + x * 128 + r] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+        if (row_ok)
+          p.lse[tl.lse0 + x * 128 + r] =
+              l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       }
       tc_fence_before();
       __syncwarp();
@@ -446,9 +482,9 @@ done:
   }
 }
 
-template <int D, bool BCAST>
+template <int D, bool BCAST, bool GEN>
 cudaError_t launch_t(const FwdParams &p, int num_sms, cudaStream_t st) {
-  auto kern = jfa_fwd_kernel<D, BCAST>;
+  auto kern = jfa_fwd_kernel<D, BCAST, GEN>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
@@ -460,8 +496,13 @@ cudaError_t launch_t(const FwdParams &p, int num_sms, cudaStream_t st) {
 
 cudaError_t launch_fwd(const FwdParams &p, int D, int num_sms, cudaStream_t st) {
   const bool bcast = p.Lq > 0;
-  if (D == 128) return bcast ? launch_t<128, true>(p, num_sms, st) : launch_t<128, false>(p, num_sms, st);
-  return bcast ? launch_t<64, true>(p, num_sms, st) : launch_t<64, false>(p, num_sms, st);
+  const bool gen = !bcast && (p.win_left >= 0 || p.win_right >= 0);
+  if (D == 128) {
+    if (bcast) return launch_t<128, true, false>(p, num_sms, st);
+    return gen ? launch_t<128, false, true>(p, num_sms, st) : launch_t<128, false, false>(p, num_sms, st);
+  }
+  if (bcast) return launch_t<64, true, false>(p, num_sms, st);
+  return gen ? launch_t<64, false, true>(p, num_sms, st) : launch_t<64, false, false>(p, num_sms, st);
 }
 
 }  // namespace jfa

@@ -14,15 +14,17 @@ struct FwdParams {
   CUtensorMap tm_q;  // bf16 [rows, H, D] viewed as {D, H, rows}, box {64, 1, 128}, 128B swizzle
   CUtensorMap tm_k;  // bf16 [Tk, H, D], same box
   CUtensorMap tm_v;
-  const void *offsets;  // device [B+1]
-  int idx64;            // offsets are int64
+  const void *offsets;    // device [B+1]: K/V sequence bounds
+  const void *q_offsets;  // device [B+1]: query sequence bounds (jagged; may equal offsets)
+  int idx64;              // offsets are int64
   const int32_t *sm_ptr;
   const int32_t *tiles;
   void *o;      // bf16
   float *lse;   // fp32
   int64_t B;    // sequences: tiles naming b >= B are skipped
-  int64_t T;    // packed K/V length (LSE row stride for the jagged layout);
-                // sequence bounds read from the offsets are clamped to [0, T]
+  int64_t T;    // packed K/V length; K/V bounds read from the offsets are clamped to [0, T]
+  int64_t Tq;   // packed query length (jagged: LSE row stride; query bounds clamped to it)
+  int win_left, win_right;  // band mask (band.h); -1 = unbounded
   int H;
   int Lq;       // broadcast-Q: dense query length; 0 for jagged self-attention
   float scale_log2;  // scale * log2(e)
@@ -50,7 +52,9 @@ struct BwdParams {
   CUtensorMap tm_k;   // bf16 [Tk, H, D], box {64, 1, 128}
   CUtensorMap tm_v;
   CUtensorMap tm_dqacc;  // fp32 [rows, H, D] as {D, H, rows}, box {32, 1, 64}, no swizzle
-  const void *offsets;
+  CUtensorMap tm_dqpart;  // deterministic dQ: fp32 partials [rows, H, D], box {32, 1, 64}
+  const void *offsets;    // K/V sequence bounds
+  const void *q_offsets;  // query sequence bounds (jagged; may equal offsets)
   int idx64;
   const int32_t *sm_ptr;
   const int32_t *tiles;
@@ -58,8 +62,16 @@ struct BwdParams {
   const void *o;  // bf16 O rows (read directly for Di)
   void *dk;  // bf16 [Tk, H, D]
   void *dv;
-  int64_t B;  // sequences: tiles naming b >= B are skipped
-  int64_t T;  // packed K/V length; sequence bounds are clamped to [0, T]
+  int64_t B;   // sequences: tiles naming b >= B are skipped
+  int64_t T;   // packed K/V length; K/V bounds are clamped to [0, T]
+  int64_t Tq;  // packed query length (jagged); query bounds are clamped to [0, Tq]
+  int win_left, win_right;  // band mask (band.h); -1 = unbounded
+  // Deterministic dQ: each key block stores its dQ partial of each query block
+  // (no atomics) at row det_base[b] + n * round_up(Lq, 64) + 64 * qb of the
+  // partial buffer (det_rows rows); a separate pass sums them in key-block order.
+  int det;
+  const int64_t *det_base;
+  int64_t det_rows;
   int H;
   int Lq;  // broadcast-Q: dense query length; 0 for jagged
   float scale;
@@ -79,6 +91,18 @@ cudaError_t launch_acc_clear(float *acc, int64_t n16, const uint32_t *status, cu
 // zero-accumulator count (the accumulator is dirty from here on).
 cudaError_t launch_dq_convert(const float *acc, void *dq, int64_t rows, int H, int D, float scale,
                               uint32_t *status, cudaStream_t st);
+
+// Deterministic dQ layout: det_base[b] (partial rows before sequence b,
+// [B+1]) and qb_base[b] (64-row query blocks before sequence b, [B+1]) from
+// the device offsets; if the partial rows exceed det_rows, status word 0 is
+// set to JFA_ERR_WORKSPACE.
+cudaError_t launch_det_layout(const BwdParams &p, int64_t *det_base, int64_t *qb_base,
+                              cudaStream_t st);
+
+// Deterministic dQ: dq[row] = bf16(scale * sum over the key blocks that walk
+// the row's query block, in key-block order, of their partials).
+cudaError_t launch_det_cast(const BwdParams &p, const float *part, const int64_t *qb_base,
+                            void *dq, int D, int num_sms, cudaStream_t st);
 
 // Block-diagonal kernels: [B, L, H, D], 64-token blocks, 128-row work units.
 struct BlockdiagParams {

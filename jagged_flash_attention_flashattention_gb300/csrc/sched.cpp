@@ -13,6 +13,7 @@
 #include <numeric>
 #include <vector>
 
+#include "band.h"
 #include "host_common.h"
 
 namespace jfa {
@@ -96,32 +97,64 @@ jfa_status enumerate(int64_t B, int H, int tile_rows, const void *off, jfa_index
 
 }  // namespace
 
-extern "C" jfa_status jfa_sched_size(int64_t B, int H, int tile_rows, const void *host_offsets,
-                                     jfa_index_t idx, int64_t fixed_rows, int64_t *n_tiles) {
-  if (!n_tiles) return fail(JFA_ERR_INVALID_ARG, "n_tiles is NULL");
-  return enumerate(B, H, tile_rows, host_offsets, idx, fixed_rows, 0, nullptr, n_tiles);
+namespace {
+
+// Tiles of the masked / cross (varlen) forward (tiles of 256 query rows) or
+// backward (tiles of 128 keys); work = the length of the key range the
+// tile's query rows can see (forward) or of the query range that can see the
+// tile's keys (backward), both from band.h. Tiles with no work are kept: the
+// forward writes O = 0 for their rows, the backward dK = dV = 0.
+jfa_status enumerate_varlen(int64_t B, int H, jfa_op op, const void *q_off, const void *kv_off,
+                            jfa_index_t idx, int left, int right, std::vector<Tile> *out,
+                            int64_t *count) {
+  if (H < 1) return fail(JFA_ERR_INVALID_ARG, "H = %d < 1", H);
+  if (op != JFA_OP_FWD && op != JFA_OP_BWD)
+    return fail(JFA_ERR_INVALID_ARG, "op must be JFA_OP_FWD or JFA_OP_BWD");
+  if (left < -1 || right < -1) return fail(JFA_ERR_INVALID_ARG, "window bounds must be >= -1");
+  if (!q_off) q_off = kv_off;
+  jfa_status st = check_host_offsets(kv_off, idx, B, -1);
+  if (st != JFA_OK) return st;
+  st = check_host_offsets(q_off, idx, B, -1);
+  if (st != JFA_OK) return st;
+  int64_t n = 0;
+  std::vector<int64_t> work;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t Lq = offset_at(q_off, idx, b + 1) - offset_at(q_off, idx, b);
+    const int64_t Lk = offset_at(kv_off, idx, b + 1) - offset_at(kv_off, idx, b);
+    const int64_t rows = op == JFA_OP_FWD ? Lq : Lk;
+    const int64_t tr = op == JFA_OP_FWD ? kFwdTileRows : kBwdTileKeys;
+    const int64_t n_m = (rows + tr - 1) / tr;
+    if (out) {  // enumeration order b, h, m (the tie order of the stable sort)
+      work.resize(n_m);
+      for (int64_t m = 0; m < n_m; ++m) {
+        int64_t lo, hi;
+        if (op == JFA_OP_FWD)
+          fwd_key_range(m * tr, band_min(Lq, m * tr + tr), Lq, Lk, left, right, &lo, &hi);
+        else
+          bwd_query_range(m * tr, band_min(Lk, m * tr + tr), Lq, Lk, left, right, &lo, &hi);
+        work[m] = hi - lo;
+      }
+      for (int h = 0; h < H; ++h)
+        for (int64_t m = 0; m < n_m; ++m) out->push_back({(int32_t)b, h, (int32_t)m, work[m]});
+    }
+    n += n_m * H;
+    if (n >= (int64_t(1) << 31) / 3) return fail(JFA_ERR_INVALID_ARG, "too many tiles");
+  }
+  *count = n;
+  return JFA_OK;
 }
 
-extern "C" jfa_status jfa_sched_build(int64_t B, int H, int tile_rows, int num_sms,
-                                      const void *host_offsets, jfa_index_t idx,
-                                      int64_t fixed_rows, int64_t fixed_work, int zigzag,
-                                      int32_t *sm_ptr, int32_t *tiles) {
-  if (num_sms < 1) return fail(JFA_ERR_INVALID_ARG, "num_sms = %d < 1", num_sms);
-  if (!sm_ptr) return fail(JFA_ERR_INVALID_ARG, "sm_ptr is NULL");
-  std::vector<Tile> all;
-  int64_t n = 0;
-  jfa_status st =
-      enumerate(B, H, tile_rows, host_offsets, idx, fixed_rows, fixed_work, &all, &n);
-  if (st != JFA_OK) return st;
-  if (n > 0 && !tiles) return fail(JFA_ERR_INVALID_ARG, "tiles is NULL");
-
+// Sorts (LPT, stable) or keeps the enumeration order and deals the tiles to
+// the SMs, zigzag or round-robin, into the CSR output.
+void deal(const std::vector<Tile> &all, int num_sms, int zigzag, int32_t *sm_ptr,
+          int32_t *tiles) {
+  const int64_t n = (int64_t)all.size();
   std::vector<int32_t> order(n);
   std::iota(order.begin(), order.end(), 0);
   if (zigzag) {
     std::stable_sort(order.begin(), order.end(),
                      [&](int32_t a, int32_t b) { return all[a].work > all[b].work; });
   }
-  // Deal: sorted position i -> SM; count per SM, then place in dealt order.
   std::vector<int32_t> sm_of(n);
   std::vector<int32_t> cnt(num_sms, 0);
   for (int64_t i = 0; i < n; ++i) {
@@ -141,5 +174,54 @@ extern "C" jfa_status jfa_sched_build(int64_t B, int H, int tile_rows, int num_s
     tiles[3 * pos + 1] = t.h;
     tiles[3 * pos + 2] = t.m;
   }
+}
+
+}  // namespace
+
+extern "C" jfa_status jfa_sched_size_varlen(int64_t B, int H, jfa_op op,
+                                            const void *host_q_offsets,
+                                            const void *host_kv_offsets, jfa_index_t idx,
+                                            int64_t *n_tiles) {
+  if (!n_tiles) return fail(JFA_ERR_INVALID_ARG, "n_tiles is NULL");
+  return enumerate_varlen(B, H, op, host_q_offsets, host_kv_offsets, idx, -1, -1, nullptr,
+                          n_tiles);
+}
+
+extern "C" jfa_status jfa_sched_build_varlen(int64_t B, int H, jfa_op op, int num_sms,
+                                             const void *host_q_offsets,
+                                             const void *host_kv_offsets, jfa_index_t idx,
+                                             int window_left, int window_right, int zigzag,
+                                             int32_t *sm_ptr, int32_t *tiles) {
+  if (num_sms < 1) return fail(JFA_ERR_INVALID_ARG, "num_sms = %d < 1", num_sms);
+  if (!sm_ptr) return fail(JFA_ERR_INVALID_ARG, "sm_ptr is NULL");
+  std::vector<Tile> all;
+  int64_t n = 0;
+  jfa_status st = enumerate_varlen(B, H, op, host_q_offsets, host_kv_offsets, idx, window_left,
+                                   window_right, &all, &n);
+  if (st != JFA_OK) return st;
+  if (n > 0 && !tiles) return fail(JFA_ERR_INVALID_ARG, "tiles is NULL");
+  deal(all, num_sms, zigzag, sm_ptr, tiles);
+  return JFA_OK;
+}
+
+extern "C" jfa_status jfa_sched_size(int64_t B, int H, int tile_rows, const void *host_offsets,
+                                     jfa_index_t idx, int64_t fixed_rows, int64_t *n_tiles) {
+  if (!n_tiles) return fail(JFA_ERR_INVALID_ARG, "n_tiles is NULL");
+  return enumerate(B, H, tile_rows, host_offsets, idx, fixed_rows, 0, nullptr, n_tiles);
+}
+
+extern "C" jfa_status jfa_sched_build(int64_t B, int H, int tile_rows, int num_sms,
+                                      const void *host_offsets, jfa_index_t idx,
+                                      int64_t fixed_rows, int64_t fixed_work, int zigzag,
+                                      int32_t *sm_ptr, int32_t *tiles) {
+  if (num_sms < 1) return fail(JFA_ERR_INVALID_ARG, "num_sms = %d < 1", num_sms);
+  if (!sm_ptr) return fail(JFA_ERR_INVALID_ARG, "sm_ptr is NULL");
+  std::vector<Tile> all;
+  int64_t n = 0;
+  jfa_status st =
+      enumerate(B, H, tile_rows, host_offsets, idx, fixed_rows, fixed_work, &all, &n);
+  if (st != JFA_OK) return st;
+  if (n > 0 && !tiles) return fail(JFA_ERR_INVALID_ARG, "tiles is NULL");
+  deal(all, num_sms, zigzag, sm_ptr, tiles);
   return JFA_OK;
 }

@@ -234,6 +234,17 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, const 
       : "memory");
 }
 
+// 3-D tiled store of a shared-memory box into global memory (rows past the
+// tensor's extent are not written).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int c0,
+                                             int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -92,6 +92,11 @@ def blockdiag_inputs(B, L, H, D, seed, device="cpu", with_grad=True):
 WORKLOADS = {
     "tiny": dict(kind="jagged", H=2, D=64, offsets_dtype=np.int32),
     "gem": dict(kind="jagged", H=4, D=128, offsets_dtype=np.int64),
+    # the GEM batch with a causal mask, and with the deterministic dQ reduction
+    "gem_causal": dict(kind="varlen", lengths="gem", H=4, D=128, offsets_dtype=np.int64,
+                       window=(-1, 0), deterministic=False),
+    "gem_det": dict(kind="varlen", lengths="gem", H=4, D=128, offsets_dtype=np.int64,
+                    window=(-1, -1), deterministic=True),
     "stress": dict(kind="jagged", H=4, D=128, offsets_dtype=np.int64),
     "bcast": dict(kind="bcast", H=4, D=128, Lq=256, offsets_dtype=np.int64),
     "blockdiag": dict(kind="blockdiag", B=1152, L=4096, H=2, D=128),
@@ -99,13 +104,27 @@ WORKLOADS = {
 }
 
 
-def useful_flops(name_or_kind, lengths=None, H=None, D=None, Lq=None, B=None, L=None, block=64):
+def visible_pairs(Lq, Lk, window=(-1, -1)):
+    """Number of (query, key) pairs of one sequence that a band mask
+    (left, right) keeps (-1 = unbounded; query i is aligned with key
+    i + Lk - Lq). Used to count useful FLOPs of masked workloads."""
+    left, right = window
+    i = np.arange(Lq, dtype=np.int64) + (Lk - Lq)
+    lo = np.zeros(Lq, dtype=np.int64) if left < 0 else np.maximum(0, i - left)
+    hi = np.full(Lq, Lk - 1, dtype=np.int64) if right < 0 else np.minimum(Lk - 1, i + right)
+    return int(np.sum(np.maximum(0, hi - lo + 1)))
+
+
+def useful_flops(name_or_kind, lengths=None, H=None, D=None, Lq=None, B=None, L=None, block=64,
+                 window=(-1, -1)):
     """Useful (unpadded) forward FLOPs: 4 * H * D * sum_b Lq_b * Lk_b.
 
     The backward counts 2.5x this (five contractions against two).
     """
     if name_or_kind == "jagged":
         return 4.0 * H * D * float(np.sum(np.asarray(lengths, dtype=np.float64) ** 2))
+    if name_or_kind == "varlen":  # self-attention lengths with a band mask
+        return 4.0 * H * D * float(sum(visible_pairs(int(n), int(n), window) for n in lengths))
     if name_or_kind == "bcast":
         return 4.0 * H * D * Lq * float(np.sum(lengths))
     if name_or_kind == "blockdiag":

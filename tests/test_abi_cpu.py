@@ -209,3 +209,56 @@ def test_host_offsets_checks():
                    (np.array([[0, 3]]), 2), (np.array([0.0, 3.0]), 2)):
         with pytest.raises(ValueError):
             jfa.check_host_offsets(bad, n)
+
+
+@pytest.mark.parametrize("window", [(-1, -1), (-1, 0), (255, 0), (0, 0), (100, 300), (-1, 7),
+                                    (513, -1)])
+@pytest.mark.parametrize("op", [jfa.OP_FWD, jfa.OP_BWD])
+def test_c_varlen_scheduler_matches_oracle(L, window, op):
+    rng = np.random.default_rng(71)
+    ql = rng.integers(0, 900, 60)
+    kl = np.where(rng.random(60) < 0.5, ql, rng.integers(0, 900, 60))  # self and cross mixed
+    for zz in (True, False):
+        sp, tl = jfa.schedule_varlen(W.offsets_of(ql), W.offsets_of(kl), 3, op, 11, window, zz)
+        rp, rt = S.schedule_varlen(list(ql), list(kl), 3, "fwd" if op == jfa.OP_FWD else "bwd",
+                                   11, window, zz)
+        assert sp.tolist() == rp
+        assert [tuple(t) for t in tl.tolist()] == rt
+
+
+def test_c_varlen_scheduler_rejects_bad_arguments(L):
+    off = np.array([0, 5, 9], dtype=np.int64)
+    sm = np.zeros(4, dtype=np.int32)
+    tl = np.zeros(30, dtype=np.int32)
+    assert L.jfa_sched_build_varlen(2, 1, jfa.OP_FWD, 3, off.ctypes.data, off.ctypes.data, 1, -2, 0,
+                                    1, sm.ctypes.data, tl.ctypes.data) == 1
+    assert L.jfa_sched_build_varlen(2, 1, jfa.OP_BCASTQ_FWD, 3, off.ctypes.data, off.ctypes.data,
+                                    1, -1, -1, 1, sm.ctypes.data, tl.ctypes.data) == 1
+    bad = np.array([0, 5, 4], dtype=np.int64)
+    assert L.jfa_sched_build_varlen(2, 1, jfa.OP_BWD, 3, bad.ctypes.data, off.ctypes.data, 1, -1,
+                                    -1, 1, sm.ctypes.data, tl.ctypes.data) == 1
+
+
+def test_varlen_workspace_sizes(L):
+    qo = np.array([0, 100, 100, 400], dtype=np.int64)
+    ko = np.array([0, 300, 301, 302], dtype=np.int64)
+    sz = ctypes.c_size_t(0)
+    assert L.jfa_varlen_workspace_size(3, qo.ctypes.data, ko.ctypes.data, 1, 2, 64, 0,
+                                       ctypes.byref(sz)) == 0
+    assert sz.value == 256 + 400 * 2 * 64 * 4
+    assert L.jfa_varlen_workspace_size(3, qo.ctypes.data, ko.ctypes.data, 1, 2, 64, 1,
+                                       ctypes.byref(sz)) == 0
+    # partial rows: ceil(300/128)*round_up(100,64) + 1*0 + 1*round_up(300,64) = 3*128 + 320
+    header = 256 + ((2 * 4 * 8 + 255) // 256) * 256
+    assert sz.value == header + (3 * 128 + 320) * 2 * 64 * 4
+
+
+def test_varlen_entry_points_reject_bad_windows_on_host(L):
+    dummy = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(dummy, ctypes.c_void_p)
+    code = L.jfa_varlen_fwd(p, p, p, p, p, 0, 1, 10, 10, 2, 64, 0.1, -3, 0, p, p, 1, p, p, p, 256,
+                            _null())
+    assert code == 1 and b"window" in L.jfa_last_error()
+    code = L.jfa_varlen_bwd(p, p, p, p, p, p, p, p, 0, 1, 10, 10, 2, 64, 0.1, 0, -5, 0, p, p, 1, p, p,
+                            p, p, 1 << 20, _null())
+    assert code == 1 and b"window" in L.jfa_last_error()
