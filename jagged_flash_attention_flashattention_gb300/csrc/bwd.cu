@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
 #pragma unroll
             for (int i = 0; i < 32; ++i) pr[i] = kv_ok ? pr[i] : 0.f;
           }
-          {  // band edges: P = 0 for the queries of these 32 columns that cannot see this key
+          if constexpr (GEN) {  // band edges: P = 0 for the queries of these 32 columns that cannot see this key
             const int cb = (tl.qb0 + i) * 64 + ch * 32;
             const int lo_rel = vq_lo - cb, hi_rel = vq_hi - cb;
             if (__any_sync(0xffffffffu, lo_rel > 0 || hi_rel < 31)) {
@@ -597,9 +597,10 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
         for (int j = 0; j < NV; ++j) o_r[j] = __ldg(src + j);
       }
     };
-    // One pending dQ reduction: head, first query row in the accumulator, rows.
+    // One pending dQ reduction: head, first query row in the accumulator (rows
+    // past the sequence carry zeros: P = 0 there).
     struct DqJob {
-      int h, row0, rows;
+      int h, row0;
       int prow;  // deterministic: partial row of the block's first query row
     };
     auto reduce_dq = [&](const DqJob &jb, int qbr) -> bool {
@@ -615,7 +616,6 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.dq_free[qbuf]);  // TMEM released before the reduction
       if (wq * 32 >= D) return true;               // D = 64: lanes 64..127 are padding
-      (void)jb.rows;  // rows past the sequence carry zeros (P = 0 there)
       if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
       if constexpr (BCAST) {  // the caller's fp32 dQ is the accumulator: scale each partial
@@ -654,7 +654,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     // Two blocks in flight between LSE/Di staging and the dQ reduction, so the
     // staging of block n runs ahead of the reduction of block n - 2.
     bool have0 = false, have1 = false;
-    DqJob job0{0, 0, 0, 0}, job1{0, 0, 0, 0};
+    DqJob job0{0, 0, 0}, job1{0, 0, 0};
     while (cur.valid) {
       const int s = qb % C::NSTAGE;
       if (!mbar_wait(&bars.stage_full[s], bit(fph, s), ctl, 31)) goto done;
@@ -683,18 +683,18 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.aux_full[s]);
-      BlockIter<BCAST, GEN> nx = cur;
-      nx.next(p);
-      if (nx.valid) prefetch(nx);
+      DqJob jnew;  // this block's reduction, run two blocks from now
+      {
+        const int qr = (cur.tl.qb0 + cur.i) * 64;
+        jnew = DqJob{cur.tl.h, cur.tl.q_row0 + qr, cur.tl.prow0 + qr};
+      }
+      cur.next(p);  // advanced in place (one tile's state live, not two)
+      if (cur.valid) prefetch(cur);
       if (have0 && !reduce_dq(job0, qb - 2)) goto done;
       job0 = job1;
       have0 = have1;
-      {
-        const int qr = (cur.tl.qb0 + cur.i) * 64;
-        job1 = DqJob{cur.tl.h, cur.tl.q_row0 + qr, min(64, cur.tl.Lq - qr), cur.tl.prow0 + qr};
-      }
+      job1 = jnew;
       have1 = true;
-      cur = nx;
       ++qb;
     }
     if (have0 && !reduce_dq(job0, qb - 2)) goto done;

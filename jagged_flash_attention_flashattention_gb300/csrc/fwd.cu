@@ -372,7 +372,8 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
         // Masked columns only where some row of the warp needs them: the
         // peeled tail past the sequence end and the edges of a band.
         const int lo_rel = vis_lo - j * 128, hi_rel = vis_hi - j * 128;
-        if (__any_sync(0xffffffffu, lo_rel > 0 || hi_rel < 127)) {
+        // (without a band the condition is the same for every row: no vote)
+        if (GEN ? __any_sync(0xffffffffu, lo_rel > 0 || hi_rel < 127) : hi_rel < 127) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
