@@ -135,6 +135,22 @@ __device__ __forceinline__ FwdTile decode_tile(const FwdParams &p, int t) {
   return d;
 }
 
+// K/V steps [lo, hi) of the tile (counted from its first loaded K/V tile)
+// that query half x can see. Without a band both halves walk every step;
+// with one, e.g. causal, the first half skips the last tile. A half with
+// rows but no step sees no key (cross attention): its O is 0.
+template <bool GEN>
+__device__ __forceinline__ int2 half_steps(const FwdTile &tl, const FwdParams &p, int x) {
+  const int rows = x ? tl.nrows1 : tl.nrows0;
+  if (rows == 0 || tl.n_kv == 0) return make_int2(0, 0);
+  if (!GEN) return make_int2(0, tl.n_kv);
+  const int64_t first = (int64_t)tl.diag0 + x * 128, last = first + rows - 1;
+  const int64_t lo = p.win_left < 0 ? 0 : max(first - p.win_left, (int64_t)0);
+  const int64_t hi = p.win_right < 0 ? (int64_t)tl.kv_len - 1 : min(last + p.win_right, (int64_t)tl.kv_len - 1);
+  if (hi < lo) return make_int2(0, 0);
+  return make_int2((int)(lo / 128), (int)min(hi / 128 + 1, (int64_t)tl.n_kv));
+}
+
 template <int D, bool BCAST, bool GEN>
 __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
@@ -196,7 +212,8 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
         if (tl.n_kv == 0) continue;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if ((x ? tl.nrows1 : tl.nrows0) == 0) continue;
+          const int2 hs = half_steps<GEN>(tl, p, x);
+          if (hs.y <= hs.x) continue;  // no step: the half's Q is not needed
           if (!mbar_wait(&bars.q_empty[x], ((qph >> x) & 1) ^ 1, ctl, 1)) goto done;
           qph ^= 1u << x;
           mbar_arrive_expect_tx(&bars.q_full[x], C::TILE_BYTES);
@@ -275,22 +292,25 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
         const FwdTile tl = nxt;
         if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
         if (tl.n_kv == 0) continue;
-        const uint32_t has = (tl.nrows0 > 0 ? 1u : 0u) | (tl.nrows1 > 0 ? 2u : 0u);
+        // Each half's steps [lo, hi): every step without a band.
+        const int2 hs0 = half_steps<GEN>(tl, p, 0), hs1 = half_steps<GEN>(tl, p, 1);
+        const uint32_t has = (hs0.y > hs0.x ? 1u : 0u) | (hs1.y > hs1.x ? 2u : 0u);
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           if (!(has >> x & 1)) continue;
           if (!mbar_wait(&bars.q_full[x], (qph >> x) & 1, ctl, 10)) goto done;
           qph ^= 1u << x;
         }
-        // S_0 for both halves (slot of step 0: K_0 only).
+        // S_0 (slot of step 0: K_0 only).
         if (!mbar_wait(&slot_full[slot], sph, ctl, 11)) goto done;
         tc_fence_after();
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if (!(has >> x & 1)) continue;
+          const int2 hs = x ? hs1 : hs0;
+          if (!(has >> x & 1) || hs.x != 0) continue;
           issue_qk(x, slot);
           mma_commit(&bars.s_full[x]);
-          if (tl.n_kv == 1) mma_commit(&bars.q_empty[x]);
+          if (hs.y == 1) mma_commit(&bars.q_empty[x]);
         }
         mma_commit(&slot_empty[slot]);
         if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
@@ -299,23 +319,26 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           const int ps = slot;
           if (!mbar_wait(&slot_full[ps], sph, ctl, 12)) goto done;
           if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
-          const bool more = j < tl.n_kv;
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
             if (!(has >> x & 1)) continue;
-            if (!mbar_wait(&bars.p_ready[x], (pph >> x) & 1, ctl, 14)) goto done;
-            pph ^= 1u << x;
-            if (j == 1) {  // first PV of the tile overwrites O: epilogue must be done with it
-              if (!mbar_wait(&bars.o_free[x], ((oph >> x) & 1) ^ 1, ctl, 15)) goto done;
-              oph ^= 1u << x;
+            const int2 hs = x ? hs1 : hs0;
+            if (j - 1 >= hs.x && j - 1 < hs.y) {  // O += P_{j-1} V_{j-1}
+              if (!mbar_wait(&bars.p_ready[x], (pph >> x) & 1, ctl, 14)) goto done;
+              pph ^= 1u << x;
+              if (j - 1 == hs.x) {  // first PV of the tile overwrites O: epilogue must be done with it
+                if (!mbar_wait(&bars.o_free[x], ((oph >> x) & 1) ^ 1, ctl, 15)) goto done;
+                oph ^= 1u << x;
+              }
+              tc_fence_after();
+              issue_pv(x, ps, j - 1 > hs.x);
+              if (j == hs.y) mma_commit(&bars.o_full[x]);
             }
-            tc_fence_after();
-            issue_pv(x, ps, j > 1);
-            if (j == tl.n_kv) mma_commit(&bars.o_full[x]);
-            if (more) {
+            if (j >= hs.x && j < hs.y) {  // S_j = Q K_j^T
+              if (j == hs.x) tc_fence_after();
               issue_qk(x, ps);
               mma_commit(&bars.s_full[x]);
-              if (j == tl.n_kv - 1) mma_commit(&bars.q_empty[x]);
+              if (j == hs.y - 1) mma_commit(&bars.q_empty[x]);
             }
           }
           mma_commit(&slot_empty[ps]);
@@ -344,7 +367,8 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       const bool row_ok = r < nrows;
       const int64_t orow = tl.out_row0 + x * 128 + r;
       uint4 *optr = reinterpret_cast<uint4 *>(obase + (orow * p.H + tl.h) * D);
-      if (tl.n_kv == 0) {  // rows that see no key (no keys, or outside the band): O = 0, LSE = -inf
+      const int2 hs = half_steps<GEN>(tl, p, x);
+      if (hs.y <= hs.x) {  // rows that see no key (no keys, or outside the band): O = 0, LSE = -inf
         if (row_ok) {
           for (int i = 0; i < D / 8; ++i) optr[i] = make_uint4(0, 0, 0, 0);
           p.lse[tl.lse0 + x * 128 + r] = -INFINITY;
@@ -361,7 +385,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
                              ? tl.kv_len - 1
                              : (int)min((int64_t)dg + p.win_right, (int64_t)tl.kv_len - 1);
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < tl.n_kv; ++j) {
+      for (int j = hs.x; j < hs.y; ++j) {
         if (!mbar_wait(&bars.s_full[x], sph, ctl, 20 + x)) goto done;
         sph ^= 1;
         tc_fence_after();
@@ -393,7 +417,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
             sl2;
         float alpha = 1.f;
-        if (j == 0) {
+        if (j == hs.x) {
           m_run = m_tile;
         } else if (m_tile > m_run + 8.f) {  // also when every earlier key was masked (m_run = -inf)
           alpha = ex2(m_run - m_tile);
@@ -418,7 +442,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           tmem_st16(tS + c * 16, pk);
         }
         l_run = l_run * alpha + ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (j > hs.x && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
