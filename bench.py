@@ -394,6 +394,43 @@ def _fracs(tflops, peak, spec=SPEC_BF16_TFLOPS):
             "frac_of_spec_peak": round(tflops / spec, 4)}
 
 
+def _dynamic_fwd_ms(st, steps, warmup, stream):
+    """Median forward kernel time of a jagged workload under the host static
+    schedule (LPT + zigzag lists) and under device-side dynamic scheduling
+    with both claim orders, each launched the same way: plans built first,
+    W warm-up launches, then K launches queued behind a device-side spin and
+    timed with CUDA events."""
+    import torch
+
+    import jagged_flash_attention_flashattention_gb300 as jfa
+
+    inp, off = st["inp"], st["plan"].offsets
+    H, D = st["H"], st["D"]
+    host = st["plan"].host_offsets
+    static_plan = jfa.Plan(off, H, D, host_offsets=host)
+    runs = {"static": lambda: jfa.jfa_fwd(inp["q"], inp["k"], inp["v"], off, plan=static_plan)}
+    for order in ("device", "lpt"):
+        plan = jfa.DynamicPlan(off, H, D, order=order, host_offsets=host)
+        runs[order] = (lambda pl: lambda: jfa.jfa_fwd_dynamic(inp["q"], inp["k"], inp["v"], off,
+                                                              plan=pl))(plan)
+    res = {}
+    for name, fn in runs.items():
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        _spin(stream)
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        res[name] = statistics.median(a.elapsed_time(b) for a, b in evs)
+    jfa.check_status(static_plan.workspace)
+    return res
+
+
 def _other_configs(args, dev, peaks):
     """Every other workload of the method, each timed like the headline one
     (W warm-up and K timed fwd+bwd steps, CUDA events, median per op), plus the
@@ -420,6 +457,7 @@ def _other_configs(args, dev, peaks):
                                  "the measured copy peak")
         out[name] = rec
         if name == "stress":
+            dyn = _dynamic_fwd_ms(st, steps, warmup, stream)
             nv = _setup(name, 0, dev, zigzag=False)
             _, nf_ms, nb_ms, _ = _time_steps(nv, steps, warmup, stream)
             out["schedule_ab"] = {
@@ -427,7 +465,15 @@ def _other_configs(args, dev, peaks):
                 "fwd_ms_zigzag": round(f_ms, 4), "fwd_ms_naive": round(nf_ms, 4),
                 "bwd_ms_zigzag": round(b_ms, 4), "bwd_ms_naive": round(nb_ms, 4),
                 "fwd_naive_over_zigzag": round(nf_ms / f_ms, 3),
-                "bwd_naive_over_zigzag": round(nb_ms / b_ms, 3)}
+                "bwd_naive_over_zigzag": round(nb_ms / b_ms, 3),
+                # forward kernel alone, each launched the same way: the host
+                # LPT + zigzag lists against device-side dynamic scheduling
+                # (CTAs claim tiles at run time) in two claim orders
+                "fwd_kernel_ms_static_zigzag": round(dyn["static"], 4),
+                "fwd_kernel_ms_dynamic_device_order": round(dyn["device"], 4),
+                "fwd_kernel_ms_dynamic_lpt_order": round(dyn["lpt"], 4),
+                "fwd_dynamic_device_over_static": round(dyn["device"] / dyn["static"], 3),
+                "fwd_dynamic_lpt_over_static": round(dyn["lpt"] / dyn["static"], 3)}
             del nv
         del st
         torch.cuda.synchronize()

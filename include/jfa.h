@@ -187,6 +187,28 @@ jfa_status jfa_fwd(const void *q, const void *k, const void *v, const void *offs
                    const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_sms, void *o,
                    float *lse, void *workspace, size_t ws_bytes, jfa_stream_t stream);
 
+/* Jagged forward with device-side dynamic tile scheduling ("A TLX nagyobb
+ * kontrollt ad a Triton fölött": Cluster Launch Control, i.e. running CTAs
+ * taking work at run time, among the primitives the pages name; reading
+ * used: persistent CTAs claim forward tiles one at a time from a global
+ * atomic counter, instead of walking a fixed per-SM list). Same inputs and
+ * outputs as jfa_fwd, without a band mask. d_tiles NULL: the tiles are
+ * enumerated on the device from the device offsets (sequence by sequence,
+ * head-major, 256 query rows each), so neither host offsets nor a host
+ * schedule are needed; otherwise d_tiles holds n_tiles (b, h, m) int32
+ * triples claimed in that order (e.g. jfa_sched_build with num_sms = 1,
+ * which lists the tiles longest first: greedy LPT). num_ctas: persistent
+ * CTAs (normally jfa_num_sms()). workspace >=
+ * jfa_fwd_dynamic_workspace_size(B) bytes (the status block, the claim
+ * counter and the device tile table); it is not the backward's workspace
+ * and clears no dQ accumulator. */
+jfa_status jfa_fwd_dynamic(const void *q, const void *k, const void *v, const void *offsets,
+                           jfa_index_t idx, int64_t B, int64_t T, int H, int D, float scale,
+                           const int32_t *d_tiles, int64_t n_tiles, int num_ctas, void *o,
+                           float *lse, void *workspace, size_t ws_bytes, jfa_stream_t stream);
+
+size_t jfa_fwd_dynamic_workspace_size(int64_t B);
+
 /* Jagged backward: given dO (device bf16 [T, H, D]) and the forward's O and
  * LSE, writes dQ, dK, dV (device bf16 [T, H, D]):
  *   P = exp(scale * Q K^T - LSE), dV = P^T dO, dP = dO V^T,

@@ -45,7 +45,7 @@ EXPORTS = [
     "jfa_bwd", "jfa_bcastq_fwd", "jfa_bcastq_bwd", "blockdiag_fwd", "blockdiag_bwd",
     "jfa_bwd_noalloc", "jfa_noalloc_check_status", "jfa_selftest_wait_timeout",
     "jfa_sched_size_varlen", "jfa_sched_build_varlen", "jfa_varlen_fwd", "jfa_varlen_bwd",
-    "jfa_varlen_workspace_size",
+    "jfa_varlen_workspace_size", "jfa_fwd_dynamic", "jfa_fwd_dynamic_workspace_size",
 ]
 
 
@@ -94,6 +94,8 @@ def lib():
         "jfa_varlen_bwd": ([P, P, P, P, P, P, P, P, I, I64, I64, I64, I, I, F, I, I, I, P, P, I, P,
                             P, P, P, SZ, P], I),
         "jfa_varlen_workspace_size": ([I64, P, P, I, I, I, I, P], I),
+        "jfa_fwd_dynamic": ([P, P, P, P, I, I64, I64, I, I, F, P, I64, I, P, P, P, SZ, P], I),
+        "jfa_fwd_dynamic_workspace_size": ([I64], SZ),
         "jfa_selftest_wait_timeout": ([P, SZ, ctypes.c_uint64, P], I),
     }
     for name, (args, res) in sig.items():
@@ -375,6 +377,51 @@ def jfa_varlen_bwd(q, k, v, o, lse, do, q_offsets, kv_offsets, scale=None, windo
                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(plan.workspace),
                                 plan.workspace.numel(), _stream()))
     return dq, dk, dv
+
+
+class DynamicPlan:
+    """Workspace (and, for order="lpt", the longest-first tile list) of the
+    forward with device-side dynamic tile scheduling. order="device": tiles
+    enumerated on the device from the device offsets, no host work at all;
+    order="lpt": the host sorts the tiles longest first and the CTAs claim
+    them in that order (greedy LPT)."""
+
+    def __init__(self, offsets, H, D, order="device", host_offsets=None):
+        if order not in ("device", "lpt"):
+            raise ValueError("order must be 'device' or 'lpt'")
+        self.offsets, self.H, self.D, self.order = offsets, H, D, order
+        self.idx = JFA_I64 if offsets.dtype == torch.int64 else JFA_I32
+        self.B = offsets.numel() - 1
+        self.n_ctas = num_sms()
+        self.tiles, self.n_tiles = None, 0
+        if order == "lpt":
+            host = np.asarray(host_offsets) if host_offsets is not None else offsets.cpu().numpy()
+            check_host_offsets(host, offsets.numel())
+            _, tl = schedule(host, H, tile_rows(OP_FWD, D), 1, zigzag=True)
+            self._pinned = torch.from_numpy(np.ascontiguousarray(tl)).pin_memory()
+            self.tiles = self._pinned.to(offsets.device, non_blocking=True)
+            self.n_tiles = tl.shape[0]
+        nbytes = lib().jfa_fwd_dynamic_workspace_size(self.B)
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=offsets.device)
+
+    def check(self):
+        _check(lib().jfa_check_status(_ptr(self.workspace), _stream()))
+
+
+def jfa_fwd_dynamic(q, k, v, offsets, scale=None, plan=None, order="device"):
+    """Jagged forward whose persistent CTAs claim tiles at run time from a
+    global counter (see :class:`DynamicPlan`). Returns (o, lse) like jfa_fwd."""
+    _need_cuda(q, k, v)
+    T, H, D = q.shape
+    plan = plan or DynamicPlan(offsets, H, D, order=order)
+    if (plan.B, plan.H, plan.D) != (offsets.numel() - 1, H, D):
+        raise ValueError("dynamic plan built for another layout")
+    o = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    _check(lib().jfa_fwd_dynamic(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), plan.idx, plan.B, T, H, D,
+                                 _scale(scale, D), _ptr(plan.tiles), plan.n_tiles, plan.n_ctas, _ptr(o),
+                                 _ptr(lse), _ptr(plan.workspace), plan.workspace.numel(), _stream()))
+    return o, lse
 
 
 def jfa_bcastq_fwd(q, k, v, kv_offsets, scale=None, plan=None):

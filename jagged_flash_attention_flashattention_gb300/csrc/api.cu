@@ -112,6 +112,13 @@ jfa_status cuda_status(cudaError_t e, const char *what) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Dynamic tile scheduling: the claim counter sits in the status block, the
+// device tile table ([B+1] int64) right after it.
+constexpr size_t kDynQueueOff = 192;
+size_t dyn_workspace_bytes(int64_t B) {
+  return kStatusBytes + round_up((size_t)(B + 1) * sizeof(int64_t), 256);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ misc
@@ -195,7 +202,8 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *k
                       const void *q_offsets, jfa_index_t idx, int64_t B, int64_t q_rows,
                       int64_t Tk, int64_t Lq, int H, int D, float scale, int win_left,
                       int win_right, const int32_t *sm_ptr, const int32_t *tiles, int num_sms,
-                      void *o, float *lse, void *ws, size_t ws_bytes, cudaStream_t st) {
+                      void *o, float *lse, void *ws, size_t ws_bytes, cudaStream_t st,
+                      int dyn = 0, int64_t n_dyn_tiles = 0) {
   JFA_TRY(check_dims(B, Tk, H, D));
   JFA_TRY(check_dims(B, q_rows, H, D));
   JFA_TRY(check_window(win_left, win_right));
@@ -205,8 +213,11 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *k
   if (num_sms < 1) return fail(JFA_ERR_INVALID_ARG, "num_sms = %d < 1", num_sms);
   JFA_TRY(need_ptr(kv_offsets, "kv_offsets"));
   if (Lq == 0) JFA_TRY(need_ptr(q_offsets, "q_offsets"));
+  if (dyn == 2 && ws_bytes < dyn_workspace_bytes(B))
+    return fail(JFA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, dyn_workspace_bytes(B));
   if (B == 0 || q_rows == 0) return JFA_OK;
-  JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
+  if (dyn == 0) JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
+  if (dyn == 1 && n_dyn_tiles > 0 && !tiles) return fail(JFA_ERR_INVALID_ARG, "tiles is NULL");
   JFA_TRY(need_ptr(q, "q"));
   JFA_TRY(need_ptr(o, "o"));
   JFA_TRY(need_ptr(lse, "lse"));
@@ -241,7 +252,19 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *k
   // A workspace sized for the jagged backward: clear its dQ accumulator here,
   // on the forward kernel's idle warps, instead of in a pass of its own.
   const size_t acc_bytes = (size_t)q_rows * H * D * sizeof(float);
-  if (Lq == 0 && ws_bytes >= kStatusBytes + round_up(acc_bytes, 256)) {
+  if (dyn) {  // the workspace holds the claim counter (and the tile table), no accumulator
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    p.dyn = dyn;
+    p.queue = reinterpret_cast<int *>(wsb + kDynQueueOff);
+    p.n_tiles = n_dyn_tiles;
+    if (dyn == 2) {
+      p.tile_base = reinterpret_cast<int64_t *>(wsb + kStatusBytes);
+      JFA_TRY(cuda_status(launch_fwd_enum(p, const_cast<int64_t *>(p.tile_base), p.queue, st),
+                          "tile enumeration"));
+    } else {
+      JFA_TRY(cuda_status(cudaMemsetAsync(p.queue, 0, sizeof(int), st), "cudaMemsetAsync"));
+    }
+  } else if (Lq == 0 && ws_bytes >= kStatusBytes + round_up(acc_bytes, 256)) {
     p.acc_zero = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kStatusBytes);
     p.acc_n16 = (int64_t)(acc_bytes / 16);
   }
@@ -257,6 +280,21 @@ extern "C" jfa_status jfa_fwd(const void *q, const void *k, const void *v, const
                               jfa_stream_t stream) {
   return fwd_common(q, k, v, offsets, offsets, idx, B, T, T, 0, H, D, scale, -1, -1, d_sm_ptr,
                     d_tiles, num_sms, o, lse, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" jfa_status jfa_fwd_dynamic(const void *q, const void *k, const void *v,
+                                      const void *offsets, jfa_index_t idx, int64_t B, int64_t T,
+                                      int H, int D, float scale, const int32_t *d_tiles,
+                                      int64_t n_tiles, int num_ctas, void *o, float *lse,
+                                      void *workspace, size_t ws_bytes, jfa_stream_t stream) {
+  if (n_tiles < 0 || n_tiles >= (int64_t(1) << 31) / 3) return fail(JFA_ERR_INVALID_ARG, "bad n_tiles");
+  return fwd_common(q, k, v, offsets, offsets, idx, B, T, T, 0, H, D, scale, -1, -1, nullptr,
+                    d_tiles, num_ctas, o, lse, workspace, ws_bytes, (cudaStream_t)stream,
+                    d_tiles ? 1 : 2, n_tiles);
+}
+
+extern "C" size_t jfa_fwd_dynamic_workspace_size(int64_t B) {
+  return B < 0 ? kStatusBytes : dyn_workspace_bytes(B);
 }
 
 extern "C" jfa_status jfa_varlen_fwd(const void *q, const void *k, const void *v,

@@ -65,9 +65,13 @@ struct FwdCfg {
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, 0, 1);
 };
 
+constexpr int kTileRing = 8;  // dynamic scheduling: tile indices published ahead
+
 struct FwdBars {
   uint64_t q_full[2], q_empty[2], s_full[2], p_ready[2], o_full[2], o_free[2];
   uint64_t drain;
+  uint64_t tile_full[kTileRing], tile_empty[kTileRing];  // dynamic scheduling ring
+  int4 ring[kTileRing];  // (b, h, m, 1) of a claimed tile, or (-1, 0, 0, 0): no more
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -86,14 +90,33 @@ __device__ __forceinline__ int64_t load_off(const void *off, int idx64, int i) {
   return idx64 ? static_cast<const int64_t *>(off)[i] : (int64_t) static_cast<const int *>(off)[i];
 }
 
+// (b, h, m) of tile index t: from the list p.tiles, or, dynamic scheduling
+// over the device enumeration (p.dyn == 2), from tile_base.
+template <bool DYN>
+__device__ __forceinline__ int4 tile_bhm(const FwdParams &p, int t) {
+  if (DYN && p.dyn == 2) {  // sequence of tile t: the last b with tile_base[b] <= t
+    int64_t lo = 0, hi = p.B;
+    while (hi - lo > 1) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (p.tile_base[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int64_t s0 = min(max(load_off(p.offsets, p.idx64, (int)lo), (int64_t)0), p.T);
+    const int64_t e0 = min(max(load_off(p.offsets, p.idx64, (int)lo + 1), s0), p.T);
+    const int nm = max(1, (int)((e0 - s0 + 255) / 256));
+    const int r = (int)(t - p.tile_base[lo]);
+    return make_int4((int)lo, r / nm, r % nm, 1);
+  }
+  return make_int4(p.tiles[3 * t], p.tiles[3 * t + 1], p.tiles[3 * t + 2], 1);
+}
+
 // GEN: the band mask is compiled in (jfa_varlen_fwd with a window); without
 // it every row sees all of its sequence's keys.
 template <bool BCAST, bool GEN>
-__device__ __forceinline__ FwdTile decode_tile(const FwdParams &p, int t) {
+__device__ __forceinline__ FwdTile decode_bhm(const FwdParams &p, int4 bhm) {
   FwdTile d;
-  d.b = p.tiles[3 * t];
-  d.h = p.tiles[3 * t + 1];
-  const int m = p.tiles[3 * t + 2];
+  d.b = bhm.x;
+  d.h = bhm.y;
+  const int m = bhm.z;
   // A tile outside this batch (a schedule built for another one) is empty,
   // and sequence bounds are clamped to [0, T]: no row past the tensors is
   // read or written whatever the tile list or the offsets hold.
@@ -151,7 +174,12 @@ __device__ __forceinline__ int2 half_steps(const FwdTile &tl, const FwdParams &p
   return make_int2((int)(lo / 128), (int)min(hi / 128 + 1, (int64_t)tl.n_kv));
 }
 
-template <int D, bool BCAST, bool GEN>
+template <bool BCAST, bool GEN, bool DYN>
+__device__ __forceinline__ FwdTile decode_tile(const FwdParams &p, int t) {
+  return decode_bhm<BCAST, GEN>(p, tile_bhm<DYN>(p, t));
+}
+
+template <int D, bool BCAST, bool GEN, bool DYN>
 __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -178,6 +206,10 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       mbar_init(&slot_full[s], 1);
       mbar_init(&slot_empty[s], 1);
     }
+    for (int s = 0; s < kTileRing; ++s) {
+      mbar_init(&bars.tile_full[s], 1);
+      mbar_init(&bars.tile_empty[s], 9);  // the MMA thread and the eight softmax warps
+    }
     bars.abort_flag = 0;
     fence_mbar_init();
   }
@@ -193,8 +225,27 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
   const uint32_t tmem = bars.tmem_base;
 
   const WaitCtl ctl{p.status, &bars.abort_flag, p.timeout_ns};
-  const int tbeg = p.sm_ptr[blockIdx.x];
-  const int tend = p.sm_ptr[blockIdx.x + 1];
+  // Static scheduling: this CTA's tiles tbeg .. tend-1 of the CSR lists.
+  // Dynamic: ordinal k of this CTA's tiles is the k-th index the producer
+  // claimed from the global queue and published in the shared ring.
+  const int tbeg = DYN ? 0 : p.sm_ptr[blockIdx.x];
+  const int tend = DYN ? 0 : p.sm_ptr[blockIdx.x + 1];
+  // Dynamic: (b, h, m) of this CTA's tile k for the MMA thread and the
+  // softmax warps (b = -1: no more), as the producer resolved it.
+  // `mask`: the lanes that run the role (the whole warp in the softmax warps,
+  // lane 0 alone in the MMA warp); lane 0's entry is broadcast to them.
+  auto tile_at = [&](int k, unsigned mask) -> int4 {
+    int4 v = make_int4(-1, 0, 0, 0);
+    if (lane == 0) {
+      const int s = k % kTileRing;
+      if (mbar_wait(&bars.tile_full[s], (k / kTileRing) & 1, ctl, 4)) {
+        const volatile int *e = reinterpret_cast<const volatile int *>(&bars.ring[s]);  // (the wait acquires)
+        v = make_int4(e[0], e[1], e[2], 0);
+        mbar_arrive(&bars.tile_empty[s]);
+      }
+    }
+    return make_int4(__shfl_sync(mask, v.x, 0), __shfl_sync(mask, v.y, 0), __shfl_sync(mask, v.z, 0), 0);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -202,13 +253,40 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       uint32_t qph = 0;
       int slot = 0;
       uint32_t sph = 0;
+      // Dynamic scheduling: claim tile indices from the global queue and
+      // publish them two ordinals ahead of this thread's loads (the other
+      // roles read ordinal k + 1 when they start ordinal k).
+      int pub = 0;
+      bool ended = false;
+      const int64_t n_dyn = !DYN ? 0 : (p.dyn == 2 ? p.tile_base[p.B] : p.n_tiles);
+      auto produce_at = [&](int k) -> int4 {
+        while (pub <= k + 1 && !ended) {
+          const int s = pub % kTileRing;
+          if (!mbar_wait(&bars.tile_empty[s], ((pub / kTileRing) & 1) ^ 1, ctl, 3))
+            return make_int4(-1, 0, 0, 0);
+          const int g = atomicAdd(p.queue, 1);
+          ended = g >= n_dyn;
+          bars.ring[s] = ended ? make_int4(-1, 0, 0, 0) : tile_bhm<DYN>(p, g);
+          mbar_arrive(&bars.tile_full[s]);  // (release: the entry is visible to the waiters)
+          ++pub;
+        }
+        return k < pub ? bars.ring[k % kTileRing] : make_int4(-1, 0, 0, 0);
+      };
       // The next tile is decoded one tile ahead (its index loads are off the
       // critical path at the tile switch).
+      // (Dynamic: t counts this CTA's tiles and id is the index of tile t.)
+      int4 bhm = DYN ? produce_at(0) : make_int4(-1, 0, 0, 0);
       FwdTile nxt{};
-      if (tbeg < tend) nxt = decode_tile<BCAST, GEN>(p, tbeg);
-      for (int t = tbeg; t < tend; ++t) {
+      if (DYN ? bhm.x >= 0 : tbeg < tend)
+        nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN>(p, tbeg);
+      for (int t = tbeg; DYN ? bhm.x >= 0 : t < tend; ++t) {
         const FwdTile tl = nxt;
-        if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
+        if (DYN) {
+          bhm = produce_at(t + 1);
+          if (bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
+        } else if (t + 1 < tend) {
+          nxt = decode_tile<BCAST, GEN, DYN>(p, t + 1);
+        }
         if (tl.n_kv == 0) continue;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
@@ -286,11 +364,18 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       };
       // The next tile is decoded one tile ahead (its index loads are off the
       // critical path at the tile switch).
+      int4 bhm = DYN ? tile_at(0, 1u) : make_int4(-1, 0, 0, 0);
       FwdTile nxt{};
-      if (tbeg < tend) nxt = decode_tile<BCAST, GEN>(p, tbeg);
-      for (int t = tbeg; t < tend; ++t) {
+      if (DYN ? bhm.x >= 0 : tbeg < tend)
+        nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN>(p, tbeg);
+      for (int t = tbeg; DYN ? bhm.x >= 0 : t < tend; ++t) {
         const FwdTile tl = nxt;
-        if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
+        if (DYN) {
+          bhm = tile_at(t + 1, 1u);
+          if (bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
+        } else if (t + 1 < tend) {
+          nxt = decode_tile<BCAST, GEN, DYN>(p, t + 1);
+        }
         if (tl.n_kv == 0) continue;
         // Each half's steps [lo, hi): every step without a band.
         const int2 hs0 = half_steps<GEN>(tl, p, 0), hs1 = half_steps<GEN>(tl, p, 1);
@@ -357,11 +442,18 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
     __nv_bfloat16 *obase = static_cast<__nv_bfloat16 *>(p.o);
     // The next tile is decoded one tile ahead (its index loads are off the
     // critical path at the tile switch).
+    int4 bhm = DYN ? tile_at(0, 0xffffffffu) : make_int4(-1, 0, 0, 0);
     FwdTile nxt{};
-    if (tbeg < tend) nxt = decode_tile<BCAST, GEN>(p, tbeg);
-    for (int t = tbeg; t < tend; ++t) {
+    if (DYN ? bhm.x >= 0 : tbeg < tend)
+      nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN>(p, tbeg);
+    for (int t = tbeg; DYN ? bhm.x >= 0 : t < tend; ++t) {
       const FwdTile tl = nxt;
-      if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
+      if (DYN) {
+        bhm = tile_at(t + 1, 0xffffffffu);
+        if (bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
+      } else if (t + 1 < tend) {
+        nxt = decode_tile<BCAST, GEN, DYN>(p, t + 1);
+      }
       const int nrows = x ? tl.nrows1 : tl.nrows0;
       if (nrows == 0) continue;
       const bool row_ok = r < nrows;
@@ -507,9 +599,9 @@ done:
   }
 }
 
-template <int D, bool BCAST, bool GEN>
+template <int D, bool BCAST, bool GEN, bool DYN>
 cudaError_t launch_t(const FwdParams &p, int num_sms, cudaStream_t st) {
-  auto kern = jfa_fwd_kernel<D, BCAST, GEN>;
+  auto kern = jfa_fwd_kernel<D, BCAST, GEN, DYN>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
@@ -517,17 +609,61 @@ cudaError_t launch_t(const FwdParams &p, int num_sms, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Per-sequence forward tile counts (H * ceil(L / 256)) as exclusive prefix
+// sums, and the queue counter zeroed.
+__global__ void __launch_bounds__(1024) fwd_enum_kernel(const FwdParams p, int64_t *tile_base,
+                                                        int *queue) {
+  __shared__ int64_t s_n[1024];
+  const int t = threadIdx.x;
+  const int64_t chunk = (p.B + 1023) / 1024;
+  const int64_t b0 = min(p.B, (int64_t)t * chunk), b1 = min(p.B, b0 + chunk);
+  auto count = [&](int64_t b) {
+    const int64_t s0 = min(max(load_off(p.offsets, p.idx64, (int)b), (int64_t)0), p.T);
+    const int64_t e0 = min(max(load_off(p.offsets, p.idx64, (int)b + 1), s0), p.T);
+    return (int64_t)p.H * ((e0 - s0 + 255) / 256);
+  };
+  int64_t n = 0;
+  for (int64_t b = b0; b < b1; ++b) n += count(b);
+  s_n[t] = n;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int64_t a = t >= off ? s_n[t - off] : 0;
+    __syncthreads();
+    s_n[t] += a;
+    __syncthreads();
+  }
+  int64_t base = s_n[t] - n;
+  for (int64_t b = b0; b < b1; ++b) {
+    tile_base[b] = base;
+    base += count(b);
+  }
+  if (t == 1023) tile_base[p.B] = s_n[1023];
+  if (t == 0) *queue = 0;
+}
+
 }  // namespace
 
 cudaError_t launch_fwd(const FwdParams &p, int D, int num_sms, cudaStream_t st) {
   const bool bcast = p.Lq > 0;
   const bool gen = !bcast && (p.win_left >= 0 || p.win_right >= 0);
-  if (D == 128) {
-    if (bcast) return launch_t<128, true, false>(p, num_sms, st);
-    return gen ? launch_t<128, false, true>(p, num_sms, st) : launch_t<128, false, false>(p, num_sms, st);
+  if (p.dyn) {  // dynamic scheduling: jagged without a band only
+    if (bcast || gen) return cudaErrorNotSupported;
+    return D == 128 ? launch_t<128, false, false, true>(p, num_sms, st)
+                    : launch_t<64, false, false, true>(p, num_sms, st);
   }
-  if (bcast) return launch_t<64, true, false>(p, num_sms, st);
-  return gen ? launch_t<64, false, true>(p, num_sms, st) : launch_t<64, false, false>(p, num_sms, st);
+  if (D == 128) {
+    if (bcast) return launch_t<128, true, false, false>(p, num_sms, st);
+    return gen ? launch_t<128, false, true, false>(p, num_sms, st)
+               : launch_t<128, false, false, false>(p, num_sms, st);
+  }
+  if (bcast) return launch_t<64, true, false, false>(p, num_sms, st);
+  return gen ? launch_t<64, false, true, false>(p, num_sms, st)
+             : launch_t<64, false, false, false>(p, num_sms, st);
+}
+
+cudaError_t launch_fwd_enum(const FwdParams &p, int64_t *tile_base, int *queue, cudaStream_t st) {
+  fwd_enum_kernel<<<1, 1024, 0, st>>>(p, tile_base, queue);
+  return cudaGetLastError();
 }
 
 }  // namespace jfa

@@ -36,6 +36,15 @@ struct FwdParams {
   // status block, so the backward that follows skips its own clearing pass.
   float *acc_zero;
   int64_t acc_n16;
+  // Dynamic tile scheduling (jagged, no band): dyn = 1 takes tiles from the
+  // list `tiles` (n_tiles entries, in order), dyn = 2 from the device
+  // enumeration tile_base[B+1] (tiles before sequence b, H * ceil(L_b / 256)
+  // each, head-major within a sequence); CTAs claim the next tile with an
+  // atomic add on *queue, which starts at zero.
+  int dyn;
+  int *queue;
+  const int64_t *tile_base;
+  int64_t n_tiles;
 };
 
 // Byte offset, in the status block, of the uint64 count of accumulator bytes
@@ -43,6 +52,11 @@ struct FwdParams {
 constexpr size_t kAccZeroedOff = 128;
 
 cudaError_t launch_fwd(const FwdParams &p, int D, int num_sms, cudaStream_t st);
+
+// Device enumeration of the forward tiles for dynamic scheduling: writes
+// tile_base[0..B] from the device offsets (clamped like the kernels) and
+// zeroes *queue. One CTA.
+cudaError_t launch_fwd_enum(const FwdParams &p, int64_t *tile_base, int *queue, cudaStream_t st);
 
 // Backward kernel (jagged and broadcast-Q). Tiles are 128 key rows; the
 // kernel walks the sequence's query rows in blocks of 64.

@@ -262,3 +262,15 @@ def test_varlen_entry_points_reject_bad_windows_on_host(L):
     code = L.jfa_varlen_bwd(p, p, p, p, p, p, p, p, 0, 1, 10, 10, 2, 64, 0.1, 0, -5, 0, p, p, 1, p, p,
                             p, p, 1 << 20, _null())
     assert code == 1 and b"window" in L.jfa_last_error()
+
+
+def test_fwd_dynamic_rejects_bad_arguments(L):
+    dummy = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(dummy, ctypes.c_void_p)
+    need = L.jfa_fwd_dynamic_workspace_size(10)
+    assert need == 256 + 256
+    # device enumeration needs the tile table in the workspace
+    assert L.jfa_fwd_dynamic(p, p, p, p, 0, 10, 100, 2, 64, 0.1, _null(), 0, 4, p, p, p, 256,
+                             _null()) == 3
+    assert L.jfa_fwd_dynamic(p, p, p, p, 0, 10, 100, 2, 64, 0.1, p, -1, 4, p, p, p, need,
+                             _null()) == 1
