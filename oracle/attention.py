@@ -37,6 +37,18 @@ per sequence and per head, with no blocking, fusion or online rescaling:
   64-token blocks and each query block attends only to its own key/value
   block, i.e. the definition above applied to every block independently.
 
+* rotary block-diagonal attention ([TLX-BA] section 1: block attention with
+  rotary embeddings fused in, forward and backward). The pages do not write
+  the rotation out; the reading used is the usual "rotate half" form: with
+  tables cos, sin of shape [L, D/2] indexed by a token's position in its
+  sequence, a row x of q or k becomes
+
+      x_r[i]       = x[i] cos[i] - x[i + D/2] sin[i]
+      x_r[i + D/2] = x[i + D/2] cos[i] + x[i] sin[i]      (i < D/2),
+
+  attention runs on (q_r, k_r, v), and the gradients of q and k are those of
+  q_r and k_r rotated back by the transposed rotation (rotation by -angle).
+
 * masked and cross (varlen) attention ([JFA-GEM] "Impacto en el desarrollo
   de modelos generativos": causal, sliding-window and block-sparse masks as
   the natural extensions of the jagged kernels; "Optimización del proceso de
@@ -312,3 +324,37 @@ def blockdiag_bwd(q, k, v, do, scale, block=BLOCK):
         dk[:, :, h] = scale * np.einsum("nij,nid->njd", dS, Q)
     shape = (B, L, H, D)
     return dq.reshape(shape), dk.reshape(shape), dv.reshape(shape)
+
+
+def rope(x, cos, sin):
+    """Rotary embedding of x [B, L, H, D] with tables cos, sin [L, D/2]
+    (position = index along L), "rotate half" form (module docstring)."""
+    x = _f64(x)
+    h = x.shape[-1] // 2
+    c = _f64(cos)[None, :, None, :]
+    s = _f64(sin)[None, :, None, :]
+    lo, hi = x[..., :h], x[..., h:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+
+
+def rope_transpose(g, cos, sin):
+    """The transposed rotation (rotation by -angle): maps the gradient of a
+    rotated tensor to the gradient of the unrotated one."""
+    g = _f64(g)
+    h = g.shape[-1] // 2
+    c = _f64(cos)[None, :, None, :]
+    s = _f64(sin)[None, :, None, :]
+    lo, hi = g[..., :h], g[..., h:]
+    return np.concatenate([lo * c + hi * s, hi * c - lo * s], axis=-1)
+
+
+def blockdiag_rotary_fwd(q, k, v, cos, sin, scale, block=BLOCK):
+    """Block-diagonal attention on rotated q and k. Returns O [B, L, H, D]."""
+    return blockdiag_fwd(rope(q, cos, sin), rope(k, cos, sin), v, scale, block)
+
+
+def blockdiag_rotary_bwd(q, k, v, do, cos, sin, scale, block=BLOCK):
+    """Backward of :func:`blockdiag_rotary_fwd` with respect to the
+    unrotated q, k and v. Returns dQ, dK, dV [B, L, H, D]."""
+    dqr, dkr, dv = blockdiag_bwd(rope(q, cos, sin), rope(k, cos, sin), v, do, scale, block)
+    return rope_transpose(dqr, cos, sin), rope_transpose(dkr, cos, sin), dv
