@@ -330,12 +330,27 @@ def _setup(name, rank, dev, seqs=0, zigzag=True):
         st["fwd_bytes"] = 4 * B * L * H * D * 2
         st["bwd_bytes"] = 7 * B * L * H * D * 2
         st["desc"] = "blockdiag: B=%d, L=%d, H=%d, D=%d, 64-token blocks" % (B, L, H, D)
+        if cfg.get("rotary"):
+            # The forward rotates q and k in the kernel and writes the rotated
+            # rows (a rotary layer's saved output: +2 tiles of writes); the
+            # backward reads those and rotates dQ, dK back in its epilogue.
+            # The fp32 tables (2 x L x D/2 x 4 bytes) stay in L2.
+            cos, sin = W.rotary_tables(L, D, device=dev)
+            st["fwd_bytes"] = 6 * B * L * H * D * 2
+            st["desc"] += ", rotary fused (fp32 tables [L, D/2]; forward writes q_rot, k_rot)"
 
-        def fwd():
-            jfa.blockdiag_fwd(inp["q"], inp["k"], inp["v"])
+            def fwd():
+                st["o"], st["q_rot"], st["k_rot"] = jfa.blockdiag_rotary_fwd(
+                    inp["q"], inp["k"], inp["v"], cos, sin, return_rotated=True)
 
-        def bwd():
-            jfa.blockdiag_bwd(inp["q"], inp["k"], inp["v"], inp["do"])
+            def bwd():
+                jfa.blockdiag_rotary_bwd(st["q_rot"], st["k_rot"], inp["v"], inp["do"], cos, sin)
+        else:
+            def fwd():
+                jfa.blockdiag_fwd(inp["q"], inp["k"], inp["v"])
+
+            def bwd():
+                jfa.blockdiag_bwd(inp["q"], inp["k"], inp["v"], inp["do"])
 
         st["check"] = lambda: jfa.check_status(device=dev)
     st["inp"] = inp
@@ -441,7 +456,8 @@ def _other_configs(args, dev, peaks):
     stream = torch.cuda.current_stream()
     steps, warmup = max(3, min(args.steps, 10)), 3
     out = {}
-    for name in ("stress", "bcast", "blockdiag", "blockdiag64", "gem_causal", "gem_det"):
+    for name in ("stress", "bcast", "blockdiag", "blockdiag64", "blockdiag_rotary", "gem_causal",
+                 "gem_det"):
         st = _setup(name, 0, dev)
         _, f_ms, b_ms, _ = _time_steps(st, steps, warmup, stream)
         ff, bf = st["fwd_flops"], st["bwd_flops"]
@@ -750,7 +766,7 @@ def main():
                          "a small profiling case")
     ap.add_argument("--config", default="gem",
                     choices=["gem", "stress", "bcast", "blockdiag", "blockdiag64", "tiny",
-                             "gem_causal", "gem_det"])
+                             "gem_causal", "gem_det", "blockdiag_rotary"])
     ap.add_argument("--schedule", default="zigzag", choices=["zigzag", "naive"],
                     help="tile order: host LPT + zigzag deal, or the unsorted round-robin deal")
     ap.add_argument("--no-configs", action="store_true",

@@ -363,6 +363,39 @@ jfa_status blockdiag_bwd(const void *q, const void *k, const void *v, const void
                          int64_t B, int64_t L, int H, int D, float scale, void *dq, void *dk,
                          void *dv, void *workspace, size_t ws_bytes, jfa_stream_t stream);
 
+/* Block-diagonal attention with rotary embeddings fused in ("TLX Block
+ * Attention", section 1: block attention with rotary embeddings, whose
+ * combined attention-and-rotary backward the page reports about 3.5 times
+ * faster than FA2 when the rotary is fused into the attention epilogue). The
+ * page does not write the rotation out; the reading used is the "rotate
+ * half" form: cos_t, sin_t are device fp32 tables [L, D/2] indexed by a
+ * token's position in its sequence (row index mod L), and each row x of q
+ * and k is rotated,
+ *   x_r[i] = x[i] cos[i] - x[i + D/2] sin[i],
+ *   x_r[i + D/2] = x[i + D/2] cos[i] + x[i] sin[i],   i < D/2.
+ * Forward: q and k (unrotated) are rotated inside the kernel on their way
+ * from memory to the products (rounded to bf16 like a separate rotary pass);
+ * o = block-diagonal attention of (q_r, k_r, v). When q_rot and k_rot
+ * (device bf16 [B, L, H, D], 16-byte aligned) are given, the rotated rows are
+ * also written there, as a rotary layer's output saved for its backward;
+ * both NULL writes nothing, one NULL is JFA_ERR_INVALID_ARG.
+ * Backward (the rotary backward fused into the attention epilogue): takes the
+ * rotated q_rot, k_rot (as written by the forward), v and dout; dq, dk are
+ * the gradients with respect to the unrotated q, k (the gradients of q_rot,
+ * k_rot rotated back by the transposed rotation in the epilogue); dv as for
+ * blockdiag_bwd. Other arguments and errors as for blockdiag_fwd /
+ * blockdiag_bwd; NULL or misaligned tables return JFA_ERR_INVALID_ARG. */
+jfa_status blockdiag_rotary_fwd(const void *q, const void *k, const void *v, const float *cos_t,
+                                const float *sin_t, int64_t B, int64_t L, int H, int D,
+                                float scale, void *o, void *q_rot, void *k_rot, void *workspace,
+                                size_t ws_bytes, jfa_stream_t stream);
+
+jfa_status blockdiag_rotary_bwd(const void *q_rot, const void *k_rot, const void *v,
+                                const void *dout, const float *cos_t, const float *sin_t,
+                                int64_t B, int64_t L, int H, int D, float scale, void *dq,
+                                void *dk, void *dv, void *workspace, size_t ws_bytes,
+                                jfa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

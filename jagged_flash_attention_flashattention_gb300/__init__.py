@@ -46,6 +46,7 @@ EXPORTS = [
     "jfa_bwd_noalloc", "jfa_noalloc_check_status", "jfa_selftest_wait_timeout",
     "jfa_sched_size_varlen", "jfa_sched_build_varlen", "jfa_varlen_fwd", "jfa_varlen_bwd",
     "jfa_varlen_workspace_size", "jfa_fwd_dynamic", "jfa_fwd_dynamic_workspace_size",
+    "blockdiag_rotary_fwd", "blockdiag_rotary_bwd",
 ]
 
 
@@ -96,6 +97,8 @@ def lib():
         "jfa_varlen_workspace_size": ([I64, P, P, I, I, I, I, P], I),
         "jfa_fwd_dynamic": ([P, P, P, P, I, I64, I64, I, I, F, P, I64, I, P, P, P, SZ, P], I),
         "jfa_fwd_dynamic_workspace_size": ([I64], SZ),
+        "blockdiag_rotary_fwd": ([P, P, P, P, P, I64, I64, I, I, F, P, P, P, P, SZ, P], I),
+        "blockdiag_rotary_bwd": ([P, P, P, P, P, P, I64, I64, I, I, F, P, P, P, P, SZ, P], I),
         "jfa_selftest_wait_timeout": ([P, SZ, ctypes.c_uint64, P], I),
     }
     for name, (args, res) in sig.items():
@@ -490,6 +493,48 @@ def blockdiag_bwd(q, k, v, do, scale=None):
     ws = _small_workspace(q.device)
     _check(lib().blockdiag_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, L, H, D, _scale(scale, D),
                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream()))
+    return dq, dk, dv
+
+
+def _check_tables(cos, sin, L, D):
+    for t in (cos, sin):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.float32 and
+                tuple(t.shape) == (L, D // 2)):
+            raise ValueError("rotary tables must be contiguous fp32 CUDA tensors [L, D/2]")
+
+
+def blockdiag_rotary_fwd(q, k, v, cos, sin, scale=None, return_rotated=False):
+    """64-token block-diagonal forward with q and k rotated in the kernel by the
+    rotary tables cos, sin [L, D/2] (fp32). Returns o, or (o, q_rot, k_rot)
+    with the rotated q and k the kernel wrote (bf16), which the backward takes."""
+    _need_cuda(q, k, v)
+    B, L, H, D = q.shape
+    _check_tables(cos, sin, L, D)
+    o = torch.empty_like(q)
+    q_rot = torch.empty_like(q) if return_rotated else None
+    k_rot = torch.empty_like(k) if return_rotated else None
+    ws = _small_workspace(q.device)
+    _check(lib().blockdiag_rotary_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cos), _ptr(sin), B, L, H, D,
+                                      _scale(scale, D), _ptr(o),
+                                      _ptr(q_rot) if return_rotated else None,
+                                      _ptr(k_rot) if return_rotated else None,
+                                      _ptr(ws), ws.numel(), _stream()))
+    return (o, q_rot, k_rot) if return_rotated else o
+
+
+def blockdiag_rotary_bwd(q_rot, k_rot, v, do, cos, sin, scale=None):
+    """Backward of :func:`blockdiag_rotary_fwd` with the rotary backward fused
+    into the epilogue: from the rotated q_rot, k_rot (as the forward writes
+    them), v and do, returns (dq, dk, dv) with respect to the unrotated q, k
+    and v."""
+    _need_cuda(q_rot, k_rot, v, do)
+    B, L, H, D = q_rot.shape
+    _check_tables(cos, sin, L, D)
+    dq, dk, dv = torch.empty_like(q_rot), torch.empty_like(k_rot), torch.empty_like(v)
+    ws = _small_workspace(q_rot.device)
+    _check(lib().blockdiag_rotary_bwd(_ptr(q_rot), _ptr(k_rot), _ptr(v), _ptr(do), _ptr(cos),
+                                      _ptr(sin), B, L, H, D, _scale(scale, D), _ptr(dq), _ptr(dk),
+                                      _ptr(dv), _ptr(ws), ws.numel(), _stream()))
     return dq, dk, dv
 
 

@@ -516,11 +516,23 @@ namespace {
 jfa_status blockdiag_common(const void *q, const void *k, const void *v, const void *dout,
                             int64_t B, int64_t L, int H, int D, float scale, void *o, void *dq,
                             void *dk, void *dv, void *ws, size_t ws_bytes, bool bwd,
-                            cudaStream_t st) {
+                            cudaStream_t st, const float *cos_t = nullptr,
+                            const float *sin_t = nullptr, bool rotary = false,
+                            void *q_rot = nullptr, void *k_rot = nullptr) {
   JFA_TRY(check_dims(B, B * L, H, D));
   if (L < 0 || L % 64 != 0) return fail(JFA_ERR_INVALID_ARG, "L = %lld is not a multiple of 64", (long long)L);
   if (!(scale > 0.f)) return fail(JFA_ERR_INVALID_ARG, "scale must be > 0");
   JFA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
+  if (rotary) {
+    JFA_TRY(need_ptr(cos_t, "cos"));
+    JFA_TRY(need_ptr(sin_t, "sin"));
+    if ((q_rot == nullptr) != (k_rot == nullptr))
+      return fail(JFA_ERR_INVALID_ARG, "q_rot and k_rot must both be given or both be NULL");
+    if (q_rot != nullptr) {
+      JFA_TRY(need_ptr(q_rot, "q_rot"));
+      JFA_TRY(need_ptr(k_rot, "k_rot"));
+    }
+  }
   if (B == 0 || L == 0) return JFA_OK;
   JFA_TRY(need_ptr(q, "q"));
   JFA_TRY(need_ptr(k, "k"));
@@ -545,6 +557,11 @@ jfa_status blockdiag_common(const void *q, const void *k, const void *v, const v
   p.dk = dk;
   p.dv = dv;
   p.rows = rows;
+  p.L = L;
+  p.cos_t = rotary ? cos_t : nullptr;
+  p.sin_t = rotary ? sin_t : nullptr;
+  p.q_rot = rotary ? q_rot : nullptr;
+  p.k_rot = rotary ? k_rot : nullptr;
   p.H = H;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -573,4 +590,23 @@ extern "C" jfa_status blockdiag_bwd(const void *q, const void *k, const void *v,
                                     size_t ws_bytes, jfa_stream_t stream) {
   return blockdiag_common(q, k, v, dout, B, L, H, D, scale, nullptr, dq, dk, dv, workspace,
                           ws_bytes, true, (cudaStream_t)stream);
+}
+
+extern "C" jfa_status blockdiag_rotary_fwd(const void *q, const void *k, const void *v,
+                                           const float *cos_t, const float *sin_t, int64_t B,
+                                           int64_t L, int H, int D, float scale, void *o,
+                                           void *q_rot, void *k_rot, void *workspace,
+                                           size_t ws_bytes, jfa_stream_t stream) {
+  return blockdiag_common(q, k, v, nullptr, B, L, H, D, scale, o, nullptr, nullptr, nullptr,
+                          workspace, ws_bytes, false, (cudaStream_t)stream, cos_t, sin_t, true,
+                          q_rot, k_rot);
+}
+
+extern "C" jfa_status blockdiag_rotary_bwd(const void *q_rot, const void *k_rot, const void *v,
+                                           const void *dout, const float *cos_t,
+                                           const float *sin_t, int64_t B, int64_t L, int H, int D,
+                                           float scale, void *dq, void *dk, void *dv,
+                                           void *workspace, size_t ws_bytes, jfa_stream_t stream) {
+  return blockdiag_common(q_rot, k_rot, v, dout, B, L, H, D, scale, nullptr, dq, dk, dv, workspace,
+                          ws_bytes, true, (cudaStream_t)stream, cos_t, sin_t, true);
 }

@@ -55,6 +55,86 @@ __device__ __forceinline__ Unit unit_of(int u, int H, int64_t rows) {
   return x;
 }
 
+// Rotary variant ("TLX Block Attention", section 1: block attention with
+// rotary embeddings fused in). Reading used: the "rotate half" rotation by
+// fp32 tables cos, sin [L, D/2] at each row's position in its sequence,
+//   x_r[i] = x[i] cos[i] - x[i + D/2] sin[i],  x_r[i + D/2] = x[i + D/2] cos[i] + x[i] sin[i].
+// The forward rotates the q and k tiles in shared memory as soon as they land
+// and before any product reads them (rounded to bf16, as a separate rotary
+// pass writing bf16 would), and can write the rotated rows out for the
+// backward. The backward reads the rotated q and k and applies the rotary
+// backward in its epilogue: dQ and dK rotated back by the transposed rotation.
+// An item is one row's 8-pair chunk j: columns 8j..8j+7 and their partners
+// 8j + D/2.. . Items it = base + u * nthr (u < U) of a 128-row tile; tab holds
+// their cos and sin values.
+template <int D, int U>
+__device__ __forceinline__ void rot_load(const BlockdiagParams &p, int64_t row0, int nrows, int base,
+                                         int nthr, float4 (&tab)[U][4]) {
+  constexpr int NC = D / 16;  // items per row
+  const int pos0 = (int)(row0 % p.L);
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int it = base + u * nthr, r = it / NC, j = it - r * NC;
+    if (it < 128 * NC && r < nrows) {
+      int pos = pos0 + r;
+      while (pos >= p.L) pos -= (int)p.L;
+      const float4 *cp = reinterpret_cast<const float4 *>(p.cos_t + (int64_t)pos * (D / 2) + j * 8);
+      const float4 *sp = reinterpret_cast<const float4 *>(p.sin_t + (int64_t)pos * (D / 2) + j * 8);
+      tab[u][0] = __ldg(cp);
+      tab[u][1] = __ldg(cp + 1);
+      tab[u][2] = __ldg(sp);
+      tab[u][3] = __ldg(sp + 1);
+    }
+  }
+}
+
+// Rotates the items in shared memory and, when qo is not null, also writes
+// them to q_rot and k_rot (qo, ko: row 0 of the tile at this head; rows are
+// rstride elements apart).
+template <int D, int U>
+__device__ __forceinline__ void rot_apply(uint8_t *qt, uint8_t *kt, int nrows, int base, int nthr,
+                                          const float4 (&tab)[U][4], __nv_bfloat16 *qo,
+                                          __nv_bfloat16 *ko, int64_t rstride) {
+  constexpr int NC = D / 16;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int it = base + u * nthr, r = it / NC, j = it - r * NC;
+    if (!(it < 128 * NC && r < nrows)) continue;
+    const float c[8] = {tab[u][0].x, tab[u][0].y, tab[u][0].z, tab[u][0].w,
+                        tab[u][1].x, tab[u][1].y, tab[u][1].z, tab[u][1].w};
+    const float sn[8] = {tab[u][2].x, tab[u][2].y, tab[u][2].z, tab[u][2].w,
+                         tab[u][3].x, tab[u][3].y, tab[u][3].z, tab[u][3].w};
+    // The pair halves: columns 8j.. and 8j + D/2.. of the row (D = 128: same
+    // place in the two 64-column boxes; D = 64: chunks j and j + 4 of one box).
+    const uint32_t lo_off = sw128_off(r, 8 * j);
+    const uint32_t hi_off = D == 128 ? 16384 + sw128_off(r, 8 * j) : sw128_off(r, 8 * j + 32);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      uint8_t *tile = t ? kt : qt;
+      uint4 *lo = reinterpret_cast<uint4 *>(tile + lo_off);
+      uint4 *hi = reinterpret_cast<uint4 *>(tile + hi_off);
+      const uint4 a = *lo, b = *hi;
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+      uint32_t ow[4], hw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&aw[e]));
+        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&bw[e]));
+        ow[e] = pack_bf16(x.x * c[2 * e] - y.x * sn[2 * e], x.y * c[2 * e + 1] - y.y * sn[2 * e + 1]);
+        hw[e] = pack_bf16(y.x * c[2 * e] + x.x * sn[2 * e], y.y * c[2 * e + 1] + x.y * sn[2 * e + 1]);
+      }
+      const uint4 o4 = make_uint4(ow[0], ow[1], ow[2], ow[3]), h4 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *lo = o4;
+      *hi = h4;
+      if (qo != nullptr) {
+        __nv_bfloat16 *g = (t ? ko : qo) + r * rstride + 8 * j;
+        *reinterpret_cast<uint4 *>(g) = o4;
+        *reinterpret_cast<uint4 *>(g + D / 2) = h4;
+      }
+    }
+  }
+}
+
 // ======================================================================= forward
 
 template <int D>
@@ -71,14 +151,17 @@ struct FCfg {
 
 struct FBars {
   uint64_t full[4], empty[4];
+  uint64_t rot[4];  // rotary variant: q and k of the stage rotated
   uint64_t s_full[2], p_ready[2], o_full[2], slot_free[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-template <int D>
-__global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_constant__ BlockdiagParams p) {
+// Rotary: 384 threads, warps 2-3 and 8-11 rotate (192 threads, each with all
+// of its table loads for a unit in flight at once).
+template <int D, bool ROPE>
+__global__ void __launch_bounds__(ROPE ? 384 : 256, 1) blockdiag_fwd_kernel(const __grid_constant__ BlockdiagParams p) {
   using C = FCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -89,6 +172,7 @@ __global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_cons
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(&bars.full[s], 1);
       mbar_init(&bars.empty[s], 1);
+      mbar_init(&bars.rot[s], 6);  // warps 2, 3 and 8-11
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars.s_full[x], 1);
@@ -115,14 +199,16 @@ __global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_cons
 
   if (warp == 0) {
     if (lane == 0) {
+      ArmedLoads armed;  // barrier s = full[s]
       uint32_t eph = 0;
       int n = 0;
       for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
         const Unit x = unit_of(u, p.H, p.rows);
         const int s = n % C::NSTAGE;
-        if (!mbar_wait(&bars.empty[s], bit(eph, s) ^ 1, ctl, 1)) goto done;
+        if (!mbar_wait(&bars.empty[s], bit(eph, s) ^ 1, ctl, 1)) goto drain;
         eph ^= 1u << (s);
         mbar_arrive_expect_tx(&bars.full[s], 3 * C::TILE);
+        armed.arm(s);
         uint8_t *st = smem + C::OFF_STAGE + s * 3 * C::TILE;
         for (int c = 0; c < D / 64; ++c) {
           tma_load_3d(st + c * 16384, &p.tm_q, &bars.full[s], c * 64, x.h, x.row0);
@@ -130,6 +216,8 @@ __global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_cons
           tma_load_3d(st + 2 * C::TILE + c * 16384, &p.tm_v, &bars.full[s], c * 64, x.h, x.row0);
         }
       }
+    drain:  // every armed copy has landed before the CTA can exit
+      armed.drain([&](int i) { return &bars.full[i]; }, p.timeout_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -143,7 +231,8 @@ __global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_cons
         const bool have = u < n_units;
         if (have) {
           const int s = n % C::NSTAGE, ts = n & 1;
-          if (!mbar_wait(&bars.full[s], bit(fph, s), ctl, 10)) goto done;
+          // (rotary: the stage's q and k are read once warps 2-3 have rotated them)
+          if (!mbar_wait(ROPE ? &bars.rot[s] : &bars.full[s], bit(fph, s), ctl, 10)) goto done;
           fph ^= 1u << (s);
           if (!mbar_wait(&bars.slot_free[ts], bit(fr, ts) ^ 1, ctl, 11)) goto done;
           fr ^= 1u << (ts);
@@ -174,7 +263,34 @@ __global__ void __launch_bounds__(256, 1) blockdiag_fwd_kernel(const __grid_cons
         prev_stage = n % C::NSTAGE;
       }
     }
-  } else if (warp >= 4) {
+  } else if (ROPE && (warp == 2 || warp == 3 || warp >= 8)) {
+    // ------------------------------------------------- rotary: q and k tiles
+    // One batch covers a unit (U items per thread, all table loads in flight
+    // at once). (Loading the next unit's table values ahead, while its q and
+    // k are still loading, measured 5% slower.)
+    constexpr int U = 128 * (D / 16) / 192 + 1;
+    static_assert(192 * U >= 128 * (D / 16), "one batch per unit");
+    const int rt = (warp < 8 ? warp - 2 : warp - 6) * 32 + lane;  // 0 .. 191
+    const int64_t rstride = (int64_t)p.H * D;
+    uint32_t fph = 0;
+    int n = 0;
+    float4 tab[U][4];
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
+      const Unit x = unit_of(u, p.H, p.rows);
+      const int s = n % C::NSTAGE;
+      if (!mbar_wait(&bars.full[s], bit(fph, s), ctl, 40)) goto done;
+      fph ^= 1u << (s);
+      rot_load<D, U>(p, x.row0, x.nrows, rt, 192, tab);
+      uint8_t *st = smem + C::OFF_STAGE + s * 3 * C::TILE;
+      const int64_t g0 = (int64_t)x.row0 * rstride + (int64_t)x.h * D;
+      __nv_bfloat16 *qo = p.q_rot ? static_cast<__nv_bfloat16 *>(p.q_rot) + g0 : nullptr;
+      __nv_bfloat16 *ko = p.k_rot ? static_cast<__nv_bfloat16 *>(p.k_rot) + g0 : nullptr;
+      rot_apply<D, U>(st, st + C::TILE, x.nrows, rt, 192, tab, qo, ko, rstride);
+      fence_async_smem();  // the products read these tiles through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.rot[s]);
+    }
+  } else if (warp >= 4 && warp < 8) {
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const int blk = wq >> 1;  // rows 0-63 -> key block 0, rows 64-127 -> key block 1
@@ -291,20 +407,22 @@ struct BCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// TMEM columns: S [0,128) then dV; dP [128,256) then dK; dQ [256, 256+D).
-enum : uint32_t { BC_S = 0, BC_DP = 128, BC_DQ = 256 };
+// TMEM columns: S then dV in [0,128) for even units of a CTA and [384,512) for
+// odd ones (a unit's S runs while the previous unit's dV is still drained);
+// dP [128,256) then dK; dQ [256, 256+D).
+enum : uint32_t { BC_S = 0, BC_DP = 128, BC_DQ = 256, BC_S2 = 384 };
 enum { T_V = 0, T_DO = 1, T_Q = 2, T_K = 3 };  // ring load order = release order
 
 struct BBars {
   uint64_t full[8], empty[8];
   uint64_t s_full, dp_full, ps_ready, ps_free, g_full;
-  uint64_t dk_free, dv_free, dq_free;  // epilogue has drained that TMEM region
+  uint64_t dk_free, dv_free[2], dq_free;  // epilogue has drained that TMEM region
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-template <int D>
+template <int D, bool ROPE>
 __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_constant__ BlockdiagParams p) {
   using C = BCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -323,7 +441,8 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
     mbar_init(&bars.ps_free, 1);
     mbar_init(&bars.g_full, 1);
     mbar_init(&bars.dk_free, 4);
-    mbar_init(&bars.dv_free, 4);
+    mbar_init(&bars.dv_free[0], 4);
+    mbar_init(&bars.dv_free[1], 4);
     mbar_init(&bars.dq_free, 4);
     mbar_init(&bars.drain, 1);
     bars.abort_flag = 0;
@@ -350,21 +469,25 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
 
   if (warp == 0) {
     if (lane == 0) {
+      ArmedLoads armed;  // barrier s = full[s]
       uint32_t eph = 0;
       int slot = 0;
       for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         const Unit x = unit_of(u, p.H, p.rows);
         for (int t = 0; t < 4; ++t) {
-          if (!mbar_wait(&bars.empty[slot], bit(eph, slot) ^ 1, ctl, 1)) goto done;
+          if (!mbar_wait(&bars.empty[slot], bit(eph, slot) ^ 1, ctl, 1)) goto drain;
           eph ^= 1u << (slot);
-          mbar_arrive_expect_tx(&bars.full[slot], C::TILE);
+          uint64_t *fb = &bars.full[slot];
+          mbar_arrive_expect_tx(fb, C::TILE);
+          armed.arm(slot);
           const CUtensorMap *m = t == T_V ? &p.tm_v : t == T_DO ? &p.tm_do : t == T_Q ? &p.tm_q : &p.tm_k;
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(smem + C::OFF_RING + slot * C::TILE + c * 16384, m, &bars.full[slot], c * 64,
-                        x.h, x.row0);
+            tma_load_3d(smem + C::OFF_RING + slot * C::TILE + c * 16384, m, fb, c * 64, x.h, x.row0);
           if (++slot == C::NSLOT) slot = 0;
         }
       }
+    drain:  // every armed copy has landed before the CTA can exit
+      armed.drain([&](int i) { return &bars.full[i]; }, p.timeout_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -393,7 +516,9 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
           mma_ss(tmem + dcol, xd + off, yd + off, C::IDESC_S, k > 0);
         }
       };
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      for (int u = blockIdx.x, n = 0; u < n_units; u += gridDim.x, ++n) {
+        const int sb = n & 1;
+        const uint32_t sreg = sb ? BC_S2 : BC_S;
         // Each product region is reused as soon as the previous unit's epilogue
         // has drained it (dK, then dV, then dQ), so this unit's dP and S run
         // while the rest of the previous epilogue is still being written.
@@ -404,11 +529,11 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
         xyT(BC_DP, tk(T_DO), tk(T_V));  // dP = dO V^T
         mma_commit(&bars.dp_full);
         mma_commit(&bars.empty[sl(T_V)]);
-        if (!mbar_wait(&bars.dv_free, vf ^ 1, ctl, 22)) goto done;
-        vf ^= 1;
+        if (!mbar_wait(&bars.dv_free[sb], bit(vf, sb) ^ 1, ctl, 22)) goto done;
+        vf ^= 1u << sb;
         if (!wait_full(T_Q) || !wait_full(T_K)) goto done;
         tc_fence_after();
-        xyT(BC_S, tk(T_Q), tk(T_K));  // S = Q K^T
+        xyT(sreg, tk(T_Q), tk(T_K));  // S = Q K^T
         mma_commit(&bars.s_full);
         if (!mbar_wait(&bars.ps_ready, psr, ctl, 21)) goto done;
         psr ^= 1;
@@ -418,7 +543,7 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
           const uint64_t bd = tm(T_DO);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + BC_S, p_mn + (k * 2048 >> 4), bd + (k * 2048 >> 4), C::IDESC_T, k > 0);
+            mma_ss(tmem + sreg, p_mn + (k * 2048 >> 4), bd + (k * 2048 >> 4), C::IDESC_T, k > 0);
         }
         mma_commit(&bars.empty[sl(T_DO)]);
         // dK = dS^T Q
@@ -456,8 +581,10 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
     uint32_t sph = 0, dpph = 0, psf = 0, gph = 0;
     uint8_t *prow = smem + C::OFF_P + blk * 16384 + r * 128;
     uint8_t *dsrow = smem + C::OFF_DS + blk * 16384 + r * 128;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    for (int u = blockIdx.x, n = 0; u < n_units; u += gridDim.x, ++n) {
       const Unit x = unit_of(u, p.H, p.rows);
+      const int sb = n & 1;
+      const uint32_t sreg = sb ? BC_S2 : BC_S;
       if (!mbar_wait(&bars.s_full, sph, ctl, 30)) goto done;
       sph ^= 1;
       if (!mbar_wait(&bars.dp_full, dpph, ctl, 31)) goto done;
@@ -467,8 +594,8 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
       float di = 0.f;
       {
         uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_off + BC_S + blk * 64, a);
-        tmem_ld32(tmem + lane_off + BC_S + blk * 64 + 32, b);
+        tmem_ld32(tmem + lane_off + sreg + blk * 64, a);
+        tmem_ld32(tmem + lane_off + sreg + blk * 64 + 32, b);
         tmem_wait_ld();
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -537,6 +664,27 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.ps_ready);
+      // Rotary: this row's table values in 16-pair pieces (dK and dQ rows r
+      // are at the same position and share them); the first two pieces load
+      // while the products run, each later one two pieces ahead of its use.
+      constexpr int NPC = ROPE ? D / 32 : 1;
+      float4 tc[NPC][4], ts[NPC][4];
+      const float4 *cr = nullptr, *sr = nullptr;
+      auto load_piece = [&](int c) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          tc[c][e] = ldg_f4_ordered(cr + c * 4 + e);
+          ts[c][e] = ldg_f4_ordered(sr + c * 4 + e);
+        }
+      };
+      if constexpr (ROPE) {
+        int pos = (int)(x.row0 % p.L) + (r < x.nrows ? r : 0);
+        while (pos >= p.L) pos -= (int)p.L;
+        cr = reinterpret_cast<const float4 *>(p.cos_t + (int64_t)pos * (D / 2));
+        sr = reinterpret_cast<const float4 *>(p.sin_t + (int64_t)pos * (D / 2));
+        load_piece(0);
+        load_piece(1);
+      }
       // epilogue: dQ (query row r), dV and dK (key row r)
       if (!mbar_wait(&bars.g_full, gph, ctl, 33)) goto done;
       gph ^= 1;
@@ -545,10 +693,41 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
         // Each 64-column (128-byte) piece of a row is stored four lanes to a row
         // (eight whole lines per store instruction, not 32-byte pieces of 32).
         const int grp = wq * 32 + (lane & ~3);  // first of this lane group's rows
+        if constexpr (ROPE) {
+          // dK and dQ rotated back (the transposed rotation) in place in tensor
+          // memory; the stores below then run as in the plain kernel. Columns
+          // i and i + D/2 are the two halves of pair i.
+#pragma unroll
+          for (int c = 0; c < NPC; ++c) {  // 16-column pieces of the low half
+            if (c + 2 < NPC) load_piece(c + 2);
+#pragma unroll 1
+            for (int g = 0; g < 2; ++g) {
+              const uint32_t col = g == 0 ? BC_DP : BC_DQ;
+              uint32_t a[16], b[16];
+              tmem_ld16(tmem + lane_off + col + c * 16, a);
+              tmem_ld16(tmem + lane_off + col + D / 2 + c * 16, b);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; e += 4) {
+                const float4 c4 = tc[c][e / 4], s4 = ts[c][e / 4];
+                const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                  const float lo = __uint_as_float(a[e + f]), hi = __uint_as_float(b[e + f]);
+                  a[e + f] = __float_as_uint(lo * cc[f] + hi * ss[f]);
+                  b[e + f] = __float_as_uint(hi * cc[f] - lo * ss[f]);
+                }
+              }
+              tmem_st16(tmem + lane_off + col + c * 16, a);
+              tmem_st16(tmem + lane_off + col + D / 2 + c * 16, b);
+            }
+          }
+          tmem_wait_st();
+        }
         // Drain order dK, dV, dQ: each region is released as soon as it is read.
 #pragma unroll 1
         for (int which = 0; which < 3; ++which) {
-          const uint32_t col = which == 0 ? BC_DP : which == 1 ? BC_S : BC_DQ;
+          const uint32_t col = which == 0 ? BC_DP : which == 1 ? sreg : BC_DQ;
           const float mul = which == 1 ? 1.f : p.scale;
           __nv_bfloat16 *base = static_cast<__nv_bfloat16 *>(which == 0 ? p.dk : which == 1 ? p.dv : p.dq);
 #pragma unroll 1
@@ -560,7 +739,7 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
             if (c + 2 >= D / 32) {  // last chunk pair read: release the region
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(which == 0 ? &bars.dk_free : which == 1 ? &bars.dv_free : &bars.dq_free);
+              if (lane == 0) mbar_arrive(which == 0 ? &bars.dk_free : which == 1 ? &bars.dv_free[sb] : &bars.dq_free);
             }
             uint32_t w[32];  // this lane's row
 #pragma unroll
@@ -593,25 +772,34 @@ done:
 }
 
 template <typename K>
-cudaError_t launch_k(K kern, int smem, const BlockdiagParams &p, int num_sms, cudaStream_t st) {
+cudaError_t launch_k(K kern, int smem, const BlockdiagParams &p, int num_sms, cudaStream_t st,
+                     int threads = 256) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int n_units = (int)((p.rows + 127) / 128) * p.H;
   const int grid = n_units < num_sms ? n_units : num_sms;
-  kern<<<grid, 256, smem, st>>>(p);
+  kern<<<grid, threads, smem, st>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_blockdiag_fwd(const BlockdiagParams &p, int D, int num_sms, cudaStream_t st) {
-  if (D == 128) return launch_k(blockdiag_fwd_kernel<128>, FCfg<128>::SMEM, p, num_sms, st);
-  return launch_k(blockdiag_fwd_kernel<64>, FCfg<64>::SMEM, p, num_sms, st);
+  const bool rope = p.cos_t != nullptr;
+  if (D == 128)
+    return rope ? launch_k(blockdiag_fwd_kernel<128, true>, FCfg<128>::SMEM, p, num_sms, st, 384)
+                : launch_k(blockdiag_fwd_kernel<128, false>, FCfg<128>::SMEM, p, num_sms, st);
+  return rope ? launch_k(blockdiag_fwd_kernel<64, true>, FCfg<64>::SMEM, p, num_sms, st, 384)
+              : launch_k(blockdiag_fwd_kernel<64, false>, FCfg<64>::SMEM, p, num_sms, st);
 }
 
 cudaError_t launch_blockdiag_bwd(const BlockdiagParams &p, int D, int num_sms, cudaStream_t st) {
-  if (D == 128) return launch_k(blockdiag_bwd_kernel<128>, BCfg<128>::SMEM, p, num_sms, st);
-  return launch_k(blockdiag_bwd_kernel<64>, BCfg<64>::SMEM, p, num_sms, st);
+  const bool rope = p.cos_t != nullptr;
+  if (D == 128)
+    return rope ? launch_k(blockdiag_bwd_kernel<128, true>, BCfg<128>::SMEM, p, num_sms, st)
+                : launch_k(blockdiag_bwd_kernel<128, false>, BCfg<128>::SMEM, p, num_sms, st);
+  return rope ? launch_k(blockdiag_bwd_kernel<64, true>, BCfg<64>::SMEM, p, num_sms, st)
+              : launch_k(blockdiag_bwd_kernel<64, false>, BCfg<64>::SMEM, p, num_sms, st);
 }
 
 }  // namespace jfa

@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      ArmedLoads armed;  // barrier 0 kv_full, 1.. stage_full
       uint32_t kvph = 0, eph = 0;
       int qb = 0;
       // The next tile is decoded one tile ahead (its index loads are off the
@@ -256,9 +257,10 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
         const BwdTile tl = nxt;
         if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
         if (tl.nq == 0 || tl.nkv <= 0) continue;
-        if (!mbar_wait(&bars.kv_empty, kvph ^ 1, ctl, 1)) goto done;
+        if (!mbar_wait(&bars.kv_empty, kvph ^ 1, ctl, 1)) goto drain;
         kvph ^= 1;
         mbar_arrive_expect_tx(&bars.kv_full, 2 * C::KV_TILE);
+        armed.arm(0);
         for (int c = 0; c < D / 64; ++c) {
           tma_load_3d(smem + C::OFF_K + c * 16384, &p.tm_k, &bars.kv_full, c * 64, tl.h, tl.kv_row0);
           tma_load_3d(smem + C::OFF_V + c * 16384, &p.tm_v, &bars.kv_full, c * 64, tl.h, tl.kv_row0);
@@ -266,9 +268,10 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
         for (int i = 0; i < tl.nq; ++i, ++qb) {
           const int s = qb % C::NSTAGE;
           const int qr = (tl.qb0 + i) * 64;  // first query row of the block in the sequence
-          if (!mbar_wait(&bars.stage_empty[s], bit(eph, s) ^ 1, ctl, 2)) goto done;
+          if (!mbar_wait(&bars.stage_empty[s], bit(eph, s) ^ 1, ctl, 2)) goto drain;
           eph ^= 1u << s;
           mbar_arrive_expect_tx(&bars.stage_full[s], 2 * C::QT);
+          armed.arm(1 + s);
           uint8_t *st = smem + C::OFF_STAGE + s * 2 * C::QT;
           for (int c = 0; c < D / 64; ++c) {
             tma_load_3d(st + c * C::QCHUNK, &p.tm_q, &bars.stage_full[s], c * 64, tl.h,
@@ -278,6 +281,8 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
           }
         }
       }
+    drain:  // every armed copy has landed before the CTA can exit
+      armed.drain([&](int i) { return i == 0 ? &bars.kv_full : &bars.stage_full[i - 1]; }, p.timeout_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer

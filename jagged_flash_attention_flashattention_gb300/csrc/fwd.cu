@@ -250,6 +250,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      ArmedLoads armed;  // barriers 0-1 q_full, 2.. slot_full
       uint32_t qph = 0;
       int slot = 0;
       uint32_t sph = 0;
@@ -292,17 +293,19 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
         for (int x = 0; x < 2; ++x) {
           const int2 hs = half_steps<GEN>(tl, p, x);
           if (hs.y <= hs.x) continue;  // no step: the half's Q is not needed
-          if (!mbar_wait(&bars.q_empty[x], ((qph >> x) & 1) ^ 1, ctl, 1)) goto done;
+          if (!mbar_wait(&bars.q_empty[x], ((qph >> x) & 1) ^ 1, ctl, 1)) goto drain;
           qph ^= 1u << x;
           mbar_arrive_expect_tx(&bars.q_full[x], C::TILE_BYTES);
+          armed.arm(x);
           for (int c = 0; c < D / 64; ++c)
             tma_load_3d(smem + C::OFF_Q + x * C::TILE_BYTES + c * 16384, &p.tm_q,
                         &bars.q_full[x], c * 64, tl.h, tl.q_coord + x * 128);
         }
         for (int j = 0; j <= tl.n_kv; ++j) {  // slot of step j: K_j (j < n) and V_{j-1} (j > 0)
-          if (!mbar_wait(&slot_empty[slot], sph ^ 1, ctl, 2)) goto done;
+          if (!mbar_wait(&slot_empty[slot], sph ^ 1, ctl, 2)) goto drain;
           const bool k_in = j < tl.n_kv, v_in = j > 0;
           mbar_arrive_expect_tx(&slot_full[slot], (k_in + v_in) * C::TILE_BYTES);
+          armed.arm(2 + slot);
           uint8_t *dst = smem + C::OFF_RING + slot * C::PAIR_BYTES;
           for (int c = 0; c < D / 64; ++c) {
             if (k_in)
@@ -317,6 +320,8 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           }
         }
       }
+    drain:  // every armed copy has landed before the CTA can exit
+      armed.drain([&](int i) { return i < 2 ? &bars.q_full[i] : &slot_full[i - 2]; }, p.timeout_ns);
     }
   } else if (warp == 2 || warp == 3) {
     // ----------------------------------- backward accumulator pre-clearing

@@ -126,6 +126,15 @@ struct BlockdiagParams {
   void *dk;
   void *dv;
   int64_t rows;  // B * L
+  int64_t L;     // tokens per sequence (a row's position is row % L)
+  // Rotary variant: fp32 tables [L, D/2]. The forward rotates q and k rows by
+  // them before the products (and writes the rotated rows to q_rot, k_rot
+  // when those are not null); the backward reads rotated q and k and rotates
+  // dQ, dK back.
+  const float *cos_t;
+  const float *sin_t;
+  void *q_rot;
+  void *k_rot;
   int H;
   float scale;
   float scale_log2;
@@ -135,5 +144,6 @@ struct BlockdiagParams {
 
 cudaError_t launch_blockdiag_fwd(const BlockdiagParams &p, int D, int num_sms, cudaStream_t st);
 cudaError_t launch_blockdiag_bwd(const BlockdiagParams &p, int D, int num_sms, cudaStream_t st);
+// (p.cos_t != nullptr selects the rotary variant of either kernel.)
 
 }  // namespace jfa

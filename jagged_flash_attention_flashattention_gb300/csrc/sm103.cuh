@@ -171,6 +171,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
   }
 }
 
+// Copies armed by a producer thread: bit i of `any` marks barrier i as armed
+// at least once, bit i of `cnt` the parity of the number of phases armed on
+// it. After a give-up the producer waits (bounded) until the last armed phase
+// of each barrier has completed, so that no copy lands in the shared memory
+// of a CTA that has exited.
+struct ArmedLoads {
+  uint32_t any = 0, cnt = 0;
+  __device__ __forceinline__ void arm(int i) {
+    any |= 1u << i;
+    cnt ^= 1u << i;
+  }
+  template <typename BarOf>
+  __device__ __forceinline__ void drain(BarOf bar_of, uint64_t timeout_ns) const {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t m = any; m != 0; m &= m - 1) {
+      const int i = __ffs(m) - 1;
+      const uint32_t par = ((cnt >> i) & 1) ^ 1;  // parity of the last armed phase
+      while (!mbar_try_wait(bar_of(i), par) && globaltimer() - t0 < timeout_ns) {
+      }
+    }
+  }
+};
+
+// Read-only 16-byte global load kept in program order with the other
+// volatile asm statements (so the compiler does not hoist it above a
+// barrier arrive and lengthen the live range of its registers).
+__device__ __forceinline__ float4 ldg_f4_ordered(const float4 *p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // One of four words by a 2-bit index, without indexing a register array.
 __device__ __forceinline__ uint32_t sel4(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, int i) {
   const uint32_t lo = (i & 1) ? x1 : x0, hi = (i & 1) ? x3 : x2;
@@ -376,6 +410,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
         "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// As tmem_ld32 for 16 consecutive columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 }

@@ -29,7 +29,8 @@ import math
 import numpy as np
 import torch
 
-SEEDS = {"tiny": 1, "gem": 2, "stress": 3, "bcast": 4, "blockdiag": 5, "blockdiag64": 5}
+SEEDS = {"tiny": 1, "gem": 2, "stress": 3, "bcast": 4, "blockdiag": 5, "blockdiag64": 5,
+         "blockdiag_rotary": 5}
 
 
 def lengths_for(name, seed=None):
@@ -89,6 +90,15 @@ def blockdiag_inputs(B, L, H, D, seed, device="cpu", with_grad=True):
     return {n: randn_bf16((B, L, H, D), seed * 1000 + i, device) for i, n in enumerate(names)}
 
 
+def rotary_tables(L, D, base=10000.0, device="cpu"):
+    """The usual rotary tables: angle = position * base^(-2i/D) for i < D/2,
+    computed in float64 and stored as fp32 [L, D/2] (cos, sin)."""
+    i = np.arange(D // 2, dtype=np.float64)
+    ang = np.arange(L, dtype=np.float64)[:, None] * base ** (-2.0 * i / D)[None, :]
+    return (torch.from_numpy(np.cos(ang).astype(np.float32)).to(device),
+            torch.from_numpy(np.sin(ang).astype(np.float32)).to(device))
+
+
 WORKLOADS = {
     "tiny": dict(kind="jagged", H=2, D=64, offsets_dtype=np.int32),
     "gem": dict(kind="jagged", H=4, D=128, offsets_dtype=np.int64),
@@ -101,6 +111,8 @@ WORKLOADS = {
     "bcast": dict(kind="bcast", H=4, D=128, Lq=256, offsets_dtype=np.int64),
     "blockdiag": dict(kind="blockdiag", B=1152, L=4096, H=2, D=128),
     "blockdiag64": dict(kind="blockdiag", B=1152, L=4096, H=2, D=64),
+    # the block-diagonal configuration with rotary embeddings fused in
+    "blockdiag_rotary": dict(kind="blockdiag", B=1152, L=4096, H=2, D=128, rotary=True),
 }
 
 

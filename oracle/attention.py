@@ -48,6 +48,9 @@ per sequence and per head, with no blocking, fusion or online rescaling:
 
   attention runs on (q_r, k_r, v), and the gradients of q and k are those of
   q_r and k_r rotated back by the transposed rotation (rotation by -angle).
+  The backward is also given from q_r and k_r themselves (the rotary
+  layer's saved output), the form whose rotary part the page fuses into the
+  attention epilogue.
 
 * masked and cross (varlen) attention ([JFA-GEM] "Impacto en el desarrollo
   de modelos generativos": causal, sliding-window and block-sparse masks as
@@ -357,4 +360,14 @@ def blockdiag_rotary_bwd(q, k, v, do, cos, sin, scale, block=BLOCK):
     """Backward of :func:`blockdiag_rotary_fwd` with respect to the
     unrotated q, k and v. Returns dQ, dK, dV [B, L, H, D]."""
     dqr, dkr, dv = blockdiag_bwd(rope(q, cos, sin), rope(k, cos, sin), v, do, scale, block)
+    return rope_transpose(dqr, cos, sin), rope_transpose(dkr, cos, sin), dv
+
+
+def blockdiag_rotary_bwd_from_rotated(q_r, k_r, v, do, cos, sin, scale, block=BLOCK):
+    """The combined attention-and-rotary backward ([TLX-BA] section 1: the
+    rotary backward fused into the attention backward), taken from the
+    rotated q_r, k_r that a rotary layer saves: the block-diagonal attention
+    backward on (q_r, k_r, v), then the gradients of q_r and k_r rotated back.
+    Returns dQ, dK, dV [B, L, H, D] with respect to the unrotated q, k and v."""
+    dqr, dkr, dv = blockdiag_bwd(q_r, k_r, v, do, scale, block)
     return rope_transpose(dqr, cos, sin), rope_transpose(dkr, cos, sin), dv

@@ -10,7 +10,9 @@
   scaled_dot_product_attention with a block mask, forward and, by autograd,
   backward;
 * central finite differences of sum(O * dO) on a tiny case;
-* a planted mistake (the backward rotating forward instead of back) fails.
+* a planted mistake (the backward rotating forward instead of back) fails;
+* the backward taken from the rotated q_r, k_r equals the one taken from q
+  and k (with q_r, k_r the rotation of q, k).
 """
 
 import math
@@ -124,3 +126,18 @@ def test_planted_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(A, "rope_transpose", A.rope)  # backward rotates the wrong way
     with pytest.raises(AssertionError):
         _fd_pin()
+
+
+def test_backward_from_rotated_inputs_equals_backward_from_unrotated():
+    rng = np.random.default_rng(87)
+    B, L, H, D = 2, 128, 2, 16
+    q, k, v, do = (_rand((B, L, H, D), rng) for _ in range(4))
+    c, s = _tables(L, D)
+    ref = A.blockdiag_rotary_bwd(q, k, v, do, c, s, 0.3)
+    got = A.blockdiag_rotary_bwd_from_rotated(A.rope(q, c, s), A.rope(k, c, s), v, do, c, s, 0.3)
+    for a, b in zip(got, ref):
+        np.testing.assert_allclose(a, b, atol=1e-12)
+    # and with unrelated q_r, k_r it is not the rotation-free backward
+    plain = A.blockdiag_bwd(q, k, v, do, 0.3)
+    dq_wrong = A.blockdiag_rotary_bwd_from_rotated(q, k, v, do, c, s, 0.3)[0]
+    assert np.abs(dq_wrong - plain[0]).max() > 1e-3
