@@ -446,6 +446,38 @@ def _dynamic_fwd_ms(st, steps, warmup, stream):
     return res
 
 
+def _pair_fwd_ms(st, steps, warmup, stream):
+    """Median forward kernel time of a jagged D = 128 workload on single CTAs
+    (jfa_fwd) and on CTA pairs (jfa_fwd_pair), each launched the same way as
+    in _dynamic_fwd_ms."""
+    import torch
+
+    import jagged_flash_attention_flashattention_gb300 as jfa
+
+    inp, off = st["inp"], st["plan"].offsets
+    H, D = st["H"], st["D"]
+    host = st["plan"].host_offsets
+    plans = {"single": jfa.Plan(off, H, D, host_offsets=host),
+             "pair": jfa.Plan(off, H, D, host_offsets=host, pair=True)}
+    res = {}
+    for name, plan in plans.items():
+        fn = (lambda pl: lambda: jfa.jfa_fwd(inp["q"], inp["k"], inp["v"], off, plan=pl))(plan)
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        _spin(stream)
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        res[name] = statistics.median(a.elapsed_time(b) for a, b in evs)
+        plan.check()
+    return res
+
+
 def _other_configs(args, dev, peaks):
     """Every other workload of the method, each timed like the headline one
     (W warm-up and K timed fwd+bwd steps, CUDA events, median per op), plus the
@@ -491,6 +523,18 @@ def _other_configs(args, dev, peaks):
                 "fwd_dynamic_device_over_static": round(dyn["device"] / dyn["static"], 3),
                 "fwd_dynamic_lpt_over_static": round(dyn["lpt"] / dyn["static"], 3)}
             del nv
+        if name == "stress":
+            out["pair_ab"] = {}
+            for pname, pst in (("gem", None), ("stress", st)):
+                pst = pst or _setup("gem", 0, dev)
+                pr = _pair_fwd_ms(pst, steps, warmup, stream)
+                # forward kernel alone on single CTAs against CTA pairs
+                # (cta_group::2 products, 512-row tiles)
+                out["pair_ab"][pname] = {
+                    "fwd_kernel_ms_single": round(pr["single"], 4),
+                    "fwd_kernel_ms_pair": round(pr["pair"], 4),
+                    "pair_over_single": round(pr["pair"] / pr["single"], 3)}
+                del pst
         del st
         torch.cuda.synchronize()
         torch.cuda.empty_cache()

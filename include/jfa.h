@@ -66,7 +66,8 @@ typedef enum {
   JFA_OP_BCASTQ_FWD = 2,
   JFA_OP_BCASTQ_BWD = 3,
   JFA_OP_BLOCKDIAG_FWD = 4,
-  JFA_OP_BLOCKDIAG_BWD = 5
+  JFA_OP_BLOCKDIAG_BWD = 5,
+  JFA_OP_FWD_PAIR = 6 /* jfa_fwd_pair: 512-row tiles, D = 128 */
 } jfa_op;
 
 /* Human-readable name of a status code (static string). */
@@ -186,6 +187,25 @@ jfa_status jfa_fwd(const void *q, const void *k, const void *v, const void *offs
                    jfa_index_t idx, int64_t B, int64_t T, int H, int D, float scale,
                    const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_sms, void *o,
                    float *lse, void *workspace, size_t ws_bytes, jfa_stream_t stream);
+
+/* Jagged forward on CTA pairs ("Desarrollo de Jagged Flash Attention para
+ * el modelo GEM", "Optimización del proceso de Backward y dQ": the 2-CTA MMA
+ * of FA4, to raise tensor-core utilisation). Same inputs, outputs and
+ * workspace as jfa_fwd (including the clearing of the backward's dQ
+ * accumulator), for jagged self-attention at D = 128 (other D:
+ * JFA_ERR_UNSUPPORTED). Two CTAs of a cluster compute each product together
+ * (M = 256 rows, each CTA loading half of every K and V tile); a tile is 512
+ * query rows of one (sequence, head). Tiles: jfa_sched_build() with
+ * tile_rows = jfa_tile_rows(JFA_OP_FWD_PAIR) = 512 and num_sms = num_pairs
+ * (normally jfa_num_pairs()); the grid is 2 * num_pairs CTAs. */
+jfa_status jfa_fwd_pair(const void *q, const void *k, const void *v, const void *offsets,
+                        jfa_index_t idx, int64_t B, int64_t T, int H, int D, float scale,
+                        const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_pairs, void *o,
+                        float *lse, void *workspace, size_t ws_bytes, jfa_stream_t stream);
+
+/* Number of two-CTA clusters of jfa_fwd_pair that fit on the current device
+ * at once (at most half its SMs). */
+jfa_status jfa_num_pairs(int *num_pairs);
 
 /* Jagged forward with device-side dynamic tile scheduling ("A TLX nagyobb
  * kontrollt ad a Triton fölött": Cluster Launch Control, i.e. running CTAs

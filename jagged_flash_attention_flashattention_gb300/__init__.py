@@ -32,7 +32,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libjfa.so")
 
 JFA_I32, JFA_I64 = 0, 1
-OP_FWD, OP_BWD, OP_BCASTQ_FWD, OP_BCASTQ_BWD, OP_BLOCKDIAG_FWD, OP_BLOCKDIAG_BWD = range(6)
+OP_FWD, OP_BWD, OP_BCASTQ_FWD, OP_BCASTQ_BWD, OP_BLOCKDIAG_FWD, OP_BLOCKDIAG_BWD, OP_FWD_PAIR = range(7)
 
 (JFA_OK, JFA_ERR_INVALID_ARG, JFA_ERR_UNSUPPORTED, JFA_ERR_WORKSPACE, JFA_ERR_CUDA,
  JFA_ERR_TIMEOUT) = range(6)
@@ -44,6 +44,7 @@ EXPORTS = [
     "jfa_num_sms", "jfa_workspace_size", "jfa_workspace_init", "jfa_check_status", "jfa_fwd",
     "jfa_bwd", "jfa_bcastq_fwd", "jfa_bcastq_bwd", "blockdiag_fwd", "blockdiag_bwd",
     "jfa_bwd_noalloc", "jfa_noalloc_check_status", "jfa_selftest_wait_timeout",
+    "jfa_fwd_pair", "jfa_num_pairs",
     "jfa_sched_size_varlen", "jfa_sched_build_varlen", "jfa_varlen_fwd", "jfa_varlen_bwd",
     "jfa_varlen_workspace_size", "jfa_fwd_dynamic", "jfa_fwd_dynamic_workspace_size",
     "blockdiag_rotary_fwd", "blockdiag_rotary_bwd",
@@ -100,6 +101,8 @@ def lib():
         "blockdiag_rotary_fwd": ([P, P, P, P, P, I64, I64, I, I, F, P, P, P, P, SZ, P], I),
         "blockdiag_rotary_bwd": ([P, P, P, P, P, P, I64, I64, I, I, F, P, P, P, P, SZ, P], I),
         "jfa_selftest_wait_timeout": ([P, SZ, ctypes.c_uint64, P], I),
+        "jfa_fwd_pair": ([P, P, P, P, I, I64, I64, I, I, F, P, P, I, P, P, P, SZ, P], I),
+        "jfa_num_pairs": ([P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -133,6 +136,13 @@ def _need_cuda(*ts):
 def num_sms():
     n = ctypes.c_int(0)
     _check(lib().jfa_num_sms(ctypes.byref(n)))
+    return n.value
+
+
+def num_pairs():
+    """Two-CTA clusters of the pair forward that fit on the device at once."""
+    n = ctypes.c_int(0)
+    _check(lib().jfa_num_pairs(ctypes.byref(n)))
     return n.value
 
 
@@ -210,7 +220,7 @@ class Plan:
 
     def __init__(self, offsets, H, D, kind="jagged", Lq=0, zigzag=True, host_offsets=None,
                  workspace=None, q_offsets=None, host_q_offsets=None, window=(-1, -1),
-                 deterministic=False):
+                 deterministic=False, pair=False):
         if not offsets.is_cuda:
             raise ValueError("offsets must be a CUDA tensor")
         self.offsets = offsets
@@ -244,7 +254,15 @@ class Plan:
             bwd = schedule_varlen(self.host_q_offsets, host, H, OP_BWD, self.n_sms, self.window,
                                   zigzag)
         elif kind == "jagged":
-            fwd = schedule(host, H, tile_rows(OP_FWD, D), self.n_sms, zigzag=zigzag)
+            # pair: the forward runs on CTA pairs (jfa_fwd_pair, D = 128 only).
+            self.pair = bool(pair)
+            if self.pair and D != 128:
+                raise ValueError("the CTA-pair forward takes D = 128")
+            if self.pair:
+                self.n_pairs = num_pairs()
+                fwd = schedule(host, H, tile_rows(OP_FWD_PAIR, D), self.n_pairs, zigzag=zigzag)
+            else:
+                fwd = schedule(host, H, tile_rows(OP_FWD, D), self.n_sms, zigzag=zigzag)
             bwd = schedule(host, H, tile_rows(OP_BWD, D), self.n_sms, zigzag=zigzag)
         else:
             fwd = schedule(host, H, tile_rows(OP_BCASTQ_FWD, D), self.n_sms, fixed_rows=self.Lq,
@@ -315,9 +333,14 @@ def jfa_fwd(q, k, v, offsets, scale=None, plan=None):
     o = torch.empty_like(q)
     lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
     sp, tl = plan.fwd_sched
-    _check(lib().jfa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), plan.idx, plan.B, T, H, D,
-                         _scale(scale, D), _ptr(sp), _ptr(tl), plan.n_sms, _ptr(o), _ptr(lse),
-                         _ptr(plan.workspace), plan.workspace.numel(), _stream()))
+    if getattr(plan, "pair", False):
+        _check(lib().jfa_fwd_pair(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), plan.idx, plan.B, T, H,
+                                  D, _scale(scale, D), _ptr(sp), _ptr(tl), plan.n_pairs, _ptr(o),
+                                  _ptr(lse), _ptr(plan.workspace), plan.workspace.numel(), _stream()))
+    else:
+        _check(lib().jfa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(offsets), plan.idx, plan.B, T, H, D,
+                             _scale(scale, D), _ptr(sp), _ptr(tl), plan.n_sms, _ptr(o), _ptr(lse),
+                             _ptr(plan.workspace), plan.workspace.numel(), _stream()))
     return o, lse
 
 

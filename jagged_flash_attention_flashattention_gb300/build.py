@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libjfa.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["sched.cpp", "api.cu", "fwd.cu", "bwd.cu", "blockdiag.cu", "noalloc.cu", "selftest.cu"]
+SOURCES = ["sched.cpp", "api.cu", "fwd.cu", "fwd_pair.cu", "bwd.cu", "blockdiag.cu", "noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -133,6 +133,10 @@ extern "C" jfa_status jfa_tile_rows(jfa_op op, int D, int *tile_rows) {
     case JFA_OP_BCASTQ_BWD: *tile_rows = 128; return JFA_OK;
     case JFA_OP_BLOCKDIAG_FWD:
     case JFA_OP_BLOCKDIAG_BWD: *tile_rows = 128; return JFA_OK;
+    case JFA_OP_FWD_PAIR:
+      if (D != 128) return fail(JFA_ERR_UNSUPPORTED, "the CTA-pair forward takes D = 128");
+      *tile_rows = 512;
+      return JFA_OK;
   }
   return fail(JFA_ERR_INVALID_ARG, "unknown op %d", (int)op);
 }
@@ -203,7 +207,7 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *k
                       int64_t Tk, int64_t Lq, int H, int D, float scale, int win_left,
                       int win_right, const int32_t *sm_ptr, const int32_t *tiles, int num_sms,
                       void *o, float *lse, void *ws, size_t ws_bytes, cudaStream_t st,
-                      int dyn = 0, int64_t n_dyn_tiles = 0) {
+                      int dyn = 0, int64_t n_dyn_tiles = 0, bool pair = false) {
   JFA_TRY(check_dims(B, Tk, H, D));
   JFA_TRY(check_dims(B, q_rows, H, D));
   JFA_TRY(check_window(win_left, win_right));
@@ -213,6 +217,8 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *k
   if (num_sms < 1) return fail(JFA_ERR_INVALID_ARG, "num_sms = %d < 1", num_sms);
   JFA_TRY(need_ptr(kv_offsets, "kv_offsets"));
   if (Lq == 0) JFA_TRY(need_ptr(q_offsets, "q_offsets"));
+  if (pair && (D != 128 || Lq != 0 || win_left >= 0 || win_right >= 0 || dyn != 0))
+    return fail(JFA_ERR_UNSUPPORTED, "the CTA-pair forward takes jagged self-attention at D = 128 only");
   if (dyn == 2 && ws_bytes < dyn_workspace_bytes(B))
     return fail(JFA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, dyn_workspace_bytes(B));
   if (B == 0 || q_rows == 0) return JFA_OK;
@@ -232,6 +238,7 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *k
   JFA_TRY(map_rows_bf16(&p.tm_q, q, q_rows, H, D, 128));
   JFA_TRY(map_rows_bf16(&p.tm_k, k, Tk > 0 ? Tk : q_rows, H, D, 128));
   JFA_TRY(map_rows_bf16(&p.tm_v, v, Tk > 0 ? Tk : q_rows, H, D, 128));
+  if (pair) JFA_TRY(map_rows_bf16(&p.tm_khalf, k, Tk > 0 ? Tk : q_rows, H, D, 64));
   p.offsets = kv_offsets;
   p.q_offsets = Lq > 0 ? kv_offsets : q_offsets;
   p.idx64 = idx == JFA_I64;
@@ -268,6 +275,7 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *k
     p.acc_zero = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kStatusBytes);
     p.acc_n16 = (int64_t)(acc_bytes / 16);
   }
+  if (pair) return cuda_status(launch_fwd_pair(p, num_sms, st), "pair fwd launch");
   return cuda_status(launch_fwd(p, D, num_sms, st), "fwd launch");
 }
 
@@ -280,6 +288,24 @@ extern "C" jfa_status jfa_fwd(const void *q, const void *k, const void *v, const
                               jfa_stream_t stream) {
   return fwd_common(q, k, v, offsets, offsets, idx, B, T, T, 0, H, D, scale, -1, -1, d_sm_ptr,
                     d_tiles, num_sms, o, lse, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" jfa_status jfa_fwd_pair(const void *q, const void *k, const void *v,
+                                   const void *offsets, jfa_index_t idx, int64_t B, int64_t T, int H,
+                                   int D, float scale, const int32_t *d_sm_ptr,
+                                   const int32_t *d_tiles, int num_pairs, void *o, float *lse,
+                                   void *workspace, size_t ws_bytes, jfa_stream_t stream) {
+  return fwd_common(q, k, v, offsets, offsets, idx, B, T, T, 0, H, D, scale, -1, -1, d_sm_ptr,
+                    d_tiles, num_pairs, o, lse, workspace, ws_bytes, (cudaStream_t)stream, 0, 0,
+                    true);
+}
+
+extern "C" jfa_status jfa_num_pairs(int *num_pairs) {
+  if (!num_pairs) return fail(JFA_ERR_INVALID_ARG, "num_pairs is NULL");
+  const int n = fwd_pair_max_clusters();
+  if (n < 1) return fail(JFA_ERR_UNSUPPORTED, "no cluster of two CTAs of the pair forward fits");
+  *num_pairs = n;
+  return JFA_OK;
 }
 
 extern "C" jfa_status jfa_fwd_dynamic(const void *q, const void *k, const void *v,

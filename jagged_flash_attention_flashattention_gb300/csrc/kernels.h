@@ -14,6 +14,7 @@ struct FwdParams {
   CUtensorMap tm_q;  // bf16 [rows, H, D] viewed as {D, H, rows}, box {64, 1, 128}, 128B swizzle
   CUtensorMap tm_k;  // bf16 [Tk, H, D], same box
   CUtensorMap tm_v;
+  CUtensorMap tm_khalf;   // CTA-pair forward: K viewed with 64-row boxes (one pair half of a K tile)
   const void *offsets;    // device [B+1]: K/V sequence bounds
   const void *q_offsets;  // device [B+1]: query sequence bounds (jagged; may equal offsets)
   int idx64;              // offsets are int64
@@ -52,6 +53,13 @@ struct FwdParams {
 constexpr size_t kAccZeroedOff = 128;
 
 cudaError_t launch_fwd(const FwdParams &p, int D, int num_sms, cudaStream_t st);
+
+// CTA-pair forward (jagged self-attention, D = 128, no band): clusters of two
+// CTAs, one per pair slot of the schedule (tiles of 512 query rows); grid =
+// 2 * num_pairs.
+cudaError_t launch_fwd_pair(const FwdParams &p, int num_pairs, cudaStream_t st);
+// Clusters of two that can be resident at once (0 if the pair kernel cannot run).
+int fwd_pair_max_clusters();
 
 // Device enumeration of the forward tiles for dynamic scheduling: writes
 // tile_base[0..B] from the device offsets (clamped like the kernels) and
