@@ -262,7 +262,8 @@ def _setup(name, rank, dev, seqs=0, zigzag=True):
     H, D = cfg["H"], cfg["D"]
     st = {"H": H, "D": D, "kind": cfg["kind"]}
     if cfg["kind"] == "jagged":
-        L = _gem_lengths(rank) if name == "gem" else W.lengths_for(name)
+        lname = cfg.get("lengths", name)
+        L = _gem_lengths(rank) if lname == "gem" else W.lengths_for(lname)
         if seqs:
             L = L[:seqs]
         off_host = W.offsets_of(L, cfg["offsets_dtype"])
@@ -278,6 +279,23 @@ def _setup(name, rank, dev, seqs=0, zigzag=True):
 
         def bwd():
             jfa.jfa_bwd(inp["q"], inp["k"], inp["v"], st["o"], st["lse"], inp["do"], off, plan=st["plan"])
+
+        if cfg.get("rotary"):
+            # rotary layer (q and k rotated at their positions in their
+            # sequences), forward on the rotated rows, and the backward with
+            # the rotary backward fused into its closing cast (dQ and dK)
+            cos, sin = W.rotary_tables(int(max(L)), D, device=dev)
+            st["desc"] += ", rotary (fp32 tables [max len, D/2])"
+
+            def fwd():  # noqa: F811
+                st["plan"] = jfa.Plan(off, H, D, host_offsets=off_host, workspace=ws_buf, zigzag=zigzag)
+                st["qr"] = jfa.jfa_rope(inp["q"], off, cos, sin, plan=st["plan"])
+                st["kr"] = jfa.jfa_rope(inp["k"], off, cos, sin, plan=st["plan"])
+                st["o"], st["lse"] = jfa.jfa_fwd(st["qr"], st["kr"], inp["v"], off, plan=st["plan"])
+
+            def bwd():  # noqa: F811
+                jfa.jfa_rotary_bwd(st["qr"], st["kr"], inp["v"], st["o"], st["lse"], inp["do"], off,
+                                   cos, sin, plan=st["plan"])
 
         st["check"] = lambda: st["plan"].check()
     elif cfg["kind"] == "varlen":
@@ -489,7 +507,7 @@ def _other_configs(args, dev, peaks):
     steps, warmup = max(3, min(args.steps, 10)), 3
     out = {}
     for name in ("stress", "bcast", "blockdiag", "blockdiag64", "blockdiag_rotary", "gem_causal",
-                 "gem_det"):
+                 "gem_det", "gem_rotary"):
         st = _setup(name, 0, dev)
         _, f_ms, b_ms, _ = _time_steps(st, steps, warmup, stream)
         ff, bf = st["fwd_flops"], st["bwd_flops"]
@@ -526,7 +544,9 @@ def _other_configs(args, dev, peaks):
         if name == "stress":
             out["pair_ab"] = {}
             for pname, pst in (("gem", None), ("stress", st)):
-                pst = pst or _setup("gem", 0, dev)
+                if pst is None:
+                    pst = _setup("gem", 0, dev)
+                    pst["fwd"]()  # builds the workload's plan (its host offsets)
                 pr = _pair_fwd_ms(pst, steps, warmup, stream)
                 # forward kernel alone on single CTAs against CTA pairs
                 # (cta_group::2 products, 512-row tiles)
@@ -810,7 +830,7 @@ def main():
                          "a small profiling case")
     ap.add_argument("--config", default="gem",
                     choices=["gem", "stress", "bcast", "blockdiag", "blockdiag64", "tiny",
-                             "gem_causal", "gem_det", "blockdiag_rotary"])
+                             "gem_causal", "gem_det", "blockdiag_rotary", "gem_rotary"])
     ap.add_argument("--schedule", default="zigzag", choices=["zigzag", "naive"],
                     help="tile order: host LPT + zigzag deal, or the unsorted round-robin deal")
     ap.add_argument("--no-configs", action="store_true",

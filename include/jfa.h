@@ -188,6 +188,35 @@ jfa_status jfa_fwd(const void *q, const void *k, const void *v, const void *offs
                    const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_sms, void *o,
                    float *lse, void *workspace, size_t ws_bytes, jfa_stream_t stream);
 
+/* Rotary embeddings for the jagged kernels ("TLX Block Attention", section 1:
+ * rotary embeddings fused into the attention backward's epilogue; the same
+ * "rotate half" reading as blockdiag_rotary_fwd, with each row's position
+ * counted from the start of its sequence). cos_t, sin_t: device fp32
+ * [rope_L, D/2]; a position past rope_L - 1 uses row rope_L - 1 (the binding
+ * refuses sequences longer than rope_L).
+ *
+ * jfa_rope: x_rot[r] = x[r] rotated at position r - offsets[b] of its
+ * sequence b (device bf16 [T, H, D]; x_rot may be x itself). The rotary
+ * forward of the layer: jfa_fwd then runs on the rotated q and k.
+ *
+ * jfa_rotary_bwd: jfa_bwd given the rotated q_rot, k_rot (and v, o, lse,
+ * dout as for jfa_bwd), whose dq, dk are the gradients with respect to the
+ * unrotated q, k: the backward's closing cast (which reads the fp32 dQ
+ * accumulator anyway) rotates dQ back (the transposed rotation) and, in the
+ * same pass, the rows of dK. Jagged self-attention without a band; the
+ * workspace, tiles and errors are those of jfa_bwd. */
+jfa_status jfa_rope(const void *x, const void *offsets, jfa_index_t idx, int64_t B, int64_t T,
+                    int H, int D, const float *cos_t, const float *sin_t, int64_t rope_L,
+                    void *x_rot, jfa_stream_t stream);
+
+jfa_status jfa_rotary_bwd(const void *q_rot, const void *k_rot, const void *v, const void *o,
+                          const float *lse, const void *dout, const void *offsets,
+                          jfa_index_t idx, int64_t B, int64_t T, int H, int D, float scale,
+                          const float *cos_t, const float *sin_t, int64_t rope_L,
+                          const int32_t *d_sm_ptr, const int32_t *d_tiles, int num_sms, void *dq,
+                          void *dk, void *dv, void *workspace, size_t ws_bytes,
+                          jfa_stream_t stream);
+
 /* Jagged forward on CTA pairs ("Desarrollo de Jagged Flash Attention para
  * el modelo GEM", "Optimización del proceso de Backward y dQ": the 2-CTA MMA
  * of FA4, to raise tensor-core utilisation). Same inputs, outputs and

@@ -44,7 +44,7 @@ EXPORTS = [
     "jfa_num_sms", "jfa_workspace_size", "jfa_workspace_init", "jfa_check_status", "jfa_fwd",
     "jfa_bwd", "jfa_bcastq_fwd", "jfa_bcastq_bwd", "blockdiag_fwd", "blockdiag_bwd",
     "jfa_bwd_noalloc", "jfa_noalloc_check_status", "jfa_selftest_wait_timeout",
-    "jfa_fwd_pair", "jfa_num_pairs",
+    "jfa_fwd_pair", "jfa_num_pairs", "jfa_rope", "jfa_rotary_bwd",
     "jfa_sched_size_varlen", "jfa_sched_build_varlen", "jfa_varlen_fwd", "jfa_varlen_bwd",
     "jfa_varlen_workspace_size", "jfa_fwd_dynamic", "jfa_fwd_dynamic_workspace_size",
     "blockdiag_rotary_fwd", "blockdiag_rotary_bwd",
@@ -103,6 +103,9 @@ def lib():
         "jfa_selftest_wait_timeout": ([P, SZ, ctypes.c_uint64, P], I),
         "jfa_fwd_pair": ([P, P, P, P, I, I64, I64, I, I, F, P, P, I, P, P, P, SZ, P], I),
         "jfa_num_pairs": ([P], I),
+        "jfa_rope": ([P, P, I, I64, I64, I, I, P, P, I64, P, P], I),
+        "jfa_rotary_bwd": ([P, P, P, P, P, P, P, I, I64, I64, I, I, F, P, P, I64, P, P, I, P, P, P,
+                            P, SZ, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -342,6 +345,52 @@ def jfa_fwd(q, k, v, offsets, scale=None, plan=None):
                              _scale(scale, D), _ptr(sp), _ptr(tl), plan.n_sms, _ptr(o), _ptr(lse),
                              _ptr(plan.workspace), plan.workspace.numel(), _stream()))
     return o, lse
+
+
+def _check_rope_tables(cos, sin, D, plan):
+    for t in (cos, sin):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.float32 and t.dim() == 2 and
+                t.shape[1] == D // 2 and t.shape[0] == cos.shape[0]):
+            raise ValueError("rotary tables must be contiguous fp32 CUDA tensors [L, D/2]")
+    lmax = int(np.max(np.diff(plan.host_offsets))) if plan.B > 0 else 0
+    if lmax > cos.shape[0]:
+        raise ValueError("a sequence of %d tokens is longer than the rotary tables (%d rows)"
+                         % (lmax, cos.shape[0]))
+
+
+def jfa_rope(x, offsets, cos, sin, plan=None):
+    """Rotary embedding of x [T, H, D] bf16 with each row at its position in its
+    sequence (tables cos, sin [L, D/2] fp32): returns x_rot. The rotary forward
+    of a layer whose attention then runs on the rotated q and k."""
+    _need_cuda(x)
+    T, H, D = x.shape
+    plan = plan or Plan(offsets, H, D)
+    plan.validate("jagged", offsets, T, H, D)
+    _check_rope_tables(cos, sin, D, plan)
+    y = torch.empty_like(x)
+    _check(lib().jfa_rope(_ptr(x), _ptr(offsets), plan.idx, plan.B, T, H, D, _ptr(cos), _ptr(sin),
+                          cos.shape[0], _ptr(y), _stream()))
+    return y
+
+
+def jfa_rotary_bwd(q_rot, k_rot, v, o, lse, do, offsets, cos, sin, scale=None, plan=None):
+    """Jagged backward from the rotated q_rot, k_rot (as jfa_rope writes them),
+    with the rotary backward fused in: returns (dq, dk, dv) with respect to the
+    unrotated q, k and v (dQ and dK rotated back in the backward's closing
+    cast of dQ)."""
+    _need_cuda(q_rot, k_rot, v, o, do)
+    T, H, D = q_rot.shape
+    plan = plan or Plan(offsets, H, D)
+    plan.validate("jagged", offsets, T, H, D)
+    _check_rope_tables(cos, sin, D, plan)
+    dq, dk, dv = torch.empty_like(q_rot), torch.empty_like(k_rot), torch.empty_like(v)
+    sp, tl = plan.bwd_sched
+    _check(lib().jfa_rotary_bwd(_ptr(q_rot), _ptr(k_rot), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                _ptr(offsets), plan.idx, plan.B, T, H, D, _scale(scale, D),
+                                _ptr(cos), _ptr(sin), cos.shape[0], _ptr(sp), _ptr(tl), plan.n_sms,
+                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(plan.workspace),
+                                plan.workspace.numel(), _stream()))
+    return dq, dk, dv
 
 
 def jfa_bwd(q, k, v, o, lse, do, offsets, scale=None, plan=None):

@@ -371,9 +371,17 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
                       int64_t Tk, int64_t Lq, int H, int D, float scale, int win_left,
                       int win_right, int det, const int32_t *sm_ptr, const int32_t *tiles,
                       int num_sms, void *dq, void *dk, void *dv, void *ws, size_t ws_bytes,
-                      cudaStream_t st) {
+                      cudaStream_t st, const float *cos_t = nullptr, const float *sin_t = nullptr,
+                      int64_t rope_L = 0) {
   JFA_TRY(check_dims(B, Tk, H, D));
   JFA_TRY(check_dims(B, q_rows, H, D));
+  if (cos_t || sin_t) {
+    JFA_TRY(need_ptr(cos_t, "cos"));
+    JFA_TRY(need_ptr(sin_t, "sin"));
+    if (rope_L < 1) return fail(JFA_ERR_INVALID_ARG, "rotary tables have %lld rows", (long long)rope_L);
+    if (Lq != 0 || det || win_left >= 0 || win_right >= 0)
+      return fail(JFA_ERR_UNSUPPORTED, "rotary backward: jagged self-attention without a band");
+  }
   JFA_TRY(check_window(win_left, win_right));
   if (idx != JFA_I32 && idx != JFA_I64) return fail(JFA_ERR_INVALID_ARG, "bad index type");
   if (!(scale > 0.f)) return fail(JFA_ERR_INVALID_ARG, "scale must be > 0");
@@ -454,6 +462,9 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = static_cast<uint32_t *>(ws);
   p.timeout_ns = kTimeoutNs;
+  p.cos_t = cos_t;
+  p.sin_t = sin_t;
+  p.rope_L = rope_L;
   if (det) {
     JFA_TRY(launch_status(launch_det_layout(p, det_base, qb_base, st), "deterministic layout"));
     if (Tk > 0) JFA_TRY(launch_status(launch_bwd(p, D, num_sms, st), "bwd launch"));
@@ -467,6 +478,7 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
                           "accumulator clear"));
   if (Tk > 0) JFA_TRY(launch_status(launch_bwd(p, D, num_sms, st), "bwd launch"));
   if (Lq > 0) return JFA_OK;
+  if (cos_t) return launch_status(launch_dq_convert_rope(p, acc, dq, acc_rows, D, st), "dq convert");
   return launch_status(launch_dq_convert(acc, dq, acc_rows, H, D, scale, p.status, st), "dq convert");
 }
 
@@ -481,6 +493,37 @@ extern "C" jfa_status jfa_bwd(const void *q, const void *k, const void *v, const
   return bwd_common(q, k, v, o, lse, dout, offsets, offsets, idx, B, T, T, 0, H, D, scale, -1, -1,
                     0, d_sm_ptr, d_tiles, num_sms, dq, dk, dv, workspace, ws_bytes,
                     (cudaStream_t)stream);
+}
+
+extern "C" jfa_status jfa_rotary_bwd(const void *q_rot, const void *k_rot, const void *v,
+                                     const void *o, const float *lse, const void *dout,
+                                     const void *offsets, jfa_index_t idx, int64_t B, int64_t T,
+                                     int H, int D, float scale, const float *cos_t,
+                                     const float *sin_t, int64_t rope_L, const int32_t *d_sm_ptr,
+                                     const int32_t *d_tiles, int num_sms, void *dq, void *dk,
+                                     void *dv, void *workspace, size_t ws_bytes,
+                                     jfa_stream_t stream) {
+  if (!cos_t || !sin_t) return fail(JFA_ERR_INVALID_ARG, "rotary tables are NULL");
+  return bwd_common(q_rot, k_rot, v, o, lse, dout, offsets, offsets, idx, B, T, T, 0, H, D, scale,
+                    -1, -1, 0, d_sm_ptr, d_tiles, num_sms, dq, dk, dv, workspace, ws_bytes,
+                    (cudaStream_t)stream, cos_t, sin_t, rope_L);
+}
+
+extern "C" jfa_status jfa_rope(const void *x, const void *offsets, jfa_index_t idx, int64_t B,
+                               int64_t T, int H, int D, const float *cos_t, const float *sin_t,
+                               int64_t rope_L, void *x_rot, jfa_stream_t stream) {
+  JFA_TRY(check_dims(B, T, H, D));
+  if (idx != JFA_I32 && idx != JFA_I64) return fail(JFA_ERR_INVALID_ARG, "bad index type");
+  if (rope_L < 1) return fail(JFA_ERR_INVALID_ARG, "rotary tables have %lld rows", (long long)rope_L);
+  JFA_TRY(need_ptr(cos_t, "cos"));
+  JFA_TRY(need_ptr(sin_t, "sin"));
+  JFA_TRY(need_ptr(offsets, "offsets"));
+  if (B == 0 || T == 0) return JFA_OK;
+  JFA_TRY(need_ptr(x, "x"));
+  JFA_TRY(need_ptr(x_rot, "x_rot"));
+  return cuda_status(launch_rope_rows(x, x_rot, T, H, D, offsets, idx == JFA_I64, B, cos_t, sin_t,
+                                      rope_L, (cudaStream_t)stream),
+                     "rope launch");
 }
 
 extern "C" jfa_status jfa_varlen_bwd(const void *q, const void *k, const void *v, const void *o,

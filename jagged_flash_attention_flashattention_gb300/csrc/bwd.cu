@@ -757,6 +757,124 @@ __global__ void dq_convert_kernel(const float4 *__restrict__ acc, uint4 *__restr
   }
 }
 
+// Positions (row - first row of its sequence) of rows [r0, r0 + n) into
+// pos[] in shared memory: thread 0 finds the first row's sequence by binary
+// search of the offsets and walks forward (offsets clamped to [0, T]).
+constexpr int kRopeChunk = 32;  // rows per block step of the rotary row kernels
+
+__device__ __forceinline__ void chunk_positions(const void *off, int idx64, int64_t B, int64_t T,
+                                                int64_t r0, int n, int *pos) {
+  if (threadIdx.x == 0) {
+    auto at = [&](int64_t b) { return min(max(load_off(off, idx64, (int)b), (int64_t)0), T); };
+    int64_t lo = 0, hi = B;  // the last b with offsets[b] <= r0
+    while (hi - lo > 1) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (at(mid) <= r0) lo = mid; else hi = mid;
+    }
+    int64_t b = lo, s = at(b), e = at(b + 1);
+    for (int i = 0; i < n; ++i) {
+      const int64_t r = r0 + i;
+      while (e <= r && b + 1 < B) {
+        ++b;
+        s = e;
+        e = at(b + 1);
+      }
+      pos[i] = (int)(r - s);
+    }
+  }
+  __syncthreads();
+}
+
+// As dq_convert_kernel, and each row's dQ rotated back (the transposed
+// rotation) at the row's position in its sequence; the same row of dK (bf16,
+// written by the backward kernel with respect to the rotated k) is rotated
+// back in place in the same pass. Item = 4 pairs (i, i + D/2) of one (row,
+// head).
+template <int D>
+__global__ void __launch_bounds__(256) dq_convert_rope_kernel(
+    const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, __nv_bfloat16 *__restrict__ dk,
+    int64_t rows, int H, float scale, const void *offsets, int idx64, int64_t B, int64_t T,
+    const float *cos_t, const float *sin_t, int64_t rope_L, uint32_t *status) {
+  __shared__ int pos_s[kRopeChunk];
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    *reinterpret_cast<volatile uint64_t *>(reinterpret_cast<uint8_t *>(status) + kAccZeroedOff) = 0;
+  constexpr int NQ = D / 8;  // 4-pair groups per (row, head)
+  const int per_row = H * NQ;
+  for (int64_t r0 = (int64_t)blockIdx.x * kRopeChunk; r0 < rows; r0 += (int64_t)gridDim.x * kRopeChunk) {
+    const int n = (int)min((int64_t)kRopeChunk, rows - r0);
+    chunk_positions(offsets, idx64, B, T, r0, n, pos_s);
+    for (int it = threadIdx.x; it < n * per_row; it += blockDim.x) {
+      const int rr = it / per_row, g = it % NQ;
+      const int64_t rh = (r0 + rr) * H + (it % per_row) / NQ;
+      const int64_t pos = min(max((int64_t)pos_s[rr], (int64_t)0), rope_L - 1);
+      const float4 cf = __ldg(reinterpret_cast<const float4 *>(cos_t + pos * (D / 2)) + g);
+      const float4 sf = __ldg(reinterpret_cast<const float4 *>(sin_t + pos * (D / 2)) + g);
+      const float4 a = *reinterpret_cast<const float4 *>(acc + rh * D + 4 * g);
+      const float4 b = *reinterpret_cast<const float4 *>(acc + rh * D + D / 2 + 4 * g);
+      const float l0 = (a.x * cf.x + b.x * sf.x) * scale, l1 = (a.y * cf.y + b.y * sf.y) * scale;
+      const float l2 = (a.z * cf.z + b.z * sf.z) * scale, l3 = (a.w * cf.w + b.w * sf.w) * scale;
+      const float h0 = (b.x * cf.x - a.x * sf.x) * scale, h1 = (b.y * cf.y - a.y * sf.y) * scale;
+      const float h2 = (b.z * cf.z - a.z * sf.z) * scale, h3 = (b.w * cf.w - a.w * sf.w) * scale;
+      *reinterpret_cast<uint2 *>(dq + rh * D + 4 * g) = make_uint2(pack_bf16(l0, l1), pack_bf16(l2, l3));
+      *reinterpret_cast<uint2 *>(dq + rh * D + D / 2 + 4 * g) =
+          make_uint2(pack_bf16(h0, h1), pack_bf16(h2, h3));
+      uint2 *kl = reinterpret_cast<uint2 *>(dk + rh * D + 4 * g);
+      uint2 *kh = reinterpret_cast<uint2 *>(dk + rh * D + D / 2 + 4 * g);
+      const uint2 ka = *kl, kb = *kh;
+      const float2 a01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ka.x));
+      const float2 a23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ka.y));
+      const float2 b01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kb.x));
+      const float2 b23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kb.y));
+      *kl = make_uint2(pack_bf16(a01.x * cf.x + b01.x * sf.x, a01.y * cf.y + b01.y * sf.y),
+                       pack_bf16(a23.x * cf.z + b23.x * sf.z, a23.y * cf.w + b23.y * sf.w));
+      *kh = make_uint2(pack_bf16(b01.x * cf.x - a01.x * sf.x, b01.y * cf.y - a01.y * sf.y),
+                       pack_bf16(b23.x * cf.z - a23.x * sf.z, b23.y * cf.w - a23.y * sf.w));
+    }
+    __syncthreads();  // pos_s is rewritten for the next chunk
+  }
+}
+
+// x_rot = x rotated at each row's position in its sequence (rotary "rotate
+// half"): item = 8 pairs (i, i + D/2) of one (row, head), in fp32, rounded
+// to bf16.
+template <int D>
+__global__ void __launch_bounds__(256) rope_rows_kernel(
+    const __nv_bfloat16 *__restrict__ x, __nv_bfloat16 *__restrict__ y, int64_t rows, int H,
+    const void *offsets, int idx64, int64_t B, int64_t T, const float *cos_t, const float *sin_t,
+    int64_t rope_L) {
+  __shared__ int pos_s[kRopeChunk];
+  constexpr int NQ = D / 16;  // 8-pair groups per (row, head)
+  const int per_row = H * NQ;
+  for (int64_t r0 = (int64_t)blockIdx.x * kRopeChunk; r0 < rows; r0 += (int64_t)gridDim.x * kRopeChunk) {
+    const int n = (int)min((int64_t)kRopeChunk, rows - r0);
+    chunk_positions(offsets, idx64, B, T, r0, n, pos_s);
+    for (int it = threadIdx.x; it < n * per_row; it += blockDim.x) {
+      const int rr = it / per_row, g = it % NQ;
+      const int64_t rh = (r0 + rr) * H + (it % per_row) / NQ;
+      const int64_t pos = min(max((int64_t)pos_s[rr], (int64_t)0), rope_L - 1);
+      const float4 *cp = reinterpret_cast<const float4 *>(cos_t + pos * (D / 2) + 8 * g);
+      const float4 *sp = reinterpret_cast<const float4 *>(sin_t + pos * (D / 2) + 8 * g);
+      const float4 c0 = __ldg(cp), c1 = __ldg(cp + 1), s0v = __ldg(sp), s1v = __ldg(sp + 1);
+      const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const float sn[8] = {s0v.x, s0v.y, s0v.z, s0v.w, s1v.x, s1v.y, s1v.z, s1v.w};
+      const uint4 a = *reinterpret_cast<const uint4 *>(x + rh * D + 8 * g);
+      const uint4 b = *reinterpret_cast<const uint4 *>(x + rh * D + D / 2 + 8 * g);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+      uint32_t ow[4], hw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 xl = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&aw[e]));
+        const float2 xh = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&bw[e]));
+        ow[e] = pack_bf16(xl.x * c[2 * e] - xh.x * sn[2 * e], xl.y * c[2 * e + 1] - xh.y * sn[2 * e + 1]);
+        hw[e] = pack_bf16(xh.x * c[2 * e] + xl.x * sn[2 * e], xh.y * c[2 * e + 1] + xl.y * sn[2 * e + 1]);
+      }
+      *reinterpret_cast<uint4 *>(y + rh * D + 8 * g) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      *reinterpret_cast<uint4 *>(y + rh * D + D / 2 + 8 * g) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    }
+    __syncthreads();  // pos_s is rewritten for the next chunk
+  }
+}
+
 // Sequence bounds exactly as decode_tile reads them (clamped to the tensors).
 __device__ __forceinline__ void seq_bounds(const BwdParams &p, int64_t b, int64_t *qs, int64_t *Lq,
                                            int64_t *Lk) {
@@ -915,6 +1033,37 @@ static int grid_for(int64_t n) {
 cudaError_t launch_acc_clear(float *acc, int64_t n16, const uint32_t *status, cudaStream_t st) {
   if (n16 == 0) return cudaSuccess;
   acc_clear_kernel<<<grid_for(n16), 256, 0, st>>>(acc, n16, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert_rope(const BwdParams &p, const float *acc, void *dq, int64_t rows,
+                                   int D, cudaStream_t st) {
+  auto *dkp = static_cast<__nv_bfloat16 *>(p.dk);
+  const int64_t n = (rows + kRopeChunk - 1) / kRopeChunk * 256;  // one 256-thread block per chunk
+  auto *out = static_cast<__nv_bfloat16 *>(dq);
+  if (D == 128)
+    dq_convert_rope_kernel<128><<<grid_for(n), 256, 0, st>>>(acc, out, dkp, rows, p.H, p.scale, p.offsets,
+                                                             p.idx64, p.B, p.T, p.cos_t, p.sin_t,
+                                                             p.rope_L, p.status);
+  else
+    dq_convert_rope_kernel<64><<<grid_for(n), 256, 0, st>>>(acc, out, dkp, rows, p.H, p.scale, p.offsets,
+                                                            p.idx64, p.B, p.T, p.cos_t, p.sin_t,
+                                                            p.rope_L, p.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_rows(const void *x, void *y, int64_t rows, int H, int D, const void *offsets,
+                             int idx64, int64_t B, const float *cos_t, const float *sin_t,
+                             int64_t rope_L, cudaStream_t st) {
+  const int64_t n = (rows + kRopeChunk - 1) / kRopeChunk * 256;  // one 256-thread block per chunk
+  const auto *xi = static_cast<const __nv_bfloat16 *>(x);
+  auto *yo = static_cast<__nv_bfloat16 *>(y);
+  if (D == 128)
+    rope_rows_kernel<128><<<grid_for(n), 256, 0, st>>>(xi, yo, rows, H, offsets, idx64, B, rows,
+                                                       cos_t, sin_t, rope_L);
+  else
+    rope_rows_kernel<64><<<grid_for(n), 256, 0, st>>>(xi, yo, rows, H, offsets, idx64, B, rows,
+                                                      cos_t, sin_t, rope_L);
   return cudaGetLastError();
 }
 

@@ -100,9 +100,25 @@ struct BwdParams {
   float scale_log2;
   uint32_t *status;
   uint64_t timeout_ns;
+  // Rotary (jagged self-attention, no band): fp32 tables [rope_L, D/2]; q and
+  // k are the rotated rows, and the closing cast rotates dQ and dK back by the
+  // transposed rotation at each row's position in its sequence. Null: no
+  // rotary.
+  const float *cos_t;
+  const float *sin_t;
+  int64_t rope_L;
 };
 
 cudaError_t launch_bwd(const BwdParams &p, int D, int num_sms, cudaStream_t st);
+// x_rot = x [rows, H, D] bf16 rotated at each row's position in its sequence
+// (offsets [B+1]; positions clamped to [0, rope_L)).
+cudaError_t launch_rope_rows(const void *x, void *y, int64_t rows, int H, int D, const void *offsets,
+                             int idx64, int64_t B, const float *cos_t, const float *sin_t,
+                             int64_t rope_L, cudaStream_t st);
+// The cast of launch_dq_convert with each row rotated back (p.cos_t, p.sin_t),
+// and the same rows of dK (p.dk, bf16) rotated back in place.
+cudaError_t launch_dq_convert_rope(const BwdParams &p, const float *acc, void *dq, int64_t rows,
+                                   int D, cudaStream_t st);
 
 // Zeroes the fp32 dQ accumulator (n16 units of 16 bytes) unless the status
 // block already records at least that many zero bytes.

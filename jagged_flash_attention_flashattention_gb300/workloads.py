@@ -30,7 +30,7 @@ import numpy as np
 import torch
 
 SEEDS = {"tiny": 1, "gem": 2, "stress": 3, "bcast": 4, "blockdiag": 5, "blockdiag64": 5,
-         "blockdiag_rotary": 5}
+         "blockdiag_rotary": 5, "gem_rotary": 2}
 
 
 def lengths_for(name, seed=None):
@@ -111,6 +111,10 @@ WORKLOADS = {
     "bcast": dict(kind="bcast", H=4, D=128, Lq=256, offsets_dtype=np.int64),
     "blockdiag": dict(kind="blockdiag", B=1152, L=4096, H=2, D=128),
     "blockdiag64": dict(kind="blockdiag", B=1152, L=4096, H=2, D=64),
+    # the GEM batch with rotary embeddings (rotary layer, forward, backward
+    # with the rotary backward fused in)
+    "gem_rotary": dict(kind="jagged", lengths="gem", H=4, D=128, offsets_dtype=np.int64,
+                       rotary=True),
     # the block-diagonal configuration with rotary embeddings fused in
     "blockdiag_rotary": dict(kind="blockdiag", B=1152, L=4096, H=2, D=128, rotary=True),
 }

@@ -50,7 +50,8 @@ per sequence and per head, with no blocking, fusion or online rescaling:
   q_r and k_r rotated back by the transposed rotation (rotation by -angle).
   The backward is also given from q_r and k_r themselves (the rotary
   layer's saved output), the form whose rotary part the page fuses into the
-  attention epilogue.
+  attention epilogue. The jagged form rotates each packed row at its
+  position counted from the start of its own sequence.
 
 * masked and cross (varlen) attention ([JFA-GEM] "Impacto en el desarrollo
   de modelos generativos": causal, sliding-window and block-sparse masks as
@@ -371,3 +372,40 @@ def blockdiag_rotary_bwd_from_rotated(q_r, k_r, v, do, cos, sin, scale, block=BL
     Returns dQ, dK, dV [B, L, H, D] with respect to the unrotated q, k and v."""
     dqr, dkr, dv = blockdiag_bwd(q_r, k_r, v, do, scale, block)
     return rope_transpose(dqr, cos, sin), rope_transpose(dkr, cos, sin), dv
+
+
+def jagged_rope(x, offsets, cos, sin):
+    """Rotary embedding of packed rows x [T, H, D], each row at its position
+    in its own sequence (row - offsets[b]); tables [L, D/2], L at least the
+    longest sequence. The jagged form of :func:`rope`."""
+    x = _f64(x)
+    out = np.empty_like(x)
+    for s, e in _bounds(offsets):
+        out[s:e] = rope(x[s:e][None], _f64(cos)[:e - s], _f64(sin)[:e - s])[0]
+    return out
+
+
+def jagged_rope_transpose(g, offsets, cos, sin):
+    """The transposed rotation of :func:`jagged_rope` (gradient of the rotated
+    rows to gradient of the unrotated ones)."""
+    g = _f64(g)
+    out = np.empty_like(g)
+    for s, e in _bounds(offsets):
+        out[s:e] = rope_transpose(g[s:e][None], _f64(cos)[:e - s], _f64(sin)[:e - s])[0]
+    return out
+
+
+def jagged_rotary_fwd(q, k, v, offsets, cos, sin, scale):
+    """Jagged attention on rotated q and k. Returns O, LSE."""
+    return jagged_fwd(jagged_rope(q, offsets, cos, sin), jagged_rope(k, offsets, cos, sin), v,
+                      offsets, scale)
+
+
+def jagged_rotary_bwd_from_rotated(q_r, k_r, v, do, offsets, cos, sin, scale):
+    """The combined attention-and-rotary backward on jagged sequences, taken
+    from the rotated q_r, k_r: the jagged attention backward on (q_r, k_r, v),
+    then the gradients of q_r and k_r rotated back. Returns dQ, dK, dV with
+    respect to the unrotated q, k and v."""
+    dqr, dkr, dv = jagged_bwd(q_r, k_r, v, do, offsets, scale)
+    return (jagged_rope_transpose(dqr, offsets, cos, sin),
+            jagged_rope_transpose(dkr, offsets, cos, sin), dv)

@@ -141,3 +141,47 @@ def test_backward_from_rotated_inputs_equals_backward_from_unrotated():
     plain = A.blockdiag_bwd(q, k, v, do, 0.3)
     dq_wrong = A.blockdiag_rotary_bwd_from_rotated(q, k, v, do, c, s, 0.3)[0]
     assert np.abs(dq_wrong - plain[0]).max() > 1e-3
+
+
+def test_jagged_rotary_on_64_token_sequences_equals_block_diagonal_rotary():
+    # Sequences of 64 tokens each: a row's position in its sequence is its
+    # index mod 64 and attention never crosses a 64-token block, so the
+    # jagged rotary forward and backward equal the block-diagonal ones.
+    rng = np.random.default_rng(88)
+    B, L, H, D = 3, 64, 2, 16
+    q, k, v, do = (_rand((B, L, H, D), rng) for _ in range(4))
+    c, s = _tables(L, D)
+    offs = np.arange(B + 1) * L
+    flat = lambda t: t.reshape(B * L, H, D)
+    o_j, _ = A.jagged_rotary_fwd(flat(q), flat(k), flat(v), offs, c, s, 0.3)
+    np.testing.assert_allclose(o_j, flat(A.blockdiag_rotary_fwd(q, k, v, c, s, 0.3)), atol=1e-12)
+    qr, kr = A.rope(q, c, s), A.rope(k, c, s)
+    np.testing.assert_allclose(A.jagged_rope(flat(q), offs, c, s), flat(qr), atol=1e-14)
+    got = A.jagged_rotary_bwd_from_rotated(flat(qr), flat(kr), flat(v), flat(do), offs, c, s, 0.3)
+    ref = A.blockdiag_rotary_bwd_from_rotated(qr, kr, v, do, c, s, 0.3)
+    for a, b in zip(got, ref):
+        np.testing.assert_allclose(a, flat(b), atol=1e-12)
+
+
+def test_jagged_rotary_backward_matches_finite_differences():
+    # d/dq of sum(O * dO) with O = attention(rope(q), rope(k), v) on ragged
+    # sequences (positions restart at every sequence start).
+    rng = np.random.default_rng(89)
+    lengths, H, D = [3, 5, 1], 1, 4
+    offs = np.concatenate([[0], np.cumsum(lengths)])
+    T = int(offs[-1])
+    q, k, v, do = (_rand((T, H, D), rng) for _ in range(4))
+    c, s = _tables(max(lengths), D)
+    sc = 0.7
+    grads = A.jagged_rotary_bwd_from_rotated(A.jagged_rope(q, offs, c, s), A.jagged_rope(k, offs, c, s),
+                                             v, do, offs, c, s, sc)
+    eps = 1e-6
+    for which, g in ((0, grads[0]), (1, grads[1])):
+        for idx in [(0, 0, 1), (4, 0, 3), (8, 0, 0)]:
+            args = [q.copy(), k.copy(), v]
+            args[which][idx] += eps
+            lp = float(np.sum(A.jagged_rotary_fwd(*args, offs, c, s, sc)[0] * do))
+            args[which][idx] -= 2 * eps
+            lm = float(np.sum(A.jagged_rotary_fwd(*args, offs, c, s, sc)[0] * do))
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(fd)), (which, idx, fd, g[idx])
