@@ -219,6 +219,8 @@ class Plan:
     are copied from the device once. Tile lists are copied to the device
     asynchronously from pinned memory. `workspace` (uint8 CUDA tensor) may be
     shared between plans; it is allocated when absent or too small.
+    `pair` (jagged, D = 128): the forward runs on CTA pairs (jfa_fwd_pair,
+    512-row tiles scheduled over jfa_num_pairs() slots); same results.
     """
 
     def __init__(self, offsets, H, D, kind="jagged", Lq=0, zigzag=True, host_offsets=None,

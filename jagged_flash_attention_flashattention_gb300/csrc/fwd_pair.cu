@@ -11,11 +11,13 @@
 // covers rows [256x, 256x + 256): rank 0 holds rows [256x, 256x + 128) and
 // rank 1 rows [256x + 128, 256x + 256), each in its own shared memory (Q)
 // and tensor memory (S, P, O). Every product is one M = 256 MMA issued by
-// rank 0, so each CTA reads only half of each K tile (64 keys) and half of
-// each V tile (64 of the 128 columns) from its own shared memory, and one
-// instruction does the work of two: per K/V step a CTA reads 96 KB of
-// operands and 32 KB of loads land, against 192 KB and 64 KB in the
-// single-CTA kernel, whose products are bound by shared-memory bandwidth.
+// rank 0, so each CTA loads only half of each K tile (64 keys) and half of
+// each V tile (64 of the 128 columns) into its own shared memory (32 KB of
+// loads per K/V step against 64 KB in the single-CTA kernel), and one
+// instruction does the work of two. Measured against the single-CTA forward
+// it is slower at the GEM and stress shapes (512-row tiles pad short
+// sequences more, and every step waits on the other SM), so it is offered
+// beside it rather than instead of it.
 //
 // Roles (384 threads in each CTA of the pair):
 //   warp 0       TMA producer of this CTA's halves: Q rows, and through a
