@@ -409,3 +409,70 @@ def jagged_rotary_bwd_from_rotated(q_r, k_r, v, do, offsets, cos, sin, scale):
     dqr, dkr, dv = jagged_bwd(q_r, k_r, v, do, offsets, scale)
     return (jagged_rope_transpose(dqr, offsets, cos, sin),
             jagged_rope_transpose(dkr, offsets, cos, sin), dv)
+
+
+# ----------------------------------------------------------- block-sparse masks
+SPARSE_BLOCK = 128  # query and key rows per mask block
+
+
+def block_visible(Lq, Lk, mask):
+    """Boolean [Lq, Lk] of a block mask ([JFA-GEM] "Impacto en el desarrollo
+    de modelos generativos": sparse-block masks on the jagged kernels; reading
+    used: mask[i // 128, j // 128] says whether query i of the sequence sees
+    key j, blocks counted from the start of the query and key sequences)."""
+    mask = np.asarray(mask, dtype=bool)
+    nqb, nkb = -(-Lq // SPARSE_BLOCK), -(-Lk // SPARSE_BLOCK)
+    assert mask.shape == (nqb, nkb), (mask.shape, nqb, nkb)
+    rows = np.arange(Lq) // SPARSE_BLOCK
+    cols = np.arange(Lk) // SPARSE_BLOCK
+    return mask[rows][:, cols]
+
+
+def _sparse_seq(Q, K, V, dO, scale, ok):
+    """Forward (and backward when dO is given) of one sequence and head under
+    the element mask `ok` [Lq, Lk]: the definitions of the module docstring
+    with masked scores at -inf; rows that see no key get O = 0, LSE = -inf
+    and no gradient."""
+    S = scale * (Q @ K.T)
+    P, lse = masked_softmax_rows(S, ok)
+    O = P @ V
+    if dO is None:
+        return O, lse
+    dV = P.T @ dO
+    dP = dO @ V.T
+    Di = np.sum(dO * O, axis=1, keepdims=True)
+    dS = P * (dP - Di)
+    return scale * dS @ K, scale * dS.T @ Q, dV
+
+
+def blocksparse_fwd(q, k, v, q_offsets, kv_offsets, masks, scale):
+    """Attention with a block mask per sequence (`masks[b]` of shape
+    [ceil(Lq_b / 128), ceil(Lk_b / 128)]), separate query and key offsets.
+    Returns O [Tq, H, D] and LSE [H, Tq]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Tq, H, _ = q.shape
+    o = np.zeros((Tq, H, v.shape[2]))
+    lse = np.full((H, Tq), -np.inf)
+    for b, ((qs, qe), (ks, ke)) in enumerate(zip(_bounds(q_offsets), _bounds(kv_offsets))):
+        if qe == qs or ke == ks:
+            continue
+        ok = block_visible(qe - qs, ke - ks, masks[b])
+        for h in range(H):
+            o[qs:qe, h], lse[h, qs:qe] = _sparse_seq(q[qs:qe, h], k[ks:ke, h], v[ks:ke, h], None,
+                                                     scale, ok)
+    return o, lse
+
+
+def blocksparse_bwd(q, k, v, do, q_offsets, kv_offsets, masks, scale):
+    """Backward of :func:`blocksparse_fwd`. Returns dQ, dK, dV."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    H = q.shape[1]
+    for b, ((qs, qe), (ks, ke)) in enumerate(zip(_bounds(q_offsets), _bounds(kv_offsets))):
+        if qe == qs or ke == ks:
+            continue
+        ok = block_visible(qe - qs, ke - ks, masks[b])
+        for h in range(H):
+            dq[qs:qe, h], dk[ks:ke, h], dv[ks:ke, h] = _sparse_seq(
+                q[qs:qe, h], k[ks:ke, h], v[ks:ke, h], do[qs:qe, h], scale, ok)
+    return dq, dk, dv

@@ -41,6 +41,8 @@ unbounded) reuse the same sort and deal; only a tile's rows and work change:
 Without a mask and with equal offsets this is the jagged schedule above.
 """
 
+import numpy as np
+
 
 def enumerate_tiles(lengths, H, tile_rows, fixed_rows=0, fixed_work=0):
     """All tiles in enumeration order, each as (b, h, m, work)."""
@@ -153,3 +155,57 @@ def _deal(tiles, num_sms, zigzag):
         flat.extend(lst)
         sm_ptr.append(len(flat))
     return sm_ptr, flat
+
+
+# ----------------------------------------------------------- block-sparse masks
+# Tiles of block-sparse attention (masks[b] [ceil(Lq/128), ceil(Lk/128)] of
+# oracle.attention.block_visible) and the lists the kernels walk:
+#
+# * forward tile (b, h, m): query blocks 2m and 2m+1 (its two 128-row
+#   halves); it walks the union of the key blocks either half sees, in
+#   increasing order, each entry with a bit per half; its work is the number
+#   of keys in those blocks;
+# * backward tile (b, h, n): key block n; it walks the 64-row query blocks qb
+#   (in increasing order) whose 128-row block qb // 2 sees it; its work is the
+#   number of query rows in them.
+
+
+def sparse_tiles(q_lengths, kv_lengths, H, op, masks):
+    """(b, h, m, work, entries) in enumeration order; entries are
+    (key block, sees0, sees1) for the forward, query blocks for the backward."""
+    out = []
+    for b, (Lq, Lk) in enumerate(zip(q_lengths, kv_lengths)):
+        mask = np.asarray(masks[b], dtype=bool)
+        nqb, nkb = -(-Lq // 128), -(-Lk // 128)
+        if op == "fwd":
+            n_m = -(-Lq // FWD_ROWS)
+            per = []
+            for m in range(n_m):
+                ent = []
+                for j in range(nkb):
+                    s0 = bool(mask[2 * m, j]) if 2 * m < nqb else False
+                    s1 = bool(mask[2 * m + 1, j]) if 2 * m + 1 < nqb else False
+                    if s0 or s1:
+                        ent.append((j, s0, s1))
+                work = sum(min(Lk, 128 * j + 128) - 128 * j for j, _, _ in ent)
+                per.append((work, ent))
+        else:
+            n_m = nkb
+            per = []
+            for n in range(n_m):
+                ent = [qb for qb in range(-(-Lq // 64)) if mask[qb // 2, n]]
+                work = sum(min(Lq, 64 * qb + 64) - 64 * qb for qb in ent)
+                per.append((work, ent))
+        for h in range(H):
+            for m in range(n_m):
+                out.append((b, h, m, per[m][0], per[m][1]))
+    return out
+
+
+def schedule_sparse(q_lengths, kv_lengths, H, op, num_sms, masks, zigzag=True):
+    """LPT + zigzag deal of the block-sparse tiles. Returns (sm_ptr, tiles,
+    lists): lists[i] are the entries of dealt tile i."""
+    tiles = sparse_tiles(q_lengths, kv_lengths, H, op, masks)
+    sm_ptr, flat = _deal([t[:4] for t in tiles], num_sms, zigzag)
+    key = {t[:3]: t[4] for t in tiles}
+    return sm_ptr, flat, [key[tuple(t)] for t in flat]
