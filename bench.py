@@ -323,6 +323,42 @@ def _setup(name, rank, dev, seqs=0, zigzag=True):
                                window=win, deterministic=det, plan=st["plan"])
 
         st["check"] = lambda: st["plan"].check()
+    elif cfg["kind"] == "sparse":
+        L = _gem_lengths(rank) if cfg["lengths"] == "gem" else W.lengths_for(cfg["lengths"])
+        if seqs:
+            L = L[:seqs]
+        off_host = W.offsets_of(L, cfg["offsets_dtype"])
+        masks = W.block_masks(L, L, W.MASK_SEEDS[name] + 1000 * rank, density=cfg["density"])
+        flat = jfa.pack_block_masks(masks, off_host, off_host)  # an input, like the host offsets
+        inp = W.jagged_inputs(L, H, D, W.SEEDS[name] + 1000 * rank, device=dev)
+        off = torch.from_numpy(off_host).to(dev)
+        ws_buf = jfa.Plan(off, H, D, kind="sparse", host_offsets=off_host, block_masks=flat).workspace
+        st["fwd_flops"] = W.useful_flops("sparse", L, H=H, D=D, masks=masks)
+        kept = sum(int(m.sum()) for m in masks)
+        st["desc"] = ("%s: B=%d, T=%d, H=%d, D=%d, block-causal 128x128 block masks, off-diagonal "
+                      "blocks kept with p=%.2f (%d of %d blocks)" % (
+                          name, len(L), int(off_host[-1]), H, D, cfg["density"], kept,
+                          sum(m.size for m in masks)))
+
+        def fwd():
+            st["plan"] = jfa.Plan(off, H, D, kind="sparse", host_offsets=off_host, block_masks=flat,
+                                  workspace=ws_buf, zigzag=zigzag)
+            kfwd()
+
+        def kfwd():
+            st["o"], st["lse"] = jfa.jfa_sparse_fwd(inp["q"], inp["k"], inp["v"], off, off,
+                                                    plan=st["plan"])
+
+        def bwd():
+            jfa.jfa_sparse_bwd(inp["q"], inp["k"], inp["v"], st["o"], st["lse"], inp["do"], off, off,
+                               plan=st["plan"])
+
+        # The kernels alone, on the plan of the last step: the block lists are
+        # built on the host in every step (about 3 ms for this batch), longer
+        # than the kernels, so the step times above include host time.
+        st["kernels"] = (kfwd, bwd)
+
+        st["check"] = lambda: st["plan"].check()
     elif cfg["kind"] == "bcast":
         L = W.lengths_for(name)
         Lq = cfg["Lq"]
@@ -496,6 +532,29 @@ def _pair_fwd_ms(st, steps, warmup, stream):
     return res
 
 
+def _kernel_ms(st, steps, warmup, stream):
+    """Median fwd and bwd times of a workload's kernel calls on a plan built
+    beforehand (st["kernels"]), each call bracketed by CUDA events."""
+    import torch
+
+    res = {}
+    for op, fn in zip(("fwd", "bwd"), st["kernels"]):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        _spin(stream)
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        res[op] = statistics.median(a.elapsed_time(b) for a, b in evs)
+    st["check"]()
+    return res
+
+
 def _other_configs(args, dev, peaks):
     """Every other workload of the method, each timed like the headline one
     (W warm-up and K timed fwd+bwd steps, CUDA events, median per op), plus the
@@ -507,7 +566,7 @@ def _other_configs(args, dev, peaks):
     steps, warmup = max(3, min(args.steps, 10)), 3
     out = {}
     for name in ("stress", "bcast", "blockdiag", "blockdiag64", "blockdiag_rotary", "gem_causal",
-                 "gem_det", "gem_rotary"):
+                 "gem_det", "gem_rotary", "gem_sparse"):
         st = _setup(name, 0, dev)
         _, f_ms, b_ms, _ = _time_steps(st, steps, warmup, stream)
         ff, bf = st["fwd_flops"], st["bwd_flops"]
@@ -521,6 +580,12 @@ def _other_configs(args, dev, peaks):
                 rec[op]["frac_of_hbm_peak"] = round(gbs / hbm_peak, 4)
             rec["bytes_note"] = ("modelled bytes (inputs read once, outputs written once) over "
                                  "the measured copy peak")
+        if "kernels" in st:  # step times include host-side planning: the kernels alone as well
+            km = _kernel_ms(st, steps, warmup, stream)
+            rec["kernels_only"] = {
+                "note": "plan (host block lists) built before the timed calls",
+                "fwd": dict(ms=round(km["fwd"], 4), **_fracs(ff / km["fwd"] / 1e9, tc_peak)),
+                "bwd": dict(ms=round(km["bwd"], 4), **_fracs(bf / km["bwd"] / 1e9, tc_peak))}
         out[name] = rec
         if name == "stress":
             dyn = _dynamic_fwd_ms(st, steps, warmup, stream)
@@ -621,7 +686,7 @@ def run_ours(args):
             "pct_of_spec_peak": round(100 * value / SPEC_BF16_TFLOPS, 2),
             "roofline": roof,
             "clocks": clk,
-            "gpu_launches": (4 if st["kind"] in ("jagged", "varlen") else 2) * args.steps,
+            "gpu_launches": (4 if st["kind"] in ("jagged", "varlen", "sparse") else 2) * args.steps,
         }
         if full_gem:
             line["targets"] = {
@@ -830,7 +895,8 @@ def main():
                          "a small profiling case")
     ap.add_argument("--config", default="gem",
                     choices=["gem", "stress", "bcast", "blockdiag", "blockdiag64", "tiny",
-                             "gem_causal", "gem_det", "blockdiag_rotary", "gem_rotary"])
+                             "gem_causal", "gem_det", "blockdiag_rotary", "gem_rotary",
+                             "gem_sparse"])
     ap.add_argument("--schedule", default="zigzag", choices=["zigzag", "naive"],
                     help="tile order: host LPT + zigzag deal, or the unsorted round-robin deal")
     ap.add_argument("--no-configs", action="store_true",

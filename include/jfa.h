@@ -127,6 +127,41 @@ jfa_status jfa_sched_build_varlen(int64_t B, int H, jfa_op op, int num_sms,
                                   jfa_index_t idx, int window_left, int window_right, int zigzag,
                                   int32_t *sm_ptr, int32_t *tiles);
 
+/* Scheduler for jfa_sparse_fwd / jfa_sparse_bwd: block-sparse attention
+ * with separate query and key/value offsets. host_masks holds, for each
+ * sequence b in order, a row-major [ceil(Lq_b / 128), ceil(Lk_b / 128)]
+ * byte array (non-zero: the 128 queries of that block row see the 128 keys
+ * of that block column), concatenated; n_mask = its total length, which must
+ * equal the sum of those sizes (JFA_ERR_INVALID_ARG otherwise).
+ *
+ * Forward (op = JFA_OP_FWD): tiles of 256 query rows (query blocks 2m and
+ * 2m + 1, the tile's two 128-row halves). Tile i walks list entries
+ * list[list_ptr[i] .. list_ptr[i + 1]): the key blocks that either half sees,
+ * in increasing order, each encoded as (key block) | (half 0 sees it) << 29
+ * | (half 1 sees it) << 30; meta[4 i .. 4 i + 3] = first step and one past
+ * the last step (indices into the tile's entries) that half 0, then half 1,
+ * sees ((0, 0) for a half that sees none). Work (the sort key) = the keys in
+ * the listed blocks.
+ *
+ * Backward (op = JFA_OP_BWD): tiles of one 128-key block; entries are the
+ * 64-row query blocks whose 128-row block sees the key block, increasing;
+ * work = the query rows in them; meta is not written (may be NULL).
+ *
+ * Sort, tie order and deal are those of jfa_sched_build; lists follow the
+ * dealt order of `tiles`. Sizes: sm_ptr [num_sms + 1], tiles [3 n_tiles],
+ * list_ptr [n_tiles + 1], list [n_entries], meta [4 n_tiles], all host
+ * int32 buffers owned by the caller. */
+jfa_status jfa_sched_size_sparse(int64_t B, int H, jfa_op op, const void *host_q_offsets,
+                                 const void *host_kv_offsets, jfa_index_t idx,
+                                 const uint8_t *host_masks, int64_t n_mask, int64_t *n_tiles,
+                                 int64_t *n_entries);
+
+jfa_status jfa_sched_build_sparse(int64_t B, int H, jfa_op op, int num_sms,
+                                  const void *host_q_offsets, const void *host_kv_offsets,
+                                  jfa_index_t idx, const uint8_t *host_masks, int64_t n_mask,
+                                  int zigzag, int32_t *sm_ptr, int32_t *tiles, int32_t *list_ptr,
+                                  int32_t *list, int32_t *meta);
+
 /* Rows per tile that the kernels of `op` expect from the scheduler. */
 jfa_status jfa_tile_rows(jfa_op op, int D, int *tile_rows);
 
@@ -334,6 +369,44 @@ jfa_status jfa_varlen_bwd(const void *q, const void *k, const void *v, const voi
 jfa_status jfa_varlen_workspace_size(int64_t B, const void *host_q_offsets,
                                      const void *host_kv_offsets, jfa_index_t idx, int H, int D,
                                      int deterministic, size_t *bytes);
+
+/* ------------------------------------------------------------------------
+ * Block-sparse attention.
+ *
+ * The third mask family that "Desarrollo de Jagged Flash Attention para el
+ * modelo GEM", section "Impacto en el desarrollo de modelos generativos",
+ * names for the jagged kernels. The pages give no mask format; the reading
+ * used: one mask of 128 x 128 blocks per sequence, blocks counted from the
+ * first query and the first key of the sequence, so query i sees key j iff
+ * mask_b[i / 128][j / 128] != 0 (the last block row and column cover the
+ * ragged tails). A query that sees no key gets O = 0, LSE = -inf and
+ * contributes no gradient; keys that no query sees get dK = dV = 0.
+ *
+ * Layouts as for jfa_varlen_fwd / jfa_varlen_bwd (q, o, dout, dq [Tq, H, D],
+ * k, v, dk, dv [Tk, H, D] bf16, LSE fp32 [H, Tq], q_offsets and kv_offsets
+ * [B+1]). The mask enters only through the schedule: d_sm_ptr, d_tiles,
+ * d_list_ptr, d_list (and, forward, d_meta) are device copies of
+ * jfa_sched_build_sparse's output for the same offsets, masks and op. The
+ * kernels clamp every listed block to its sequence: a list of another batch
+ * gives wrong numbers but touches no memory outside the tensors. The
+ * backward sums dQ in the fp32 accumulator of jfa_varlen_bwd's
+ * non-deterministic workspace (jfa_varlen_workspace_size with
+ * deterministic = 0); there is no deterministic mode here.
+ * ---------------------------------------------------------------------- */
+jfa_status jfa_sparse_fwd(const void *q, const void *k, const void *v, const void *q_offsets,
+                          const void *kv_offsets, jfa_index_t idx, int64_t B, int64_t Tq,
+                          int64_t Tk, int H, int D, float scale, const int32_t *d_sm_ptr,
+                          const int32_t *d_tiles, const int32_t *d_list_ptr,
+                          const int32_t *d_list, const int32_t *d_meta, int num_sms, void *o,
+                          float *lse, void *workspace, size_t ws_bytes, jfa_stream_t stream);
+
+jfa_status jfa_sparse_bwd(const void *q, const void *k, const void *v, const void *o,
+                          const float *lse, const void *dout, const void *q_offsets,
+                          const void *kv_offsets, jfa_index_t idx, int64_t B, int64_t Tq,
+                          int64_t Tk, int H, int D, float scale, const int32_t *d_sm_ptr,
+                          const int32_t *d_tiles, const int32_t *d_list_ptr,
+                          const int32_t *d_list, int num_sms, void *dq, void *dk, void *dv,
+                          void *workspace, size_t ws_bytes, jfa_stream_t stream);
 
 /* jfa_bwd without a workspace argument. The paper has no counterpart: this
  * entry point exists for callers that cannot allocate device memory when

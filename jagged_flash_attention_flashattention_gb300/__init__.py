@@ -16,6 +16,8 @@ Functions mirror the C entry points:
 * :func:`jfa_varlen_fwd`, :func:`jfa_varlen_bwd` -- separate query and
   key/value offsets (jagged cross attention), an optional band mask
   (causal, sliding window) and an optional deterministic dQ reduction;
+* :func:`jfa_sparse_fwd`, :func:`jfa_sparse_bwd` -- block-sparse masks of
+  128 x 128 blocks per sequence, with separate query and key/value offsets;
 * :func:`blockdiag_fwd`, :func:`blockdiag_bwd` -- 64-token block-diagonal
   attention on ``[B, L, H, D]``;
 * :func:`schedule` -- the host LPT + zigzag tile scheduler.
@@ -48,6 +50,7 @@ EXPORTS = [
     "jfa_sched_size_varlen", "jfa_sched_build_varlen", "jfa_varlen_fwd", "jfa_varlen_bwd",
     "jfa_varlen_workspace_size", "jfa_fwd_dynamic", "jfa_fwd_dynamic_workspace_size",
     "blockdiag_rotary_fwd", "blockdiag_rotary_bwd",
+    "jfa_sched_size_sparse", "jfa_sched_build_sparse", "jfa_sparse_fwd", "jfa_sparse_bwd",
 ]
 
 
@@ -106,6 +109,12 @@ def lib():
         "jfa_rope": ([P, P, I, I64, I64, I, I, P, P, I64, P, P], I),
         "jfa_rotary_bwd": ([P, P, P, P, P, P, P, I, I64, I64, I, I, F, P, P, I64, P, P, I, P, P, P,
                             P, SZ, P], I),
+        "jfa_sched_size_sparse": ([I64, I, I, P, P, I, P, I64, P, P], I),
+        "jfa_sched_build_sparse": ([I64, I, I, I, P, P, I, P, I64, I, P, P, P, P, P], I),
+        "jfa_sparse_fwd": ([P, P, P, P, P, I, I64, I64, I64, I, I, F, P, P, P, P, P, I, P, P, P, SZ,
+                            P], I),
+        "jfa_sparse_bwd": ([P, P, P, P, P, P, P, P, I, I64, I64, I64, I, I, F, P, P, P, P, I, P, P,
+                            P, P, SZ, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -206,6 +215,69 @@ def schedule_varlen(q_offsets_host, kv_offsets_host, H, op, n_sms, window=(-1, -
     return sm_ptr, tiles[: n.value]
 
 
+SPARSE_BLOCK = 128  # query and key rows per block of a block mask
+
+
+def pack_block_masks(masks, q_offsets_host, kv_offsets_host):
+    """The scheduler's mask array from one boolean (or 0/1) array per sequence,
+    masks[b] of shape [ceil(Lq_b / 128), ceil(Lk_b / 128)] (row-major,
+    concatenated, uint8), or a flat array already in that layout (checked
+    for length)."""
+    qo = np.asarray(q_offsets_host, dtype=np.int64)
+    ko = np.asarray(kv_offsets_host, dtype=np.int64)
+    nq = -(-np.diff(qo) // SPARSE_BLOCK)
+    nk = -(-np.diff(ko) // SPARSE_BLOCK)
+    need = int(np.sum(nq * nk))
+    if isinstance(masks, np.ndarray) and masks.ndim == 1:
+        # already packed: used as is when it is contiguous uint8 (any non-zero byte is a kept block)
+        flat = masks if masks.dtype == np.uint8 else (masks != 0).astype(np.uint8)
+        flat = np.ascontiguousarray(flat)
+    else:
+        if len(masks) != len(nq):
+            raise ValueError("%d block masks for %d sequences" % (len(masks), len(nq)))
+        arrs = [np.asarray(m) for m in masks]
+        shapes = np.array([m.shape if m.ndim == 2 else (-1, -1) for m in arrs], dtype=np.int64)
+        bad = np.flatnonzero((shapes[:, 0] != nq) | (shapes[:, 1] != nk)) if arrs else []
+        if len(bad):
+            b = int(bad[0])
+            raise ValueError("block mask %d has shape %s, its sequence needs %s" % (
+                b, arrs[b].shape, (int(nq[b]), int(nk[b]))))
+        flat = (np.concatenate([m.ravel() for m in arrs]) != 0).view(np.uint8) if arrs \
+            else np.zeros(0, np.uint8)
+    if flat.size != need:
+        raise ValueError("block masks hold %d blocks, the offsets need %d" % (flat.size, need))
+    return flat
+
+
+def schedule_sparse(q_offsets_host, kv_offsets_host, H, op, n_sms, masks, zigzag=True):
+    """Host LPT + zigzag schedule of block-sparse tiles (op = OP_FWD or
+    OP_BWD) and their lists. `masks`: as for :func:`pack_block_masks`.
+    Returns (sm_ptr, tiles [n, 3], list_ptr [n + 1], entries, meta [n, 4] or
+    None for the backward), int32 numpy."""
+    qo = np.ascontiguousarray(q_offsets_host)
+    ko = np.ascontiguousarray(kv_offsets_host)
+    if qo.dtype != ko.dtype or ko.dtype not in (np.int32, np.int64):
+        raise ValueError("offsets must both be int32 or both int64")
+    idx = JFA_I64 if ko.dtype == np.int64 else JFA_I32
+    flat = pack_block_masks(masks, qo, ko)
+    B = ko.size - 1
+    n, ne = ctypes.c_int64(0), ctypes.c_int64(0)
+    L = lib()
+    _check(L.jfa_sched_size_sparse(B, H, op, qo.ctypes.data, ko.ctypes.data, idx, flat.ctypes.data,
+                                   flat.size, ctypes.byref(n), ctypes.byref(ne)))
+    sm_ptr = np.zeros(n_sms + 1, dtype=np.int32)
+    tiles = np.zeros((max(n.value, 1), 3), dtype=np.int32)
+    list_ptr = np.zeros(n.value + 1, dtype=np.int32)
+    entries = np.zeros(max(ne.value, 1), dtype=np.int32)
+    meta = np.zeros((max(n.value, 1), 4), dtype=np.int32)
+    _check(L.jfa_sched_build_sparse(B, H, op, n_sms, qo.ctypes.data, ko.ctypes.data, idx,
+                                    flat.ctypes.data, flat.size, 1 if zigzag else 0,
+                                    sm_ptr.ctypes.data, tiles.ctypes.data, list_ptr.ctypes.data,
+                                    entries.ctypes.data, meta.ctypes.data))
+    return (sm_ptr, tiles[: n.value], list_ptr, entries,
+            meta[: n.value] if op == OP_FWD else None)
+
+
 class Plan:
     """Schedules (on the device) and workspace for one batch layout.
 
@@ -221,11 +293,15 @@ class Plan:
     shared between plans; it is allocated when absent or too small.
     `pair` (jagged, D = 128): the forward runs on CTA pairs (jfa_fwd_pair,
     512-row tiles scheduled over jfa_num_pairs() slots); same results.
+    kind "sparse": as "varlen" without a window, plus `block_masks` (one
+    [ceil(Lq_b / 128), ceil(Lk_b / 128)] boolean array per sequence, see
+    :func:`pack_block_masks`); the schedules then carry the per-tile block
+    lists.
     """
 
     def __init__(self, offsets, H, D, kind="jagged", Lq=0, zigzag=True, host_offsets=None,
                  workspace=None, q_offsets=None, host_q_offsets=None, window=(-1, -1),
-                 deterministic=False, pair=False):
+                 deterministic=False, pair=False, block_masks=None):
         if not offsets.is_cuda:
             raise ValueError("offsets must be a CUDA tensor")
         self.offsets = offsets
@@ -240,7 +316,7 @@ class Plan:
         self.deterministic = bool(deterministic)
         self.n_sms = num_sms()
         dev = offsets.device
-        if kind == "varlen":
+        if kind in ("varlen", "sparse"):
             self.q_offsets = offsets if q_offsets is None else q_offsets
             if self.q_offsets.dtype != offsets.dtype:
                 raise ValueError("q_offsets and offsets must have the same dtype")
@@ -253,7 +329,17 @@ class Plan:
             check_host_offsets(hq, self.q_offsets.numel())
             self.host_q_offsets = hq
             self.Tq = int(hq[-1])
-        if kind == "varlen":
+        if kind == "sparse":
+            if block_masks is None:
+                raise ValueError("a sparse plan needs block_masks")
+            if self.window != (-1, -1) or self.deterministic:
+                raise ValueError("block masks take no window and no deterministic dQ")
+            flat = pack_block_masks(block_masks, self.host_q_offsets, host)
+            f = schedule_sparse(self.host_q_offsets, host, H, OP_FWD, self.n_sms, flat, zigzag)
+            bwd = schedule_sparse(self.host_q_offsets, host, H, OP_BWD, self.n_sms, flat, zigzag)[:4]
+            # (sm_ptr, tiles, list_ptr, entries, meta); meta keeps one row when there are no tiles
+            fwd = f[:4] + (f[4] if f[4].size else np.zeros((1, 4), np.int32),)
+        elif kind == "varlen":
             fwd = schedule_varlen(self.host_q_offsets, host, H, OP_FWD, self.n_sms, self.window,
                                   zigzag)
             bwd = schedule_varlen(self.host_q_offsets, host, H, OP_BWD, self.n_sms, self.window,
@@ -274,11 +360,12 @@ class Plan:
                            zigzag=zigzag)
             bwd = schedule(host, H, tile_rows(OP_BCASTQ_BWD, D), self.n_sms, fixed_work=self.Lq,
                            zigzag=zigzag)
-        self._pinned = [torch.from_numpy(a).pin_memory() for a in fwd + bwd]
+        self._pinned = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in fwd + bwd]
         d = [t.to(dev, non_blocking=True) for t in self._pinned]
-        self.fwd_sched, self.bwd_sched = (d[0], d[1]), (d[2], d[3])
+        nf = len(fwd)
+        self.fwd_sched, self.bwd_sched = tuple(d[:nf]), tuple(d[nf:])
         self.n_fwd_tiles, self.n_bwd_tiles = fwd[1].shape[0], bwd[1].shape[0]
-        if kind == "varlen":
+        if kind in ("varlen", "sparse"):
             sz = ctypes.c_size_t(0)
             hq = np.ascontiguousarray(self.host_q_offsets)
             hk = np.ascontiguousarray(host)
@@ -452,6 +539,58 @@ def jfa_varlen_bwd(q, k, v, o, lse, do, q_offsets, kv_offsets, scale=None, windo
                                 _scale(scale, D), int(window[0]), int(window[1]),
                                 1 if deterministic else 0, _ptr(sp), _ptr(tl), plan.n_sms,
                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(plan.workspace),
+                                plan.workspace.numel(), _stream()))
+    return dq, dk, dv
+
+
+def _check_sparse_plan(plan, q_offsets, kv_offsets, Tq, Tk, H, D):
+    if plan is None or plan.kind != "sparse":
+        raise ValueError("a block-sparse call needs a plan of kind 'sparse' (it holds the masks)")
+    if (plan.B, plan.T, plan.Tq, plan.H, plan.D) != (kv_offsets.numel() - 1, Tk, Tq, H, D):
+        raise ValueError("plan built for (B, Tk, Tq, H, D) = %s, call has %s" % (
+            (plan.B, plan.T, plan.Tq, plan.H, plan.D), (kv_offsets.numel() - 1, Tk, Tq, H, D)))
+    if q_offsets.numel() != kv_offsets.numel():
+        raise ValueError("q_offsets and kv_offsets must have the same length")
+
+
+def jfa_sparse_fwd(q, k, v, q_offsets, kv_offsets, block_masks=None, scale=None, plan=None):
+    """Block-sparse attention forward: query i of sequence b sees key j iff
+    block_masks[b][i // 128, j // 128]. q [Tq, H, D], k, v [Tk, H, D] bf16
+    CUDA; q_offsets, kv_offsets [B+1] (same dtype). Pass block_masks, or a
+    plan of kind "sparse" built with them. Returns (o [Tq, H, D] bf16,
+    lse [H, Tq] fp32); rows that see no key get O = 0, LSE = -inf."""
+    _need_cuda(q, k, v)
+    Tq, H, D = q.shape
+    Tk = k.shape[0]
+    if plan is None:
+        plan = Plan(kv_offsets, H, D, kind="sparse", q_offsets=q_offsets, block_masks=block_masks)
+    _check_sparse_plan(plan, q_offsets, kv_offsets, Tq, Tk, H, D)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device)
+    sp, tl, lp, ent, meta = plan.fwd_sched
+    _check(lib().jfa_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(q_offsets), _ptr(kv_offsets),
+                                plan.idx, plan.B, Tq, Tk, H, D, _scale(scale, D), _ptr(sp), _ptr(tl),
+                                _ptr(lp), _ptr(ent), _ptr(meta), plan.n_sms, _ptr(o), _ptr(lse),
+                                _ptr(plan.workspace), plan.workspace.numel(), _stream()))
+    return o, lse
+
+
+def jfa_sparse_bwd(q, k, v, o, lse, do, q_offsets, kv_offsets, block_masks=None, scale=None,
+                   plan=None):
+    """Backward of :func:`jfa_sparse_fwd`. Returns (dq, dk, dv) bf16; keys that
+    no query sees get dK = dV = 0."""
+    _need_cuda(q, k, v, o, do)
+    Tq, H, D = q.shape
+    Tk = k.shape[0]
+    if plan is None:
+        plan = Plan(kv_offsets, H, D, kind="sparse", q_offsets=q_offsets, block_masks=block_masks)
+    _check_sparse_plan(plan, q_offsets, kv_offsets, Tq, Tk, H, D)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    sp, tl, lp, ent = plan.bwd_sched
+    _check(lib().jfa_sparse_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                _ptr(q_offsets), _ptr(kv_offsets), plan.idx, plan.B, Tq, Tk, H, D,
+                                _scale(scale, D), _ptr(sp), _ptr(tl), _ptr(lp), _ptr(ent),
+                                plan.n_sms, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(plan.workspace),
                                 plan.workspace.numel(), _stream()))
     return dq, dk, dv
 

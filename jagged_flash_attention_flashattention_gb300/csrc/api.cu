@@ -207,7 +207,9 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *k
                       int64_t Tk, int64_t Lq, int H, int D, float scale, int win_left,
                       int win_right, const int32_t *sm_ptr, const int32_t *tiles, int num_sms,
                       void *o, float *lse, void *ws, size_t ws_bytes, cudaStream_t st,
-                      int dyn = 0, int64_t n_dyn_tiles = 0, bool pair = false) {
+                      int dyn = 0, int64_t n_dyn_tiles = 0, bool pair = false,
+                      const int32_t *blk_ptr = nullptr, const int32_t *blk_list = nullptr,
+                      const int32_t *blk_meta = nullptr) {
   JFA_TRY(check_dims(B, Tk, H, D));
   JFA_TRY(check_dims(B, q_rows, H, D));
   JFA_TRY(check_window(win_left, win_right));
@@ -224,6 +226,12 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *k
   if (B == 0 || q_rows == 0) return JFA_OK;
   if (dyn == 0) JFA_TRY(check_sched(sm_ptr, tiles, num_sms));
   if (dyn == 1 && n_dyn_tiles > 0 && !tiles) return fail(JFA_ERR_INVALID_ARG, "tiles is NULL");
+  if (blk_ptr || blk_list || blk_meta) {
+    if (!blk_ptr || !blk_list || !blk_meta)
+      return fail(JFA_ERR_INVALID_ARG, "list_ptr, list and meta must all be given");
+    if (Lq != 0 || dyn != 0 || pair || win_left >= 0 || win_right >= 0)
+      return fail(JFA_ERR_UNSUPPORTED, "block masks: jagged layouts without a band");
+  }
   JFA_TRY(need_ptr(q, "q"));
   JFA_TRY(need_ptr(o, "o"));
   JFA_TRY(need_ptr(lse, "lse"));
@@ -256,6 +264,9 @@ jfa_status fwd_common(const void *q, const void *k, const void *v, const void *k
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = static_cast<uint32_t *>(ws);
   p.timeout_ns = kTimeoutNs;
+  p.blk_ptr = blk_ptr;
+  p.blk_list = blk_list;
+  p.blk_meta = reinterpret_cast<const int4 *>(blk_meta);
   // A workspace sized for the jagged backward: clear its dQ accumulator here,
   // on the forward kernel's idle warps, instead of in a pass of its own.
   const size_t acc_bytes = (size_t)q_rows * H * D * sizeof(float);
@@ -372,7 +383,8 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
                       int win_right, int det, const int32_t *sm_ptr, const int32_t *tiles,
                       int num_sms, void *dq, void *dk, void *dv, void *ws, size_t ws_bytes,
                       cudaStream_t st, const float *cos_t = nullptr, const float *sin_t = nullptr,
-                      int64_t rope_L = 0) {
+                      int64_t rope_L = 0, const int32_t *blk_ptr = nullptr,
+                      const int32_t *blk_list = nullptr) {
   JFA_TRY(check_dims(B, Tk, H, D));
   JFA_TRY(check_dims(B, q_rows, H, D));
   if (cos_t || sin_t) {
@@ -383,6 +395,11 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
       return fail(JFA_ERR_UNSUPPORTED, "rotary backward: jagged self-attention without a band");
   }
   JFA_TRY(check_window(win_left, win_right));
+  if (blk_ptr || blk_list) {
+    if (!blk_ptr || !blk_list) return fail(JFA_ERR_INVALID_ARG, "list_ptr and list must both be given");
+    if (Lq != 0 || det || win_left >= 0 || win_right >= 0 || cos_t)
+      return fail(JFA_ERR_UNSUPPORTED, "block masks: jagged layouts without a band or deterministic dQ");
+  }
   if (idx != JFA_I32 && idx != JFA_I64) return fail(JFA_ERR_INVALID_ARG, "bad index type");
   if (!(scale > 0.f)) return fail(JFA_ERR_INVALID_ARG, "scale must be > 0");
   if (det && Lq > 0) return fail(JFA_ERR_UNSUPPORTED, "deterministic dQ is for the jagged layouts");
@@ -465,6 +482,8 @@ jfa_status bwd_common(const void *q, const void *k, const void *v, const void *o
   p.cos_t = cos_t;
   p.sin_t = sin_t;
   p.rope_L = rope_L;
+  p.blk_ptr = blk_ptr;
+  p.blk_list = blk_list;
   if (det) {
     JFA_TRY(launch_status(launch_det_layout(p, det_base, qb_base, st), "deterministic layout"));
     if (Tk > 0) JFA_TRY(launch_status(launch_bwd(p, D, num_sms, st), "bwd launch"));
@@ -537,6 +556,37 @@ extern "C" jfa_status jfa_varlen_bwd(const void *q, const void *k, const void *v
   return bwd_common(q, k, v, o, lse, dout, kv_offsets, q_offsets, idx, B, Tq, Tk, 0, H, D, scale,
                     window_left, window_right, deterministic ? 1 : 0, d_sm_ptr, d_tiles, num_sms,
                     dq, dk, dv, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" jfa_status jfa_sparse_fwd(const void *q, const void *k, const void *v,
+                                     const void *q_offsets, const void *kv_offsets,
+                                     jfa_index_t idx, int64_t B, int64_t Tq, int64_t Tk, int H,
+                                     int D, float scale, const int32_t *d_sm_ptr,
+                                     const int32_t *d_tiles, const int32_t *d_list_ptr,
+                                     const int32_t *d_list, const int32_t *d_meta, int num_sms,
+                                     void *o, float *lse, void *workspace, size_t ws_bytes,
+                                     jfa_stream_t stream) {
+  JFA_TRY(need_ptr(d_list_ptr, "list_ptr"));
+  JFA_TRY(need_ptr(d_list, "list"));
+  JFA_TRY(need_ptr(d_meta, "meta"));
+  return fwd_common(q, k, v, kv_offsets, q_offsets, idx, B, Tq, Tk, 0, H, D, scale, -1, -1,
+                    d_sm_ptr, d_tiles, num_sms, o, lse, workspace, ws_bytes, (cudaStream_t)stream,
+                    0, 0, false, d_list_ptr, d_list, d_meta);
+}
+
+extern "C" jfa_status jfa_sparse_bwd(const void *q, const void *k, const void *v, const void *o,
+                                     const float *lse, const void *dout, const void *q_offsets,
+                                     const void *kv_offsets, jfa_index_t idx, int64_t B,
+                                     int64_t Tq, int64_t Tk, int H, int D, float scale,
+                                     const int32_t *d_sm_ptr, const int32_t *d_tiles,
+                                     const int32_t *d_list_ptr, const int32_t *d_list,
+                                     int num_sms, void *dq, void *dk, void *dv, void *workspace,
+                                     size_t ws_bytes, jfa_stream_t stream) {
+  JFA_TRY(need_ptr(d_list_ptr, "list_ptr"));
+  JFA_TRY(need_ptr(d_list, "list"));
+  return bwd_common(q, k, v, o, lse, dout, kv_offsets, q_offsets, idx, B, Tq, Tk, 0, H, D, scale,
+                    -1, -1, 0, d_sm_ptr, d_tiles, num_sms, dq, dk, dv, workspace, ws_bytes,
+                    (cudaStream_t)stream, nullptr, nullptr, 0, d_list_ptr, d_list);
 }
 
 extern "C" jfa_status jfa_varlen_workspace_size(int64_t B, const void *host_q_offsets,

@@ -109,6 +109,7 @@ struct BwdTile {
   int Lq;             // query rows of the sequence
   int64_t lse0;       // LSE index of query row 0 (jagged: + h*Tq; bcast: (b*H+h)*Lq)
   int prow0;          // deterministic dQ: partial row of query row 0 for this key block
+  int lst;            // block-sparse: the tile's first list entry
 };
 
 __device__ __forceinline__ int64_t load_off(const void *off, int idx64, int i) {
@@ -155,7 +156,23 @@ __device__ __forceinline__ BwdTile decode_tile(const BwdParams &p, int t) {
     d.lse0 = (int64_t)d.h * p.Tq + qs;
     if (GEN && p.det && d.nq > 0) d.prow0 = (int)(p.det_base[d.b] + (int64_t)n * ((d.Lq + 63) / 64 * 64));
   }
+  d.lst = 0;
+  if (GEN && p.blk_ptr != nullptr) {  // block-sparse: the query blocks of the tile's list
+    d.lst = p.blk_ptr[t];
+    d.qb0 = 0;
+    d.nq = d.nkv > 0 ? min(max(p.blk_ptr[t + 1] - d.lst, 0), (d.Lq + 63) / 64) : 0;
+  }
   return d;
+}
+
+// Query block (of 64 rows, counted in the sequence) of the tile's i-th step:
+// consecutive from qb0, or the i-th list entry (clamped to the sequence)
+// with a block mask.
+template <bool GEN>
+__device__ __forceinline__ int query_block(const BwdParams &p, const BwdTile &tl, int i) {
+  if (GEN && p.blk_ptr != nullptr)
+    return min((int)((uint32_t)__ldg(p.blk_list + tl.lst + i) & 0xffffffu), max((tl.Lq + 63) / 64 - 1, 0));
+  return tl.qb0 + i;
 }
 
 // Walks the (tile, query block) sequence of one CTA, skipping empty tiles.
@@ -267,7 +284,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
         }
         for (int i = 0; i < tl.nq; ++i, ++qb) {
           const int s = qb % C::NSTAGE;
-          const int qr = (tl.qb0 + i) * 64;  // first query row of the block in the sequence
+          const int qr = query_block<GEN>(p, tl, i) * 64;  // first query row of the block in the sequence
           if (!mbar_wait(&bars.stage_empty[s], bit(eph, s) ^ 1, ctl, 2)) goto drain;
           eph ^= 1u << s;
           mbar_arrive_expect_tx(&bars.stage_full[s], 2 * C::QT);
@@ -454,6 +471,8 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
             for (int i = 0; i < 32; ++i) pr[i] = kv_ok ? pr[i] : 0.f;
           }
           if constexpr (GEN) {  // band edges: P = 0 for the queries of these 32 columns that cannot see this key
+            // (a block mask has no band: vq_lo = 0, vq_hi = 2^30, and nothing
+            // is masked whatever the block, so its position is not looked up)
             const int cb = (tl.qb0 + i) * 64 + ch * 32;
             const int lo_rel = vq_lo - cb, hi_rel = vq_hi - cb;
             if (__any_sync(0xffffffffu, lo_rel > 0 || hi_rel < 31)) {
@@ -592,7 +611,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
     float lse_r = INFINITY;
     bool row_ok = false;
     auto prefetch = [&](const BlockIter<BCAST, GEN> &it) {
-      const int qrow = (it.tl.qb0 + it.i) * 64 + row;
+      const int qrow = query_block<GEN>(p, it.tl, it.i) * 64 + row;
       row_ok = qrow < it.tl.Lq;
       if (row_ok) {
         lse_r = p.lse[it.tl.lse0 + qrow];
@@ -690,7 +709,7 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
       if (lane == 0) mbar_arrive(&bars.aux_full[s]);
       DqJob jnew;  // this block's reduction, run two blocks from now
       {
-        const int qr = (cur.tl.qb0 + cur.i) * 64;
+        const int qr = query_block<GEN>(p, cur.tl, cur.i) * 64;
         jnew = DqJob{cur.tl.h, cur.tl.q_row0 + qr, cur.tl.prow0 + qr};
       }
       cur.next(p);  // advanced in place (one tile's state live, not two)
@@ -1013,7 +1032,7 @@ cudaError_t launch_det_cast(const BwdParams &p, const float *part, const int64_t
 
 cudaError_t launch_bwd(const BwdParams &p, int D, int num_sms, cudaStream_t st) {
   const bool bcast = p.Lq > 0;
-  const bool gen = !bcast && (p.win_left >= 0 || p.win_right >= 0 || p.det);
+  const bool gen = !bcast && (p.win_left >= 0 || p.win_right >= 0 || p.det || p.blk_ptr != nullptr);
   if (D == 128) {
     if (bcast) return launch_t<128, true, false>(p, num_sms, st);
     return gen ? launch_t<128, false, true>(p, num_sms, st) : launch_t<128, false, false>(p, num_sms, st);

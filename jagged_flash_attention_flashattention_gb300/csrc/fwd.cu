@@ -161,12 +161,26 @@ __device__ __forceinline__ FwdTile decode_bhm(const FwdParams &p, int4 bhm) {
 // K/V steps [lo, hi) of the tile (counted from its first loaded K/V tile)
 // that query half x can see. Without a band both halves walk every step;
 // with one, e.g. causal, the first half skips the last tile. A half with
-// rows but no step sees no key (cross attention): its O is 0.
-template <bool GEN>
-__device__ __forceinline__ int2 half_steps(const FwdTile &tl, const FwdParams &p, int x) {
+// rows but no step sees no key (cross attention): its O is 0. With a block
+// mask, lo and hi - 1 are the first and last steps the half sees; the steps
+// between them that it does not see are skipped by their list entries.
+// (t: the tile's index in the list, for the block mask's per-tile steps)
+template <bool GEN, bool SP>
+__device__ __forceinline__ int2 half_steps(const FwdTile &tl, const FwdParams &p, int x, int t) {
   const int rows = x ? tl.nrows1 : tl.nrows0;
   if (rows == 0 || tl.n_kv == 0) return make_int2(0, 0);
   if (!GEN) return make_int2(0, tl.n_kv);
+  if (SP) {
+    // The range must start and end on steps the half sees (so that every role
+    // takes the same first and last step); otherwise the half walks nothing.
+    const int2 m = reinterpret_cast<const int2 *>(p.blk_meta)[2 * t + x];
+    const int lo = min(max(m.x, 0), tl.n_kv), hi = min(max(m.y, 0), tl.n_kv);
+    if (hi <= lo) return make_int2(0, 0);
+    const int lst = p.blk_ptr[t];
+    const bool ok = ((__ldg(p.blk_list + lst + lo) & __ldg(p.blk_list + lst + hi - 1)) >>
+                     (kBlkSeesShift + x)) & 1;
+    return ok ? make_int2(lo, hi) : make_int2(0, 0);
+  }
   const int64_t first = (int64_t)tl.diag0 + x * 128, last = first + rows - 1;
   const int64_t lo = p.win_left < 0 ? 0 : max(first - p.win_left, (int64_t)0);
   const int64_t hi = p.win_right < 0 ? (int64_t)tl.kv_len - 1 : min(last + p.win_right, (int64_t)tl.kv_len - 1);
@@ -174,12 +188,36 @@ __device__ __forceinline__ int2 half_steps(const FwdTile &tl, const FwdParams &p
   return make_int2((int)(lo / 128), (int)min(hi / 128 + 1, (int64_t)tl.n_kv));
 }
 
-template <bool BCAST, bool GEN, bool DYN>
+// SP: block-sparse masks compiled in (with GEN, no band).
+template <bool BCAST, bool GEN, bool DYN, bool SP>
 __device__ __forceinline__ FwdTile decode_tile(const FwdParams &p, int t) {
-  return decode_bhm<BCAST, GEN>(p, tile_bhm<DYN>(p, t));
+  FwdTile d = decode_bhm<BCAST, GEN>(p, tile_bhm<DYN>(p, t));
+  if (SP) {
+    // Block-sparse: the tile's steps are its list entries, at most one per
+    // key block of the sequence (no band: the keys start at the sequence's
+    // first key, kv_len = the sequence's keys); the halves' step ranges are
+    // clamped to the list.
+    const int nkb = (d.kv_len + 127) / 128;
+    d.n_kv = d.nrows0 > 0 ? min(max(p.blk_ptr[t + 1] - p.blk_ptr[t], 0), nkb) : 0;
+  }
+  return d;
 }
 
-template <int D, bool BCAST, bool GEN, bool DYN>
+// List entry of step j (lst: the tile's first entry): the key block (clamped
+// to the sequence) in the low bits, a bit per query half that sees it.
+// Without a block mask step j is key tile j, seen by both halves.
+template <bool SP>
+__device__ __forceinline__ uint32_t step_entry(const FwdParams &p, const FwdTile &tl, int lst, int j) {
+  if (SP) {
+    const uint32_t e = (uint32_t)__ldg(p.blk_list + lst + j);
+    const uint32_t kb = min(e & kBlkIndex, (uint32_t)max((tl.kv_len - 1) >> 7, 0));
+    return kb | (e & ~kBlkIndex);
+  }
+  return (uint32_t)j | (3u << kBlkSeesShift);
+}
+__device__ __forceinline__ bool half_sees(uint32_t e, int x) { return (e >> (kBlkSeesShift + x)) & 1u; }
+
+template <int D, bool BCAST, bool GEN, bool DYN, bool SP>
 __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -279,19 +317,19 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       int4 bhm = DYN ? produce_at(0) : make_int4(-1, 0, 0, 0);
       FwdTile nxt{};
       if (DYN ? bhm.x >= 0 : tbeg < tend)
-        nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN>(p, tbeg);
+        nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN, SP>(p, tbeg);
       for (int t = tbeg; DYN ? bhm.x >= 0 : t < tend; ++t) {
         const FwdTile tl = nxt;
         if (DYN) {
           bhm = produce_at(t + 1);
           if (bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
         } else if (t + 1 < tend) {
-          nxt = decode_tile<BCAST, GEN, DYN>(p, t + 1);
+          nxt = decode_tile<BCAST, GEN, DYN, SP>(p, t + 1);
         }
         if (tl.n_kv == 0) continue;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          const int2 hs = half_steps<GEN>(tl, p, x);
+          const int2 hs = half_steps<GEN, SP>(tl, p, x, t);
           if (hs.y <= hs.x) continue;  // no step: the half's Q is not needed
           if (!mbar_wait(&bars.q_empty[x], ((qph >> x) & 1) ^ 1, ctl, 1)) goto drain;
           qph ^= 1u << x;
@@ -301,18 +339,24 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
             tma_load_3d(smem + C::OFF_Q + x * C::TILE_BYTES + c * 16384, &p.tm_q,
                         &bars.q_full[x], c * 64, tl.h, tl.q_coord + x * 128);
         }
+        // Key tile of each step (its list entry with a block mask).
+        const int lst = SP ? p.blk_ptr[t] : 0;
+        uint32_t kb_cur = 0, kb_prev = 0;
         for (int j = 0; j <= tl.n_kv; ++j) {  // slot of step j: K_j (j < n) and V_{j-1} (j > 0)
-          if (!mbar_wait(&slot_empty[slot], sph ^ 1, ctl, 2)) goto drain;
           const bool k_in = j < tl.n_kv, v_in = j > 0;
+          kb_prev = kb_cur;
+          if (k_in) kb_cur = SP ? step_entry<SP>(p, tl, lst, j) & kBlkIndex : (uint32_t)j;
+          if (!mbar_wait(&slot_empty[slot], sph ^ 1, ctl, 2)) goto drain;
           mbar_arrive_expect_tx(&slot_full[slot], (k_in + v_in) * C::TILE_BYTES);
           armed.arm(2 + slot);
           uint8_t *dst = smem + C::OFF_RING + slot * C::PAIR_BYTES;
           for (int c = 0; c < D / 64; ++c) {
             if (k_in)
-              tma_load_3d(dst + c * 16384, &p.tm_k, &slot_full[slot], c * 64, tl.h, tl.kv0 + j * 128);
+              tma_load_3d(dst + c * 16384, &p.tm_k, &slot_full[slot], c * 64, tl.h,
+                          tl.kv0 + (int)kb_cur * 128);
             if (v_in)
               tma_load_3d(dst + C::TILE_BYTES + c * 16384, &p.tm_v, &slot_full[slot], c * 64, tl.h,
-                          tl.kv0 + (j - 1) * 128);
+                          tl.kv0 + (int)kb_prev * 128);
           }
           if (++slot == C::NSLOT) {
             slot = 0;
@@ -372,18 +416,18 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       int4 bhm = DYN ? tile_at(0, 1u) : make_int4(-1, 0, 0, 0);
       FwdTile nxt{};
       if (DYN ? bhm.x >= 0 : tbeg < tend)
-        nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN>(p, tbeg);
+        nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN, SP>(p, tbeg);
       for (int t = tbeg; DYN ? bhm.x >= 0 : t < tend; ++t) {
         const FwdTile tl = nxt;
         if (DYN) {
           bhm = tile_at(t + 1, 1u);
           if (bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
         } else if (t + 1 < tend) {
-          nxt = decode_tile<BCAST, GEN, DYN>(p, t + 1);
+          nxt = decode_tile<BCAST, GEN, DYN, SP>(p, t + 1);
         }
         if (tl.n_kv == 0) continue;
         // Each half's steps [lo, hi): every step without a band.
-        const int2 hs0 = half_steps<GEN>(tl, p, 0), hs1 = half_steps<GEN>(tl, p, 1);
+        const int2 hs0 = half_steps<GEN, SP>(tl, p, 0, t), hs1 = half_steps<GEN, SP>(tl, p, 1, t);
         const uint32_t has = (hs0.y > hs0.x ? 1u : 0u) | (hs1.y > hs1.x ? 2u : 0u);
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
@@ -404,7 +448,20 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
         }
         mma_commit(&slot_empty[slot]);
         if (++slot == C::NSLOT) { slot = 0; sph ^= 1; }
+        // List entries of steps j - 1, j and j + 1 (a block mask: which halves
+        // see the step; otherwise both), the next one loaded a step ahead.
+        uint32_t e_prev = 0, e_cur = 0, e_next = 0;
+        const int lst = SP ? p.blk_ptr[t] : 0;
+        if constexpr (SP) {
+          e_cur = step_entry<SP>(p, tl, lst, 0);
+          e_next = tl.n_kv > 1 ? step_entry<SP>(p, tl, lst, 1) : 0u;
+        }
         for (int j = 1; j <= tl.n_kv; ++j) {
+          if constexpr (SP) {
+            e_prev = e_cur;
+            e_cur = e_next;
+            e_next = j + 1 < tl.n_kv ? step_entry<SP>(p, tl, lst, j + 1) : 0u;
+          }
           // One slot: V_{j-1}, and K_j unless this is the last step.
           const int ps = slot;
           if (!mbar_wait(&slot_full[ps], sph, ctl, 12)) goto done;
@@ -413,7 +470,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           for (int x = 0; x < 2; ++x) {
             if (!(has >> x & 1)) continue;
             const int2 hs = x ? hs1 : hs0;
-            if (j - 1 >= hs.x && j - 1 < hs.y) {  // O += P_{j-1} V_{j-1}
+            if (j - 1 >= hs.x && j - 1 < hs.y && (!SP || half_sees(e_prev, x))) {  // O += P_{j-1} V_{j-1}
               if (!mbar_wait(&bars.p_ready[x], (pph >> x) & 1, ctl, 14)) goto done;
               pph ^= 1u << x;
               if (j - 1 == hs.x) {  // first PV of the tile overwrites O: epilogue must be done with it
@@ -424,7 +481,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
               issue_pv(x, ps, j - 1 > hs.x);
               if (j == hs.y) mma_commit(&bars.o_full[x]);
             }
-            if (j >= hs.x && j < hs.y) {  // S_j = Q K_j^T
+            if (j >= hs.x && j < hs.y && (!SP || half_sees(e_cur, x))) {  // S_j = Q K_j^T
               if (j == hs.x) tc_fence_after();
               issue_qk(x, ps);
               mma_commit(&bars.s_full[x]);
@@ -450,21 +507,21 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
     int4 bhm = DYN ? tile_at(0, 0xffffffffu) : make_int4(-1, 0, 0, 0);
     FwdTile nxt{};
     if (DYN ? bhm.x >= 0 : tbeg < tend)
-      nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN>(p, tbeg);
+      nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN, SP>(p, tbeg);
     for (int t = tbeg; DYN ? bhm.x >= 0 : t < tend; ++t) {
       const FwdTile tl = nxt;
       if (DYN) {
         bhm = tile_at(t + 1, 0xffffffffu);
         if (bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
       } else if (t + 1 < tend) {
-        nxt = decode_tile<BCAST, GEN, DYN>(p, t + 1);
+        nxt = decode_tile<BCAST, GEN, DYN, SP>(p, t + 1);
       }
       const int nrows = x ? tl.nrows1 : tl.nrows0;
       if (nrows == 0) continue;
       const bool row_ok = r < nrows;
       const int64_t orow = tl.out_row0 + x * 128 + r;
       uint4 *optr = reinterpret_cast<uint4 *>(obase + (orow * p.H + tl.h) * D);
-      const int2 hs = half_steps<GEN>(tl, p, x);
+      const int2 hs = half_steps<GEN, SP>(tl, p, x, t);
       if (hs.y <= hs.x) {  // rows that see no key (no keys, or outside the band): O = 0, LSE = -inf
         if (row_ok) {
           for (int i = 0; i < D / 8; ++i) optr[i] = make_uint4(0, 0, 0, 0);
@@ -482,7 +539,11 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
                              ? tl.kv_len - 1
                              : (int)min((int64_t)dg + p.win_right, (int64_t)tl.kv_len - 1);
       float m_run = -INFINITY, l_run = 0.f;
+      const int lst = SP ? p.blk_ptr[t] : 0;
       for (int j = hs.x; j < hs.y; ++j) {
+        const uint32_t e = SP ? step_entry<SP>(p, tl, lst, j) : 0u;  // key tile of the step, and who sees it
+        if (SP && !half_sees(e, x)) continue;
+        const int kt = SP ? (int)(e & kBlkIndex) : j;
         if (!mbar_wait(&bars.s_full[x], sph, ctl, 20 + x)) goto done;
         sph ^= 1;
         tc_fence_after();
@@ -492,7 +553,7 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
         tmem_wait_ld();
         // Masked columns only where some row of the warp needs them: the
         // peeled tail past the sequence end and the edges of a band.
-        const int lo_rel = vis_lo - j * 128, hi_rel = vis_hi - j * 128;
+        const int lo_rel = vis_lo - kt * 128, hi_rel = vis_hi - kt * 128;
         // (without a band the condition is the same for every row: no vote)
         if (GEN ? __any_sync(0xffffffffu, lo_rel > 0 || hi_rel < 127) : hi_rel < 127) {
 #pragma unroll
@@ -604,9 +665,9 @@ done:
   }
 }
 
-template <int D, bool BCAST, bool GEN, bool DYN>
+template <int D, bool BCAST, bool GEN, bool DYN, bool SP = false>
 cudaError_t launch_t(const FwdParams &p, int num_sms, cudaStream_t st) {
-  auto kern = jfa_fwd_kernel<D, BCAST, GEN, DYN>;
+  auto kern = jfa_fwd_kernel<D, BCAST, GEN, DYN, SP>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
@@ -651,6 +712,11 @@ __global__ void __launch_bounds__(1024) fwd_enum_kernel(const FwdParams p, int64
 cudaError_t launch_fwd(const FwdParams &p, int D, int num_sms, cudaStream_t st) {
   const bool bcast = p.Lq > 0;
   const bool gen = !bcast && (p.win_left >= 0 || p.win_right >= 0);
+  if (p.blk_ptr != nullptr) {  // block-sparse: jagged, no band, static schedule
+    if (bcast || gen || p.dyn) return cudaErrorNotSupported;
+    return D == 128 ? launch_t<128, false, true, false, true>(p, num_sms, st)
+                    : launch_t<64, false, true, false, true>(p, num_sms, st);
+  }
   if (p.dyn) {  // dynamic scheduling: jagged without a band only
     if (bcast || gen) return cudaErrorNotSupported;
     return D == 128 ? launch_t<128, false, false, true>(p, num_sms, st)

@@ -46,7 +46,18 @@ struct FwdParams {
   int *queue;
   const int64_t *tile_base;
   int64_t n_tiles;
+  // Block-sparse masks (masked / cross instantiation, no band): tile i of the
+  // list walks the key blocks blk_list[blk_ptr[i] .. blk_ptr[i + 1]) (block |
+  // half-0 bit << 29 | half-1 bit << 30); blk_meta[i] = first / end step of
+  // each half. Null: no block mask.
+  const int32_t *blk_ptr;
+  const int32_t *blk_list;
+  const int4 *blk_meta;
 };
+
+// Block-sparse list entries: key block in the low bits, one bit per query half.
+constexpr uint32_t kBlkIndex = (1u << 29) - 1;
+constexpr int kBlkSeesShift = 29;
 
 // Byte offset, in the status block, of the uint64 count of accumulator bytes
 // known to be zero (written by the forward kernel, reset by the dQ cast).
@@ -107,6 +118,11 @@ struct BwdParams {
   const float *cos_t;
   const float *sin_t;
   int64_t rope_L;
+  // Block-sparse masks (masked / cross instantiation, no band, no
+  // deterministic dQ): tile i walks the 64-row query blocks
+  // blk_list[blk_ptr[i] .. blk_ptr[i + 1]). Null: no block mask.
+  const int32_t *blk_ptr;
+  const int32_t *blk_list;
 };
 
 cudaError_t launch_bwd(const BwdParams &p, int D, int num_sms, cudaStream_t st);

@@ -17,6 +17,7 @@ stress       4 x 16384 plus 252 uniform in [1, 256], shuffled       4, 128
 bcast        Lq=256 dense Q; B=512 K/V lengths uniform [64, 1024]   4, 128
 blockdiag    B=1152, L=4096 (64 blocks of 64 tokens)               2, 128
 blockdiag64  same, D=64                                            2, 64
+gem_sparse   the gem lengths with block masks (block_masks below)  4, 128
 ===========  ====================================================  =====
 
 Lengths come from ``numpy.random.default_rng(seed)``; values are N(0, 1)
@@ -30,7 +31,8 @@ import numpy as np
 import torch
 
 SEEDS = {"tiny": 1, "gem": 2, "stress": 3, "bcast": 4, "blockdiag": 5, "blockdiag64": 5,
-         "blockdiag_rotary": 5, "gem_rotary": 2}
+         "blockdiag_rotary": 5, "gem_rotary": 2, "gem_sparse": 2}
+MASK_SEEDS = {"gem_sparse": 12}
 
 
 def lengths_for(name, seed=None):
@@ -55,6 +57,27 @@ def offsets_of(lengths, dtype=np.int64):
     off = np.zeros(len(lengths) + 1, dtype=np.int64)
     off[1:] = np.cumsum(np.asarray(lengths, dtype=np.int64))
     return off.astype(dtype)
+
+
+def block_masks(q_lengths, kv_lengths, seed, density=0.5, causal=True):
+    """One boolean mask of 128 x 128 blocks per sequence, shape
+    [ceil(Lq / 128), ceil(Lk / 128)], drawn from numpy.random.default_rng(seed).
+    causal=True: block-causal (block column j <= block row i, counted from the
+    bottom-right corner when Lq != Lk) with the diagonal block kept and every
+    other block below it kept with probability `density` (a local-plus-random
+    pattern: every query sees its own block). causal=False: every block kept
+    with probability `density`."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for lq, lk in zip(q_lengths, kv_lengths):
+        nq, nk = -(-int(lq) // 128), -(-int(lk) // 128)
+        keep = rng.random((nq, nk)) < density
+        if causal:
+            i = np.arange(nq)[:, None] + (nk - nq)
+            j = np.arange(nk)[None, :]
+            keep = (keep & (j < i)) | (j == i)
+        out.append(keep)
+    return out
 
 
 def randn_bf16(shape, seed, device="cpu"):
@@ -117,6 +140,9 @@ WORKLOADS = {
                        rotary=True),
     # the block-diagonal configuration with rotary embeddings fused in
     "blockdiag_rotary": dict(kind="blockdiag", B=1152, L=4096, H=2, D=128, rotary=True),
+    # the GEM batch with block-causal block-sparse masks (block_masks, density 0.5)
+    "gem_sparse": dict(kind="sparse", lengths="gem", H=4, D=128, offsets_dtype=np.int64,
+                       density=0.5),
 }
 
 
@@ -131,8 +157,16 @@ def visible_pairs(Lq, Lk, window=(-1, -1)):
     return int(np.sum(np.maximum(0, hi - lo + 1)))
 
 
+def masked_pairs(Lq, Lk, mask):
+    """Number of (query, key) pairs of one sequence that a 128 x 128 block mask
+    keeps (rows and columns of the last block clipped to the sequence)."""
+    rows = np.minimum(128, Lq - 128 * np.arange(-(-Lq // 128)))
+    cols = np.minimum(128, Lk - 128 * np.arange(-(-Lk // 128)))
+    return int(rows @ np.asarray(mask, dtype=np.int64) @ cols) if rows.size and cols.size else 0
+
+
 def useful_flops(name_or_kind, lengths=None, H=None, D=None, Lq=None, B=None, L=None, block=64,
-                 window=(-1, -1)):
+                 window=(-1, -1), masks=None):
     """Useful (unpadded) forward FLOPs: 4 * H * D * sum_b Lq_b * Lk_b.
 
     The backward counts 2.5x this (five contractions against two).
@@ -141,6 +175,8 @@ def useful_flops(name_or_kind, lengths=None, H=None, D=None, Lq=None, B=None, L=
         return 4.0 * H * D * float(np.sum(np.asarray(lengths, dtype=np.float64) ** 2))
     if name_or_kind == "varlen":  # self-attention lengths with a band mask
         return 4.0 * H * D * float(sum(visible_pairs(int(n), int(n), window) for n in lengths))
+    if name_or_kind == "sparse":  # self-attention lengths with block masks
+        return 4.0 * H * D * float(sum(masked_pairs(int(n), int(n), m) for n, m in zip(lengths, masks)))
     if name_or_kind == "bcast":
         return 4.0 * H * D * Lq * float(np.sum(lengths))
     if name_or_kind == "blockdiag":
