@@ -385,13 +385,16 @@ def _setup(name, rank, dev, seqs=0, zigzag=True):
         st["bwd_bytes"] = 7 * B * L * H * D * 2
         st["desc"] = "blockdiag: B=%d, L=%d, H=%d, D=%d, 64-token blocks" % (B, L, H, D)
         if cfg.get("rotary"):
-            # The forward rotates q and k in the kernel and writes the rotated
-            # rows (a rotary layer's saved output: +2 tiles of writes); the
-            # backward reads those and rotates dQ, dK back in its epilogue.
+            # The forward writes the rotated rows (a rotary layer's saved
+            # output): a rotary pass on q and k and the plain forward on them;
+            # the backward reads those and rotates dQ, dK back in its
+            # epilogue. Modelled bytes are the operation's own (q, k, v read,
+            # o, q_rot, k_rot written: 6 tiles); the two-pass forward moves 8.
             # The fp32 tables (2 x L x D/2 x 4 bytes) stay in L2.
             cos, sin = W.rotary_tables(L, D, device=dev)
             st["fwd_bytes"] = 6 * B * L * H * D * 2
-            st["desc"] += ", rotary fused (fp32 tables [L, D/2]; forward writes q_rot, k_rot)"
+            st["desc"] += (", rotary (fp32 tables [L, D/2]; forward: rotary pass writing q_rot, k_rot, "
+                           "then the plain forward; backward: rotation fused in its epilogue)")
 
             def fwd():
                 st["o"], st["q_rot"], st["k_rot"] = jfa.blockdiag_rotary_fwd(

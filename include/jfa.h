@@ -495,12 +495,15 @@ jfa_status blockdiag_bwd(const void *q, const void *k, const void *v, const void
  * and k is rotated,
  *   x_r[i] = x[i] cos[i] - x[i + D/2] sin[i],
  *   x_r[i + D/2] = x[i + D/2] cos[i] + x[i] sin[i],   i < D/2.
- * Forward: q and k (unrotated) are rotated inside the kernel on their way
- * from memory to the products (rounded to bf16 like a separate rotary pass);
- * o = block-diagonal attention of (q_r, k_r, v). When q_rot and k_rot
- * (device bf16 [B, L, H, D], 16-byte aligned) are given, the rotated rows are
- * also written there, as a rotary layer's output saved for its backward;
- * both NULL writes nothing, one NULL is JFA_ERR_INVALID_ARG.
+ * Forward: o = block-diagonal attention of (q_r, k_r, v), the rotated rows
+ * rounded to bf16 like a separate rotary pass writing bf16. When q_rot and
+ * k_rot (device bf16 [B, L, H, D], 16-byte aligned) are given, the rotated
+ * rows are written there, as a rotary layer's output saved for its backward:
+ * a rotary pass writes them and the plain forward runs on them (faster than
+ * rotating inside the forward's two-stage pipeline). Both NULL writes
+ * nothing and needs no scratch: q and k are rotated in shared memory inside
+ * the forward on their way to the products. The two give the same o bit for
+ * bit. One NULL is JFA_ERR_INVALID_ARG.
  * Backward (the rotary backward fused into the attention epilogue): takes the
  * rotated q_rot, k_rot (as written by the forward), v and dout; dq, dk are
  * the gradients with respect to the unrotated q, k (the gradients of q_rot,

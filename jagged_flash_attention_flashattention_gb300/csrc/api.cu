@@ -541,7 +541,7 @@ extern "C" jfa_status jfa_rope(const void *x, const void *offsets, jfa_index_t i
   JFA_TRY(need_ptr(x, "x"));
   JFA_TRY(need_ptr(x_rot, "x_rot"));
   return cuda_status(launch_rope_rows(x, x_rot, T, H, D, offsets, idx == JFA_I64, B, cos_t, sin_t,
-                                      rope_L, (cudaStream_t)stream),
+                                      rope_L, 0, (cudaStream_t)stream),
                      "rope launch");
 }
 
@@ -656,6 +656,19 @@ jfa_status blockdiag_common(const void *q, const void *k, const void *v, const v
   JFA_TRY(need_ptr(q, "q"));
   JFA_TRY(need_ptr(k, "k"));
   JFA_TRY(need_ptr(v, "v"));
+  if (rotary && !bwd && q_rot != nullptr) {
+    // The caller keeps the rotated rows: write them with the rotary pass
+    // (HBM-bound, positions row mod L) and run the plain forward on them; the
+    // same rotation and the same products as the fused forward (bit-identical),
+    // off the fused kernel's two-stage pipeline. Without q_rot and k_rot the
+    // fused forward rotates in shared memory and needs no scratch.
+    JFA_TRY(cuda_status(launch_rope_rows(q, q_rot, B * L, H, D, nullptr, 0, B, cos_t, sin_t, L, L, st),
+                        "rope launch"));
+    JFA_TRY(cuda_status(launch_rope_rows(k, k_rot, B * L, H, D, nullptr, 0, B, cos_t, sin_t, L, L, st),
+                        "rope launch"));
+    return blockdiag_common(q_rot, k_rot, v, nullptr, B, L, H, D, scale, o, nullptr, nullptr,
+                            nullptr, ws, ws_bytes, false, st);
+  }
   BlockdiagParams p;
   memset(&p, 0, sizeof(p));
   const int64_t rows = B * L;
@@ -679,8 +692,6 @@ jfa_status blockdiag_common(const void *q, const void *k, const void *v, const v
   p.L = L;
   p.cos_t = rotary ? cos_t : nullptr;
   p.sin_t = rotary ? sin_t : nullptr;
-  p.q_rot = rotary ? q_rot : nullptr;
-  p.k_rot = rotary ? k_rot : nullptr;
   p.H = H;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;

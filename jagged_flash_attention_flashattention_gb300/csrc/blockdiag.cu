@@ -61,8 +61,8 @@ __device__ __forceinline__ Unit unit_of(int u, int H, int64_t rows) {
 //   x_r[i] = x[i] cos[i] - x[i + D/2] sin[i],  x_r[i + D/2] = x[i + D/2] cos[i] + x[i] sin[i].
 // The forward rotates the q and k tiles in shared memory as soon as they land
 // and before any product reads them (rounded to bf16, as a separate rotary
-// pass writing bf16 would), and can write the rotated rows out for the
-// backward. The backward reads the rotated q and k and applies the rotary
+// pass writing bf16 would). (A caller that keeps the rotated rows gets them
+// from the rotary pass instead, followed by the plain forward.) The backward reads the rotated q and k and applies the rotary
 // backward in its epilogue: dQ and dK rotated back by the transposed rotation.
 // An item is one row's 8-pair chunk j: columns 8j..8j+7 and their partners
 // 8j + D/2.. . Items it = base + u * nthr (u < U) of a 128-row tile; tab holds
@@ -88,13 +88,10 @@ __device__ __forceinline__ void rot_load(const BlockdiagParams &p, int64_t row0,
   }
 }
 
-// Rotates the items in shared memory and, when qo is not null, also writes
-// them to q_rot and k_rot (qo, ko: row 0 of the tile at this head; rows are
-// rstride elements apart).
+// Rotates the items of the q and k tiles in shared memory.
 template <int D, int U>
 __device__ __forceinline__ void rot_apply(uint8_t *qt, uint8_t *kt, int nrows, int base, int nthr,
-                                          const float4 (&tab)[U][4], __nv_bfloat16 *qo,
-                                          __nv_bfloat16 *ko, int64_t rstride) {
+                                          const float4 (&tab)[U][4]) {
   constexpr int NC = D / 16;
 #pragma unroll
   for (int u = 0; u < U; ++u) {
@@ -126,11 +123,6 @@ __device__ __forceinline__ void rot_apply(uint8_t *qt, uint8_t *kt, int nrows, i
       const uint4 o4 = make_uint4(ow[0], ow[1], ow[2], ow[3]), h4 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       *lo = o4;
       *hi = h4;
-      if (qo != nullptr) {
-        __nv_bfloat16 *g = (t ? ko : qo) + r * rstride + 8 * j;
-        *reinterpret_cast<uint4 *>(g) = o4;
-        *reinterpret_cast<uint4 *>(g + D / 2) = h4;
-      }
     }
   }
 }
@@ -271,7 +263,6 @@ __global__ void __launch_bounds__(ROPE ? 384 : 256, 1) blockdiag_fwd_kernel(cons
     constexpr int U = 128 * (D / 16) / 192 + 1;
     static_assert(192 * U >= 128 * (D / 16), "one batch per unit");
     const int rt = (warp < 8 ? warp - 2 : warp - 6) * 32 + lane;  // 0 .. 191
-    const int64_t rstride = (int64_t)p.H * D;
     uint32_t fph = 0;
     int n = 0;
     float4 tab[U][4];
@@ -282,10 +273,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 256, 1) blockdiag_fwd_kernel(cons
       fph ^= 1u << (s);
       rot_load<D, U>(p, x.row0, x.nrows, rt, 192, tab);
       uint8_t *st = smem + C::OFF_STAGE + s * 3 * C::TILE;
-      const int64_t g0 = (int64_t)x.row0 * rstride + (int64_t)x.h * D;
-      __nv_bfloat16 *qo = p.q_rot ? static_cast<__nv_bfloat16 *>(p.q_rot) + g0 : nullptr;
-      __nv_bfloat16 *ko = p.k_rot ? static_cast<__nv_bfloat16 *>(p.k_rot) + g0 : nullptr;
-      rot_apply<D, U>(st, st + C::TILE, x.nrows, rt, 192, tab, qo, ko, rstride);
+      rot_apply<D, U>(st, st + C::TILE, x.nrows, rt, 192, tab);
       fence_async_smem();  // the products read these tiles through the async proxy
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.rot[s]);

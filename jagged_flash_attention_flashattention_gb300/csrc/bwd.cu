@@ -860,13 +860,18 @@ template <int D>
 __global__ void __launch_bounds__(256) rope_rows_kernel(
     const __nv_bfloat16 *__restrict__ x, __nv_bfloat16 *__restrict__ y, int64_t rows, int H,
     const void *offsets, int idx64, int64_t B, int64_t T, const float *cos_t, const float *sin_t,
-    int64_t rope_L) {
+    int64_t rope_L, int64_t dense_L) {
   __shared__ int pos_s[kRopeChunk];
   constexpr int NQ = D / 16;  // 8-pair groups per (row, head)
   const int per_row = H * NQ;
   for (int64_t r0 = (int64_t)blockIdx.x * kRopeChunk; r0 < rows; r0 += (int64_t)gridDim.x * kRopeChunk) {
     const int n = (int)min((int64_t)kRopeChunk, rows - r0);
-    chunk_positions(offsets, idx64, B, T, r0, n, pos_s);
+    if (dense_L > 0) {  // dense sequences of dense_L rows: position = row mod dense_L
+      if (threadIdx.x < n) pos_s[threadIdx.x] = (int)((r0 + threadIdx.x) % dense_L);
+      __syncthreads();
+    } else {
+      chunk_positions(offsets, idx64, B, T, r0, n, pos_s);
+    }
     for (int it = threadIdx.x; it < n * per_row; it += blockDim.x) {
       const int rr = it / per_row, g = it % NQ;
       const int64_t rh = (r0 + rr) * H + (it % per_row) / NQ;
@@ -1073,16 +1078,16 @@ cudaError_t launch_dq_convert_rope(const BwdParams &p, const float *acc, void *d
 
 cudaError_t launch_rope_rows(const void *x, void *y, int64_t rows, int H, int D, const void *offsets,
                              int idx64, int64_t B, const float *cos_t, const float *sin_t,
-                             int64_t rope_L, cudaStream_t st) {
+                             int64_t rope_L, int64_t dense_L, cudaStream_t st) {
   const int64_t n = (rows + kRopeChunk - 1) / kRopeChunk * 256;  // one 256-thread block per chunk
   const auto *xi = static_cast<const __nv_bfloat16 *>(x);
   auto *yo = static_cast<__nv_bfloat16 *>(y);
   if (D == 128)
     rope_rows_kernel<128><<<grid_for(n), 256, 0, st>>>(xi, yo, rows, H, offsets, idx64, B, rows,
-                                                       cos_t, sin_t, rope_L);
+                                                       cos_t, sin_t, rope_L, dense_L);
   else
     rope_rows_kernel<64><<<grid_for(n), 256, 0, st>>>(xi, yo, rows, H, offsets, idx64, B, rows,
-                                                      cos_t, sin_t, rope_L);
+                                                      cos_t, sin_t, rope_L, dense_L);
   return cudaGetLastError();
 }
 

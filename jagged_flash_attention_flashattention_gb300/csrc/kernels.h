@@ -127,10 +127,11 @@ struct BwdParams {
 
 cudaError_t launch_bwd(const BwdParams &p, int D, int num_sms, cudaStream_t st);
 // x_rot = x [rows, H, D] bf16 rotated at each row's position in its sequence
-// (offsets [B+1]; positions clamped to [0, rope_L)).
+// (offsets [B+1], or, dense_L > 0, sequences of dense_L rows each and no
+// offsets; positions clamped to [0, rope_L)).
 cudaError_t launch_rope_rows(const void *x, void *y, int64_t rows, int H, int D, const void *offsets,
                              int idx64, int64_t B, const float *cos_t, const float *sin_t,
-                             int64_t rope_L, cudaStream_t st);
+                             int64_t rope_L, int64_t dense_L, cudaStream_t st);
 // The cast of launch_dq_convert with each row rotated back (p.cos_t, p.sin_t),
 // and the same rows of dK (p.dk, bf16) rotated back in place.
 cudaError_t launch_dq_convert_rope(const BwdParams &p, const float *acc, void *dq, int64_t rows,
@@ -168,13 +169,10 @@ struct BlockdiagParams {
   int64_t rows;  // B * L
   int64_t L;     // tokens per sequence (a row's position is row % L)
   // Rotary variant: fp32 tables [L, D/2]. The forward rotates q and k rows by
-  // them before the products (and writes the rotated rows to q_rot, k_rot
-  // when those are not null); the backward reads rotated q and k and rotates
+  // them before the products; the backward reads rotated q and k and rotates
   // dQ, dK back.
   const float *cos_t;
   const float *sin_t;
-  void *q_rot;
-  void *k_rot;
   int H;
   float scale;
   float scale_log2;

@@ -129,6 +129,8 @@ def test_blockdiag_rotary_config_sampled():
     cos, sin = W.rotary_tables(L, D, device="cuda")
     o, q_rot, k_rot = jfa.blockdiag_rotary_fwd(inp["q"], inp["k"], inp["v"], cos, sin,
                                                return_rotated=True)
+    # without the rotated rows the fused forward runs: the same O bit for bit
+    assert torch.equal(o, jfa.blockdiag_rotary_fwd(inp["q"], inp["k"], inp["v"], cos, sin))
     g = jfa.blockdiag_rotary_bwd(inp["q"], inp["k"], inp["v"], inp["do"], cos, sin)
     jfa.check_status()
     s = 1 / math.sqrt(D)
