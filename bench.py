@@ -142,7 +142,7 @@ def _gem_lengths(seed_offset=0):
 
 
 def cpu_baseline(budget_s=12.0, lengths=None, H=4, D=128):
-    """Times the fp64 oracle (fwd + bwd) on a prefix of the GEM batch."""
+    """Times the fp64 oracle (fwd + bwd, and each separately) on a prefix of the GEM batch."""
     import torch
 
     from jagged_flash_attention_flashattention_gb300 import workloads as W
@@ -155,12 +155,17 @@ def cpu_baseline(budget_s=12.0, lengths=None, H=4, D=128):
     s = 1 / np.sqrt(D)
     t0 = time.perf_counter()
     flops = 0.0
+    t_fwd = t_bwd = 0.0
     n = 0
     while n < len(L) and time.perf_counter() - t0 < budget_s:
         a, e = int(offs[n]), int(offs[n + 1])
         for h in range(H):
+            t1 = time.perf_counter()
             A.seq_fwd(q[a:e, h], k[a:e, h], v[a:e, h], s)
+            t2 = time.perf_counter()
             A.seq_bwd(q[a:e, h], k[a:e, h], v[a:e, h], do[a:e, h], s)
+            t_fwd += t2 - t1
+            t_bwd += time.perf_counter() - t2
         flops += 3.5 * 4.0 * H * D * float(e - a) ** 2
         n += 1
     dt = time.perf_counter() - t0
@@ -171,9 +176,55 @@ def cpu_baseline(budget_s=12.0, lengths=None, H=4, D=128):
         threads = max((i.get("num_threads", 0) for i in info), default=threads)
     except Exception:
         pass
+    fwd_flops = flops / 3.5
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": int(threads), "kind": "oracle",
+            "fwd_tflops": fwd_flops / max(t_fwd, 1e-9) / 1e12,
+            "bwd_tflops": 2.5 * fwd_flops / max(t_bwd, 1e-9) / 1e12,
             "sample": "fp64 NumPy oracle fwd+bwd on the first %d GEM sequences x %d heads "
-                      "(%.1f s wall, %d host cores visible)" % (n, H, dt, os.cpu_count())}
+                      "(%.1f s wall: fwd %.1f s, bwd %.1f s; %d host cores visible)"
+                      % (n, H, dt, t_fwd, t_bwd, os.cpu_count())}
+
+
+def scheduler_times(dev, reps=10):
+    """Host time of planning the GEM batch: the C scheduler alone (forward and
+    backward tile lists), and a whole Plan (both lists, pinned staging and the
+    asynchronous upload, synchronised), for self-attention and for the
+    block-sparse masks of the gem_sparse workload. Medians over `reps`."""
+    import torch
+
+    import jagged_flash_attention_flashattention_gb300 as jfa
+    from jagged_flash_attention_flashattention_gb300 import workloads as W
+
+    L = _gem_lengths()
+    H, D = 4, 128
+    off_host = W.offsets_of(L)
+    off = torch.from_numpy(off_host).to(dev)
+    masks = jfa.pack_block_masks(W.block_masks(L, L, W.MASK_SEEDS["gem_sparse"], density=0.5),
+                                 off_host, off_host)
+    n_sms = jfa.num_sms()
+    ws = jfa.Plan(off, H, D, host_offsets=off_host).workspace
+
+    def med(fn):
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            ts.append((time.perf_counter() - t0) * 1e3)
+        return round(statistics.median(ts), 3)
+
+    def plan(**kw):
+        jfa.Plan(off, H, D, host_offsets=off_host, workspace=ws, **kw)
+        torch.cuda.synchronize()
+
+    return {
+        "workload": _gem_desc(L, H, D),
+        "sched_ms": med(lambda: (jfa.schedule(off_host, H, jfa.tile_rows(jfa.OP_FWD, D), n_sms),
+                                 jfa.schedule(off_host, H, jfa.tile_rows(jfa.OP_BWD, D), n_sms))),
+        "plan_with_upload_ms": med(plan),
+        "sparse_sched_ms": med(lambda: (jfa.schedule_sparse(off_host, off_host, H, jfa.OP_FWD, n_sms, masks),
+                                        jfa.schedule_sparse(off_host, off_host, H, jfa.OP_BWD, n_sms, masks))),
+        "sparse_plan_with_upload_ms": med(lambda: plan(kind="sparse", block_masks=masks)),
+    }
 
 
 METRIC = "useful TFLOP/s fwd+bwd (jagged attention, bf16) and % of GB300 bf16 tensor peak"
@@ -707,6 +758,8 @@ def run_ours(args):
             line["configs"] = configs
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
+        if full_gem and not args.no_configs:
+            line["scheduler"] = scheduler_times(dev)
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
