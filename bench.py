@@ -353,24 +353,36 @@ def _setup(name, rank, dev, seqs=0, zigzag=True):
         L = _gem_lengths(rank) if cfg["lengths"] == "gem" else W.lengths_for(cfg["lengths"])
         if seqs:
             L = L[:seqs]
-        off_host = W.offsets_of(L, cfg["offsets_dtype"])
         win, det = cfg["window"], cfg["deterministic"]
+        off_host = W.offsets_of(L, cfg["offsets_dtype"])
         inp = W.jagged_inputs(L, H, D, W.SEEDS[cfg["lengths"]] + 1000 * rank, device=dev)
         off = torch.from_numpy(off_host).to(dev)
-        ws_buf = jfa.Plan(off, H, D, kind="varlen", host_offsets=off_host, window=win,
-                          deterministic=det).workspace
-        st["fwd_flops"] = W.useful_flops("varlen", L, H=H, D=D, window=win)
-        st["desc"] = "%s: B=%d, T=%d, H=%d, D=%d, window %s, %s dQ" % (
-            name, len(L), int(off_host[-1]), H, D, tuple(win), "ordered" if det else "atomic")
+        if cfg.get("kv_seed"):  # cross attention: key/value lengths of their own
+            Lk = W.lengths_for(cfg["lengths"], seed=cfg["kv_seed"] + 1000 * rank)[:len(L)]
+            koff_host = W.offsets_of(Lk, cfg["offsets_dtype"])
+            kv = W.jagged_inputs(Lk, H, D, W.SEEDS[cfg["lengths"]] + 500 + 1000 * rank, device=dev)
+            inp["k"], inp["v"] = kv["k"], kv["v"]
+            koff = torch.from_numpy(koff_host).to(dev)
+            st["fwd_flops"] = W.useful_flops("cross", (L, Lk), H=H, D=D)
+            st["desc"] = "%s: B=%d, Tq=%d, Tk=%d, H=%d, D=%d, separate q/kv offsets, no mask" % (
+                name, len(L), int(off_host[-1]), int(koff_host[-1]), H, D)
+        else:
+            koff_host, koff = off_host, off
+            st["fwd_flops"] = W.useful_flops("varlen", L, H=H, D=D, window=win)
+            st["desc"] = "%s: B=%d, T=%d, H=%d, D=%d, window %s, %s dQ" % (
+                name, len(L), int(off_host[-1]), H, D, tuple(win), "ordered" if det else "atomic")
+        ws_buf = jfa.Plan(koff, H, D, kind="varlen", q_offsets=off, host_offsets=koff_host,
+                          host_q_offsets=off_host, window=win, deterministic=det).workspace
 
         def fwd():
-            st["plan"] = jfa.Plan(off, H, D, kind="varlen", host_offsets=off_host, window=win,
-                                  deterministic=det, workspace=ws_buf, zigzag=zigzag)
-            st["o"], st["lse"] = jfa.jfa_varlen_fwd(inp["q"], inp["k"], inp["v"], off, off,
+            st["plan"] = jfa.Plan(koff, H, D, kind="varlen", q_offsets=off, host_offsets=koff_host,
+                                  host_q_offsets=off_host, window=win, deterministic=det,
+                                  workspace=ws_buf, zigzag=zigzag)
+            st["o"], st["lse"] = jfa.jfa_varlen_fwd(inp["q"], inp["k"], inp["v"], off, koff,
                                                     window=win, plan=st["plan"])
 
         def bwd():
-            jfa.jfa_varlen_bwd(inp["q"], inp["k"], inp["v"], st["o"], st["lse"], inp["do"], off, off,
+            jfa.jfa_varlen_bwd(inp["q"], inp["k"], inp["v"], st["o"], st["lse"], inp["do"], off, koff,
                                window=win, deterministic=det, plan=st["plan"])
 
         st["check"] = lambda: st["plan"].check()
@@ -620,7 +632,7 @@ def _other_configs(args, dev, peaks):
     steps, warmup = max(3, min(args.steps, 10)), 3
     out = {}
     for name in ("stress", "bcast", "blockdiag", "blockdiag64", "blockdiag_rotary", "gem_causal",
-                 "gem_det", "gem_rotary", "gem_sparse"):
+                 "gem_det", "gem_cross", "gem_rotary", "gem_sparse"):
         st = _setup(name, 0, dev)
         _, f_ms, b_ms, _ = _time_steps(st, steps, warmup, stream)
         ff, bf = st["fwd_flops"], st["bwd_flops"]
@@ -952,7 +964,7 @@ def main():
     ap.add_argument("--config", default="gem",
                     choices=["gem", "stress", "bcast", "blockdiag", "blockdiag64", "tiny",
                              "gem_causal", "gem_det", "blockdiag_rotary", "gem_rotary",
-                             "gem_sparse"])
+                             "gem_sparse", "gem_cross"])
     ap.add_argument("--schedule", default="zigzag", choices=["zigzag", "naive"],
                     help="tile order: host LPT + zigzag deal, or the unsorted round-robin deal")
     ap.add_argument("--no-configs", action="store_true",

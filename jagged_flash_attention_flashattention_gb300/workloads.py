@@ -18,6 +18,8 @@ bcast        Lq=256 dense Q; B=512 K/V lengths uniform [64, 1024]   4, 128
 blockdiag    B=1152, L=4096 (64 blocks of 64 tokens)               2, 128
 blockdiag64  same, D=64                                            2, 64
 gem_sparse   the gem lengths with block masks (block_masks below)  4, 128
+gem_cross    query lengths of gem; key/value lengths drawn the      4, 128
+             same way with seed 6 (jagged cross attention)
 ===========  ====================================================  =====
 
 Lengths come from ``numpy.random.default_rng(seed)``; values are N(0, 1)
@@ -31,7 +33,8 @@ import numpy as np
 import torch
 
 SEEDS = {"tiny": 1, "gem": 2, "stress": 3, "bcast": 4, "blockdiag": 5, "blockdiag64": 5,
-         "blockdiag_rotary": 5, "gem_rotary": 2, "gem_sparse": 2}
+         "blockdiag_rotary": 5, "gem_rotary": 2, "gem_sparse": 2, "gem_cross": 2}
+KV_SEEDS = {"gem_cross": 6}  # key/value lengths of the cross-attention workload
 MASK_SEEDS = {"gem_sparse": 12}
 
 
@@ -140,6 +143,10 @@ WORKLOADS = {
                        rotary=True),
     # the block-diagonal configuration with rotary embeddings fused in
     "blockdiag_rotary": dict(kind="blockdiag", B=1152, L=4096, H=2, D=128, rotary=True),
+    # jagged cross attention: GEM query lengths against independently drawn
+    # GEM-distributed key/value lengths (separate offsets), no mask
+    "gem_cross": dict(kind="varlen", lengths="gem", kv_seed=6, H=4, D=128, offsets_dtype=np.int64,
+                      window=(-1, -1), deterministic=False),
     # the GEM batch with block-causal block-sparse masks (block_masks, density 0.5)
     "gem_sparse": dict(kind="sparse", lengths="gem", H=4, D=128, offsets_dtype=np.int64,
                        density=0.5),
@@ -175,6 +182,8 @@ def useful_flops(name_or_kind, lengths=None, H=None, D=None, Lq=None, B=None, L=
         return 4.0 * H * D * float(np.sum(np.asarray(lengths, dtype=np.float64) ** 2))
     if name_or_kind == "varlen":  # self-attention lengths with a band mask
         return 4.0 * H * D * float(sum(visible_pairs(int(n), int(n), window) for n in lengths))
+    if name_or_kind == "cross":  # separate query and key/value lengths, no mask
+        return 4.0 * H * D * float(np.dot(np.asarray(lengths[0], np.float64), np.asarray(lengths[1], np.float64)))
     if name_or_kind == "sparse":  # self-attention lengths with block masks
         return 4.0 * H * D * float(sum(masked_pairs(int(n), int(n), m) for n, m in zip(lengths, masks)))
     if name_or_kind == "bcast":

@@ -130,6 +130,35 @@ def test_gem_causal_sampled():
                 assert_close(got[a:e, h], r, "%s[b=%d,h=%d]" % (name, b, h))
 
 
+def test_gem_cross_sampled():
+    # The GEM cross-attention batch at full size: GEM query lengths against
+    # key/value lengths drawn the same way with their own seed (separate
+    # offsets, no mask), in the bench's launch configuration; sampled
+    # sequences (every head) against the oracle.
+    Lq = W.lengths_for("gem")
+    Lk = W.lengths_for("gem", seed=W.KV_SEEDS["gem_cross"])
+    H, D = 4, 128
+    inp = _cross_inputs(Lq, Lk, H, D, W.SEEDS["gem_cross"])
+    o, lse, g = _run(inp, Lq, Lk, H, D, (-1, -1))
+    qo, ko = W.offsets_of(Lq), W.offsets_of(Lk)
+    rng = np.random.default_rng(97)
+    pick = sorted(set(rng.choice(len(Lq), 6, replace=False).tolist()) |
+                  {int(np.argmax(Lq)), int(np.argmax(Lk))})
+    s = 1 / math.sqrt(D)
+    for b in pick:
+        qa, qe, ka, ke = int(qo[b]), int(qo[b + 1]), int(ko[b]), int(ko[b + 1])
+        for h in range(H):
+            Q, dO = f64(inp["q"][qa:qe, h]), f64(inp["do"][qa:qe, h])
+            K, V = f64(inp["k"][ka:ke, h]), f64(inp["v"][ka:ke, h])
+            ro, rl = A.seq_fwd(Q, K, V, s)
+            assert_close(o[qa:qe, h], ro, "O[b=%d,h=%d]" % (b, h))
+            assert_lse(lse[h, qa:qe], rl, "LSE[b=%d,h=%d]" % (b, h))
+            rq, rk, rv = A.seq_bwd(Q, K, V, dO, s)
+            assert_close(g[0][qa:qe, h], rq, "dQ[b=%d,h=%d]" % (b, h))
+            assert_close(g[1][ka:ke, h], rk, "dK[b=%d,h=%d]" % (b, h))
+            assert_close(g[2][ka:ke, h], rv, "dV[b=%d,h=%d]" % (b, h))
+
+
 def test_long_sequence_sliding_window_sampled():
     # The stress batch (four 16384-token sequences) with a causal window of
     # 1024 keys; rows of one long sequence checked on every head.
