@@ -274,14 +274,10 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
         const BwdTile tl = nxt;
         if (t + 1 < tend) nxt = decode_tile<BCAST, GEN>(p, t + 1);
         if (tl.nq == 0 || tl.nkv <= 0) continue;
-        if (!mbar_wait(&bars.kv_empty, kvph ^ 1, ctl, 1)) goto drain;
-        kvph ^= 1;
-        mbar_arrive_expect_tx(&bars.kv_full, 2 * C::KV_TILE);
-        armed.arm(0);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(smem + C::OFF_K + c * 16384, &p.tm_k, &bars.kv_full, c * 64, tl.h, tl.kv_row0);
-          tma_load_3d(smem + C::OFF_V + c * 16384, &p.tm_v, &bars.kv_full, c * 64, tl.h, tl.kv_row0);
-        }
+        // The tile's query blocks stream through the stages; block 0's stage
+        // does not depend on the K/V buffer, so it is loaded before waiting
+        // for the previous tile to release K and V (its slot frees about two
+        // blocks before that tile ends) and arrives with them, not after.
         for (int i = 0; i < tl.nq; ++i, ++qb) {
           const int s = qb % C::NSTAGE;
           const int qr = query_block<GEN>(p, tl, i) * 64;  // first query row of the block in the sequence
@@ -295,6 +291,16 @@ __global__ void __launch_bounds__(512, 1) jfa_bwd_kernel(const __grid_constant__
                         tl.q_row0 + qr);
             tma_load_3d(st + C::QT + c * C::QCHUNK, &p.tm_do, &bars.stage_full[s], c * 64, tl.h,
                         tl.o_row0 + qr);
+          }
+          if (i == 0) {  // then K and V, once the previous tile is done with them
+            if (!mbar_wait(&bars.kv_empty, kvph ^ 1, ctl, 1)) goto drain;
+            kvph ^= 1;
+            mbar_arrive_expect_tx(&bars.kv_full, 2 * C::KV_TILE);
+            armed.arm(0);
+            for (int c = 0; c < D / 64; ++c) {
+              tma_load_3d(smem + C::OFF_K + c * 16384, &p.tm_k, &bars.kv_full, c * 64, tl.h, tl.kv_row0);
+              tma_load_3d(smem + C::OFF_V + c * 16384, &p.tm_v, &bars.kv_full, c * 64, tl.h, tl.kv_row0);
+            }
           }
         }
       }

@@ -13,7 +13,7 @@ scheduler interleaves the roles many times over random tile lists and checks:
   read of its previous contents, through the barriers.
 
 Negative controls show that each check has teeth: one dQ^T TMEM buffer
-with the reduction two blocks behind deadlocks at a tile switch; a producer
+with the reduction three blocks behind deadlocks at a tile switch; a producer
 that refills stages without waiting for their release is flagged as parity
 aliasing; an MMA thread that rewrites a dQ^T buffer without waiting for its
 drain is flagged as early reuse. The scheduler is adversarial (roles are
@@ -40,15 +40,16 @@ class Roles:
     def producer(self):
         n = 0
         for t, nq in enumerate(self.tiles):
-            if t > 0:
-                yield "wait", ("kv_empty", 0), t - 1
-            yield "sig", ("kv_full", 0), t
-            for _ in range(nq):
+            for i in range(nq):
                 s, ph = self.stage(n)
                 if n >= NSTAGE:
                     yield "wait", ("stage_empty", s), ph - 1
                 yield "sig", ("stage_full", s), ph
                 n += 1
+                if i == 0:  # K and V after the tile's first stage
+                    if t > 0:
+                        yield "wait", ("kv_empty", 0), t - 1
+                    yield "sig", ("kv_full", 0), t
 
     def mma(self):
         n = 0
@@ -230,14 +231,22 @@ def test_committed_protocol_fixed_cases(tiles):
         assert simulate(tiles, rng) is None
 
 
-def test_negative_control_single_dq_buffer_two_blocks_behind_deadlocks():
+def test_negative_control_single_dq_buffer_three_blocks_behind_deadlocks():
     # The MMA thread's dQ^T of a tile's last block then waits for a drain that
-    # the dQ warps only reach after staging the next tile's first block, whose
+    # the dQ warps only reach after staging the next tile's second block, whose
     # Q/dO load the producer issues only after the next tile's K/V load, which
     # waits for this tile's products to finish.
     rng = random.Random(13)
-    results = [simulate(_random_tiles(rng), rng, dq_bufs=1, lag=2) for _ in range(300)]
+    results = [simulate(_random_tiles(rng), rng, dq_bufs=1, lag=3) for _ in range(300)]
     assert any(r is not None and r[0] == "deadlock" for r in results)
+
+
+def test_single_dq_buffer_two_blocks_behind_is_safe():
+    # With the next tile's first stage loaded ahead of its K and V, the drain
+    # that a tile's last dQ^T waits for no longer depends on that tile ending.
+    rng = random.Random(16)
+    for _ in range(1000):
+        assert simulate(_random_tiles(rng), rng, dq_bufs=1, lag=2) is None
 
 
 def test_single_dq_buffer_one_block_behind_is_safe():
