@@ -109,28 +109,53 @@ __device__ __forceinline__ int4 tile_bhm(const FwdParams &p, int t) {
   return make_int4(p.tiles[3 * t], p.tiles[3 * t + 1], p.tiles[3 * t + 2], 1);
 }
 
+// The loads of a tile's decode: its list entry, its sequence's offsets as
+// stored (clamped later) and, with a block mask, its list bounds. Split from
+// the arithmetic so that a role can issue them a tile ahead and use them a
+// tile later without waiting.
+struct FwdRaw {
+  int4 bhm;
+  int64_t s0, e0, qs, qe;
+  int ls, le;
+};
+
+template <bool BCAST, bool SP>
+__device__ __forceinline__ FwdRaw fetch_raw(const FwdParams &p, int4 bhm, int t) {
+  FwdRaw r;
+  r.bhm = bhm;
+  const bool in = bhm.x >= 0 && bhm.x < p.B && bhm.y >= 0 && bhm.y < p.H && bhm.z >= 0 && bhm.z < (1 << 22);
+  r.s0 = in ? load_off(p.offsets, p.idx64, bhm.x) : 0;
+  r.e0 = in ? load_off(p.offsets, p.idx64, bhm.x + 1) : 0;
+  r.qs = (!BCAST && in) ? load_off(p.q_offsets, p.idx64, bhm.x) : 0;
+  r.qe = (!BCAST && in) ? load_off(p.q_offsets, p.idx64, bhm.x + 1) : 0;
+  r.ls = SP ? p.blk_ptr[t] : 0;
+  r.le = SP ? p.blk_ptr[t + 1] : 0;
+  return r;
+}
+
 // GEN: the band mask is compiled in (jfa_varlen_fwd with a window); without
-// it every row sees all of its sequence's keys.
-template <bool BCAST, bool GEN>
-__device__ __forceinline__ FwdTile decode_bhm(const FwdParams &p, int4 bhm) {
+// it every row sees all of its sequence's keys. SP: block-sparse masks (with
+// GEN, no band).
+template <bool BCAST, bool GEN, bool SP>
+__device__ __forceinline__ FwdTile finish_tile(const FwdParams &p, const FwdRaw &r) {
   FwdTile d;
-  d.b = bhm.x;
-  d.h = bhm.y;
-  const int m = bhm.z;
+  d.b = r.bhm.x;
+  d.h = r.bhm.y;
+  const int m = r.bhm.z;
   // A tile outside this batch (a schedule built for another one) is empty,
   // and sequence bounds are clamped to [0, T]: no row past the tensors is
   // read or written whatever the tile list or the offsets hold.
   const bool in = d.b >= 0 && d.b < p.B && d.h >= 0 && d.h < p.H && m >= 0 && m < (1 << 22);
-  const int64_t s0 = in ? min(max(load_off(p.offsets, p.idx64, d.b), (int64_t)0), p.T) : 0;
-  const int64_t e0 = in ? min(max(load_off(p.offsets, p.idx64, d.b + 1), s0), p.T) : 0;
+  const int64_t s0 = in ? min(max(r.s0, (int64_t)0), p.T) : 0;
+  const int64_t e0 = in ? min(max(r.e0, s0), p.T) : 0;
   const int L = (int)(e0 - s0);
   int64_t qs = 0;
   int Lq;
   if (BCAST) {
     Lq = in ? p.Lq : 0;
   } else {
-    qs = in ? min(max(load_off(p.q_offsets, p.idx64, d.b), (int64_t)0), p.Tq) : 0;
-    Lq = (int)(in ? min(max(load_off(p.q_offsets, p.idx64, d.b + 1), qs), p.Tq) - qs : 0);
+    qs = in ? min(max(r.qs, (int64_t)0), p.Tq) : 0;
+    Lq = (int)(in ? min(max(r.qe, qs), p.Tq) - qs : 0);
   }
   const int row0 = m * 256;
   d.nrows0 = max(0, min(128, Lq - row0));
@@ -155,7 +180,19 @@ __device__ __forceinline__ FwdTile decode_bhm(const FwdParams &p, int4 bhm) {
     d.out_row0 = qs + row0;
     d.lse0 = (int64_t)d.h * p.Tq + qs + row0;
   }
+  if (SP) {
+    // Block-sparse: the tile's steps are its list entries, at most one per
+    // key block of the sequence (no band: the keys start at the sequence's
+    // first key, kv_len = the sequence's keys).
+    const int nkb = (d.kv_len + 127) / 128;
+    d.n_kv = d.nrows0 > 0 ? min(max(r.le - r.ls, 0), nkb) : 0;
+  }
   return d;
+}
+
+template <bool BCAST, bool GEN>
+__device__ __forceinline__ FwdTile decode_bhm(const FwdParams &p, int4 bhm) {
+  return finish_tile<BCAST, GEN, false>(p, fetch_raw<BCAST, false>(p, bhm, 0));
 }
 
 // K/V steps [lo, hi) of the tile (counted from its first loaded K/V tile)
@@ -191,16 +228,7 @@ __device__ __forceinline__ int2 half_steps(const FwdTile &tl, const FwdParams &p
 // SP: block-sparse masks compiled in (with GEN, no band).
 template <bool BCAST, bool GEN, bool DYN, bool SP>
 __device__ __forceinline__ FwdTile decode_tile(const FwdParams &p, int t) {
-  FwdTile d = decode_bhm<BCAST, GEN>(p, tile_bhm<DYN>(p, t));
-  if (SP) {
-    // Block-sparse: the tile's steps are its list entries, at most one per
-    // key block of the sequence (no band: the keys start at the sequence's
-    // first key, kv_len = the sequence's keys); the halves' step ranges are
-    // clamped to the list.
-    const int nkb = (d.kv_len + 127) / 128;
-    d.n_kv = d.nrows0 > 0 ? min(max(p.blk_ptr[t + 1] - p.blk_ptr[t], 0), nkb) : 0;
-  }
-  return d;
+  return finish_tile<BCAST, GEN, SP>(p, fetch_raw<BCAST, SP>(p, tile_bhm<DYN>(p, t), t));
 }
 
 // List entry of step j (lst: the tile's first entry): the key block (clamped
@@ -316,15 +344,23 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       // (Dynamic: t counts this CTA's tiles and id is the index of tile t.)
       int4 bhm = DYN ? produce_at(0) : make_int4(-1, 0, 0, 0);
       FwdTile nxt{};
-      if (DYN ? bhm.x >= 0 : tbeg < tend)
-        nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN, SP>(p, tbeg);
+      if (DYN && bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
+      FwdRaw raw{};  // static: decode loads issued a tile ahead (as the MMA thread)
+      int4 ent = make_int4(-1, 0, 0, 0);
+      if (!DYN && tbeg < tend) {
+        raw = fetch_raw<BCAST, SP>(p, tile_bhm<DYN>(p, tbeg), tbeg);
+        if (tbeg + 1 < tend) ent = tile_bhm<DYN>(p, tbeg + 1);
+      }
       for (int t = tbeg; DYN ? bhm.x >= 0 : t < tend; ++t) {
-        const FwdTile tl = nxt;
+        FwdTile tl;
         if (DYN) {
+          tl = nxt;
           bhm = produce_at(t + 1);
           if (bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
-        } else if (t + 1 < tend) {
-          nxt = decode_tile<BCAST, GEN, DYN, SP>(p, t + 1);
+        } else {
+          tl = finish_tile<BCAST, GEN, SP>(p, raw);
+          if (t + 1 < tend) raw = fetch_raw<BCAST, SP>(p, ent, t + 1);
+          if (t + 2 < tend) ent = tile_bhm<DYN>(p, t + 2);
         }
         if (tl.n_kv == 0) continue;
 #pragma unroll
@@ -411,19 +447,30 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, vd + (k * 2048 >> 4), C::IDESC_PV,
                  (acc || k > 0) ? 1u : 0u);
       };
-      // The next tile is decoded one tile ahead (its index loads are off the
-      // critical path at the tile switch).
+      // Dynamic: the next tile is decoded one tile ahead. Static: the loads of
+      // tile t + 1's decode (its offsets, from its list entry fetched a tile
+      // earlier) and of tile t + 2's list entry are issued at the top of tile
+      // t and used at the top of tile t + 1, so no dependent load is waited
+      // for at a tile switch.
       int4 bhm = DYN ? tile_at(0, 1u) : make_int4(-1, 0, 0, 0);
       FwdTile nxt{};
-      if (DYN ? bhm.x >= 0 : tbeg < tend)
-        nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN, SP>(p, tbeg);
+      if (DYN && bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
+      FwdRaw raw{};
+      int4 ent = make_int4(-1, 0, 0, 0);
+      if (!DYN && tbeg < tend) {
+        raw = fetch_raw<BCAST, SP>(p, tile_bhm<DYN>(p, tbeg), tbeg);
+        if (tbeg + 1 < tend) ent = tile_bhm<DYN>(p, tbeg + 1);
+      }
       for (int t = tbeg; DYN ? bhm.x >= 0 : t < tend; ++t) {
-        const FwdTile tl = nxt;
+        FwdTile tl;
         if (DYN) {
+          tl = nxt;
           bhm = tile_at(t + 1, 1u);
           if (bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
-        } else if (t + 1 < tend) {
-          nxt = decode_tile<BCAST, GEN, DYN, SP>(p, t + 1);
+        } else {
+          tl = finish_tile<BCAST, GEN, SP>(p, raw);
+          if (t + 1 < tend) raw = fetch_raw<BCAST, SP>(p, ent, t + 1);
+          if (t + 2 < tend) ent = tile_bhm<DYN>(p, t + 2);
         }
         if (tl.n_kv == 0) continue;
         // Each half's steps [lo, hi): every step without a band.
@@ -502,6 +549,8 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
     const float sl2 = p.scale_log2;
     uint32_t sph = 0, oph = 0;
     __nv_bfloat16 *obase = static_cast<__nv_bfloat16 *>(p.o);
+    // The next tile is decoded one tile ahead (its index loads are off the
+    // critical path at the tile switch).
     // The next tile is decoded one tile ahead (its index loads are off the
     // critical path at the tile switch).
     int4 bhm = DYN ? tile_at(0, 0xffffffffu) : make_int4(-1, 0, 0, 0);
