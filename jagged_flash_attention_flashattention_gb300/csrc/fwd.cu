@@ -109,10 +109,61 @@ __device__ __forceinline__ int4 tile_bhm(const FwdParams &p, int t) {
   return make_int4(p.tiles[3 * t], p.tiles[3 * t + 1], p.tiles[3 * t + 2], 1);
 }
 
-// The loads of a tile's decode: its list entry, its sequence's offsets as
-// stored (clamped later) and, with a block mask, its list bounds. Split from
-// the arithmetic so that a role can issue them a tile ahead and use them a
-// tile later without waiting.
+// GEN: the band mask is compiled in (jfa_varlen_fwd with a window); without
+// it every row sees all of its sequence's keys.
+template <bool BCAST, bool GEN>
+__device__ __forceinline__ FwdTile decode_bhm(const FwdParams &p, int4 bhm) {
+  FwdTile d;
+  d.b = bhm.x;
+  d.h = bhm.y;
+  const int m = bhm.z;
+  // A tile outside this batch (a schedule built for another one) is empty,
+  // and sequence bounds are clamped to [0, T]: no row past the tensors is
+  // read or written whatever the tile list or the offsets hold.
+  const bool in = d.b >= 0 && d.b < p.B && d.h >= 0 && d.h < p.H && m >= 0 && m < (1 << 22);
+  const int64_t s0 = in ? min(max(load_off(p.offsets, p.idx64, d.b), (int64_t)0), p.T) : 0;
+  const int64_t e0 = in ? min(max(load_off(p.offsets, p.idx64, d.b + 1), s0), p.T) : 0;
+  const int L = (int)(e0 - s0);
+  int64_t qs = 0;
+  int Lq;
+  if (BCAST) {
+    Lq = in ? p.Lq : 0;
+  } else {
+    qs = in ? min(max(load_off(p.q_offsets, p.idx64, d.b), (int64_t)0), p.Tq) : 0;
+    Lq = (int)(in ? min(max(load_off(p.q_offsets, p.idx64, d.b + 1), qs), p.Tq) - qs : 0);
+  }
+  const int row0 = m * 256;
+  d.nrows0 = max(0, min(128, Lq - row0));
+  d.nrows1 = max(0, min(128, Lq - row0 - 128));
+  // Keys the tile's rows can see (all of them without a band mask), in
+  // 128-key tiles: K/V tiles j0 .. j0 + n_kv - 1 of the sequence.
+  int64_t lo = 0, hi = 0;
+  if (d.nrows0 > 0)
+    fwd_key_range(row0, row0 + d.nrows0 + d.nrows1, Lq, L, GEN ? p.win_left : -1,
+                  GEN ? p.win_right : -1, &lo, &hi);
+  const int j0 = (int)(lo / 128);
+  d.n_kv = hi > lo ? (int)((hi + 127) / 128) - j0 : 0;
+  d.kv_len = L - j0 * 128;
+  d.diag0 = row0 + (L - Lq) - j0 * 128;
+  d.kv0 = (int)s0 + j0 * 128;
+  if (BCAST) {
+    d.q_coord = row0;
+    d.out_row0 = (int64_t)d.b * Lq + row0;
+    d.lse0 = ((int64_t)d.b * p.H + d.h) * Lq + row0;
+  } else {
+    d.q_coord = (int)qs + row0;
+    d.out_row0 = qs + row0;
+    d.lse0 = (int64_t)d.h * p.Tq + qs + row0;
+  }
+  return d;
+}
+
+// decode_tile split in two for the pipelined decode: the loads (the list
+// entry, the sequence's offsets as stored, the block list bounds) and the
+// arithmetic, so that a role can issue the loads a tile ahead and use them a
+// tile later without waiting. finish_tile(fetch_raw(...)) equals decode_tile;
+// the one-ahead decode keeps the single function, whose code the masked
+// instantiation measured faster with.
 struct FwdRaw {
   int4 bhm;
   int64_t s0, e0, qs, qe;
@@ -190,11 +241,6 @@ __device__ __forceinline__ FwdTile finish_tile(const FwdParams &p, const FwdRaw 
   return d;
 }
 
-template <bool BCAST, bool GEN>
-__device__ __forceinline__ FwdTile decode_bhm(const FwdParams &p, int4 bhm) {
-  return finish_tile<BCAST, GEN, false>(p, fetch_raw<BCAST, false>(p, bhm, 0));
-}
-
 // K/V steps [lo, hi) of the tile (counted from its first loaded K/V tile)
 // that query half x can see. Without a band both halves walk every step;
 // with one, e.g. causal, the first half skips the last tile. A half with
@@ -228,7 +274,16 @@ __device__ __forceinline__ int2 half_steps(const FwdTile &tl, const FwdParams &p
 // SP: block-sparse masks compiled in (with GEN, no band).
 template <bool BCAST, bool GEN, bool DYN, bool SP>
 __device__ __forceinline__ FwdTile decode_tile(const FwdParams &p, int t) {
-  return finish_tile<BCAST, GEN, SP>(p, fetch_raw<BCAST, SP>(p, tile_bhm<DYN>(p, t), t));
+  FwdTile d = decode_bhm<BCAST, GEN>(p, tile_bhm<DYN>(p, t));
+  if (SP) {
+    // Block-sparse: the tile's steps are its list entries, at most one per
+    // key block of the sequence (no band: the keys start at the sequence's
+    // first key, kv_len = the sequence's keys); the halves' step ranges are
+    // clamped to the list.
+    const int nkb = (d.kv_len + 127) / 128;
+    d.n_kv = d.nrows0 > 0 ? min(max(p.blk_ptr[t + 1] - p.blk_ptr[t], 0), nkb) : 0;
+  }
+  return d;
 }
 
 // List entry of step j (lst: the tile's first entry): the key block (clamped
@@ -248,6 +303,9 @@ __device__ __forceinline__ bool half_sees(uint32_t e, int x) { return (e >> (kBl
 template <int D, bool BCAST, bool GEN, bool DYN, bool SP>
 __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
+  // Static schedule, unmasked: the producer and the MMA thread pipeline their
+  // tile decode (measured faster there; slower in the masked instantiation).
+  constexpr bool PIPE = !DYN && !GEN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -342,12 +400,14 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
       // The next tile is decoded one tile ahead (its index loads are off the
       // critical path at the tile switch).
       // (Dynamic: t counts this CTA's tiles and id is the index of tile t.)
+      // Tile decode as in the MMA thread below.
       int4 bhm = DYN ? produce_at(0) : make_int4(-1, 0, 0, 0);
       FwdTile nxt{};
-      if (DYN && bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
-      FwdRaw raw{};  // static: decode loads issued a tile ahead (as the MMA thread)
+      if (DYN ? bhm.x >= 0 : (!PIPE && tbeg < tend))
+        nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN, SP>(p, tbeg);
+      FwdRaw raw{};
       int4 ent = make_int4(-1, 0, 0, 0);
-      if (!DYN && tbeg < tend) {
+      if (PIPE && tbeg < tend) {
         raw = fetch_raw<BCAST, SP>(p, tile_bhm<DYN>(p, tbeg), tbeg);
         if (tbeg + 1 < tend) ent = tile_bhm<DYN>(p, tbeg + 1);
       }
@@ -357,10 +417,13 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           tl = nxt;
           bhm = produce_at(t + 1);
           if (bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
-        } else {
+        } else if (PIPE) {
           tl = finish_tile<BCAST, GEN, SP>(p, raw);
           if (t + 1 < tend) raw = fetch_raw<BCAST, SP>(p, ent, t + 1);
           if (t + 2 < tend) ent = tile_bhm<DYN>(p, t + 2);
+        } else {
+          tl = nxt;
+          if (t + 1 < tend) nxt = decode_tile<BCAST, GEN, DYN, SP>(p, t + 1);
         }
         if (tl.n_kv == 0) continue;
 #pragma unroll
@@ -447,17 +510,18 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, vd + (k * 2048 >> 4), C::IDESC_PV,
                  (acc || k > 0) ? 1u : 0u);
       };
-      // Dynamic: the next tile is decoded one tile ahead. Static: the loads of
-      // tile t + 1's decode (its offsets, from its list entry fetched a tile
-      // earlier) and of tile t + 2's list entry are issued at the top of tile
-      // t and used at the top of tile t + 1, so no dependent load is waited
-      // for at a tile switch.
+      // Dynamic, and masked instantiations: the next tile is decoded one tile
+      // ahead. Static unmasked (PIPE): the loads of tile t + 1's decode (its
+      // offsets, from its list entry fetched a tile earlier) and of tile
+      // t + 2's list entry are issued at the top of tile t and used at the top
+      // of tile t + 1, so no dependent load is waited for at a tile switch.
       int4 bhm = DYN ? tile_at(0, 1u) : make_int4(-1, 0, 0, 0);
       FwdTile nxt{};
-      if (DYN && bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
+      if (DYN ? bhm.x >= 0 : (!PIPE && tbeg < tend))
+        nxt = DYN ? decode_bhm<BCAST, GEN>(p, bhm) : decode_tile<BCAST, GEN, DYN, SP>(p, tbeg);
       FwdRaw raw{};
       int4 ent = make_int4(-1, 0, 0, 0);
-      if (!DYN && tbeg < tend) {
+      if (PIPE && tbeg < tend) {
         raw = fetch_raw<BCAST, SP>(p, tile_bhm<DYN>(p, tbeg), tbeg);
         if (tbeg + 1 < tend) ent = tile_bhm<DYN>(p, tbeg + 1);
       }
@@ -467,10 +531,13 @@ __global__ void __launch_bounds__(384, 1) jfa_fwd_kernel(const __grid_constant__
           tl = nxt;
           bhm = tile_at(t + 1, 1u);
           if (bhm.x >= 0) nxt = decode_bhm<BCAST, GEN>(p, bhm);
-        } else {
+        } else if (PIPE) {
           tl = finish_tile<BCAST, GEN, SP>(p, raw);
           if (t + 1 < tend) raw = fetch_raw<BCAST, SP>(p, ent, t + 1);
           if (t + 2 < tend) ent = tile_bhm<DYN>(p, t + 2);
+        } else {
+          tl = nxt;
+          if (t + 1 < tend) nxt = decode_tile<BCAST, GEN, DYN, SP>(p, t + 1);
         }
         if (tl.n_kv == 0) continue;
         // Each half's steps [lo, hi): every step without a band.

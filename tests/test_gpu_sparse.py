@@ -28,13 +28,13 @@ def _cross_inputs(q_lengths, kv_lengths, H, D, seed):
     return {"q": q["q"], "do": q["do"], "k": kv["k"], "v": kv["v"]}
 
 
-def _offs(q_lengths, kv_lengths):
-    return (torch.from_numpy(W.offsets_of(q_lengths)).cuda(),
-            torch.from_numpy(W.offsets_of(kv_lengths)).cuda())
+def _offs(q_lengths, kv_lengths, dtype=np.int64):
+    return (torch.from_numpy(W.offsets_of(q_lengths, dtype)).cuda(),
+            torch.from_numpy(W.offsets_of(kv_lengths, dtype)).cuda())
 
 
-def _run(inp, q_lengths, kv_lengths, H, D, masks):
-    qo, ko = _offs(q_lengths, kv_lengths)
+def _run(inp, q_lengths, kv_lengths, H, D, masks, dtype=np.int64):
+    qo, ko = _offs(q_lengths, kv_lengths, dtype)
     plan = jfa.Plan(ko, H, D, kind="sparse", q_offsets=qo, block_masks=masks)
     o, lse = jfa.jfa_sparse_fwd(inp["q"], inp["k"], inp["v"], qo, ko, plan=plan)
     g = jfa.jfa_sparse_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], qo, ko, plan=plan)
@@ -64,15 +64,15 @@ def test_random_masks_ragged_self(D, density):
     _check(inp, RAGGED, RAGGED, D, masks, _run(inp, RAGGED, RAGGED, H, D, masks))
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_block_causal_cross(D):
+@pytest.mark.parametrize("D,dtype", [(64, np.int64), (128, np.int64), (128, np.int32)])
+def test_block_causal_cross(D, dtype):
     # Lq != Lk, empty query and empty key sequences, block-causal masks
     H = 2
     ql = [300, 0, 129, 700, 64, 513, 5]
     kl = [129, 40, 0, 1000, 640, 513, 300]
     masks = W.block_masks(ql, kl, 143, density=0.5)
     inp = _cross_inputs(ql, kl, H, D, 144)
-    _check(inp, ql, kl, D, masks, _run(inp, ql, kl, H, D, masks))
+    _check(inp, ql, kl, D, masks, _run(inp, ql, kl, H, D, masks, dtype))
 
 
 def test_empty_block_rows_and_columns_are_exact_zeros():
