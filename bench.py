@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 # the first 256 sequences (dram__bytes_read.sum + dram__bytes_write.sum)
 # scaled by the processed (key tile, query block) pairs. Reset to None
 # whenever the backward kernel changes until it is measured again.
-BWD_GEM_TRAFFIC = 4.220e9  # 680.3 + 326.5 MB on 256 sequences, x 4.1917 (129,708 / 30,944 pairs)
+BWD_GEM_TRAFFIC = 4.224e9  # 680.6 + 327.1 MB on 256 sequences, x 4.1917 (129,708 / 30,944 pairs)
 
 # Nominal dense bf16 tensor peak of one GB300 (NVIDIA's figure without 2:4
 # sparsity), the second denominator reported next to the measured cuBLAS peak.
