@@ -1,0 +1,130 @@
+"""Seeded random sweeps of the jagged, masked / cross and broadcast-Q paths
+against the fp64 oracle, through the C ABI: batch sizes, lengths (zero,
+one, every tile edge and random), head counts including odd ones, both head
+dimensions, both offset index types and non-default softmax scales, drawn
+per case from a fixed seed so that a failure names a reproducible case.
+
+Unusual draws (a larger scale, hundreds of queries on a two-key sequence)
+give gradients far above 1 in magnitude. Each output element is a sum of
+products whose bf16 operands (P, dS and the inputs) carry a relative rounding
+of up to 2^-9, so its error grows with the size of the terms: the absolute
+bound here is the usual 2e-2 or 2^-7 (four such roundings) of the tensor's
+largest reference magnitude, whichever is larger; the relative L2 bound stays
+1e-2."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import jagged_flash_attention_flashattention_gb300 as jfa
+from jagged_flash_attention_flashattention_gb300 import workloads as W
+from oracle import attention as A
+from tests._util import ATOL, assert_close, assert_lse, f64
+
+pytestmark = pytest.mark.gpu
+
+EDGES = [0, 1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 512, 513]
+
+
+def _lengths(rng, lo_b=1, hi_b=12, cap=900):
+    B = int(rng.integers(lo_b, hi_b + 1))
+    pick_edge = rng.random(B) < 0.5
+    return [int(rng.choice(EDGES)) if e else int(rng.integers(1, cap)) for e in pick_edge]
+
+
+def _close(got, ref, name, bf16_out=True):
+    atol = max(ATOL, 2.0 ** -7 * float(np.abs(f64(ref)).max(initial=0.0)))
+    assert_close(got, ref, name, atol=atol, bf16_out=bf16_out)
+
+
+def _case(seed):
+    rng = np.random.default_rng(seed)
+    H = int(rng.choice([1, 2, 3, 5]))
+    D = int(rng.choice([64, 128]))
+    idx = np.int32 if rng.random() < 0.5 else np.int64
+    # the default 1/sqrt(D), or a larger or smaller one (a larger scale makes
+    # the running maximum jump, so the lazy rescale of O runs)
+    scale = None if rng.random() < 0.5 else float(rng.choice([0.02, 0.25, 0.5])) / math.sqrt(D) * 8
+    return rng, H, D, idx, scale
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_jagged_random_batches(seed):
+    rng, H, D, idx, scale = _case(1000 + seed)
+    lengths = _lengths(rng)
+    if sum(lengths) == 0:
+        lengths[0] = 1
+    s = scale if scale is not None else 1 / math.sqrt(D)
+    inp = W.jagged_inputs(lengths, H, D, 2000 + seed, device="cuda")
+    off = torch.from_numpy(W.offsets_of(lengths, idx)).cuda()
+    plan = jfa.Plan(off, H, D)
+    o, lse = jfa.jfa_fwd(inp["q"], inp["k"], inp["v"], off, scale=scale, plan=plan)
+    g = jfa.jfa_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], off, scale=scale, plan=plan)
+    plan.check()
+    q, k, v, do = (f64(inp[n]) for n in ("q", "k", "v", "do"))
+    offs = W.offsets_of(lengths)
+    ro, rl = A.jagged_fwd(q, k, v, offs, s)
+    tag = "case %d (lengths %s, H=%d, D=%d, %s, scale %s)" % (seed, lengths, H, D, idx.__name__, scale)
+    _close(o, ro, "O " + tag)
+    assert_lse(lse, rl, "LSE " + tag)
+    for name, a, b in zip(("dQ", "dK", "dV"), g, A.jagged_bwd(q, k, v, do, offs, s)):
+        _close(a, b, name + " " + tag)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_masked_cross_random_batches(seed):
+    rng, H, D, idx, scale = _case(3000 + seed)
+    ql = _lengths(rng, hi_b=8, cap=700)
+    kl = [int(x) if rng.random() < 0.4 else int(rng.integers(0, 700)) for x in ql]
+    if sum(ql) == 0:
+        ql[0] = 1
+    if sum(kl) == 0:
+        kl[0] = 1
+    window = (int(rng.choice([-1, 0, 5, 64, 200])), int(rng.choice([-1, 0, 3, 128])))
+    s = scale if scale is not None else 1 / math.sqrt(D)
+    qi = W.jagged_inputs(ql, H, D, 4000 + seed, device="cuda")
+    ki = W.jagged_inputs(kl, H, D, 4500 + seed, device="cuda")
+    q, do, k, v = qi["q"], qi["do"], ki["k"], ki["v"]
+    qo = torch.from_numpy(W.offsets_of(ql, idx)).cuda()
+    ko = torch.from_numpy(W.offsets_of(kl, idx)).cuda()
+    plan = jfa.Plan(ko, H, D, kind="varlen", q_offsets=qo, window=window)
+    o, lse = jfa.jfa_varlen_fwd(q, k, v, qo, ko, scale=scale, window=window, plan=plan)
+    g = jfa.jfa_varlen_bwd(q, k, v, o, lse, do, qo, ko, scale=scale, window=window, plan=plan)
+    plan.check()
+    Q, K, V, dO = (f64(x) for x in (q, k, v, do))
+    qoh, koh = W.offsets_of(ql), W.offsets_of(kl)
+    tag = "case %d (q %s, kv %s, window %s, H=%d, D=%d)" % (seed, ql, kl, window, H, D)
+    ro, rl = A.varlen_fwd(Q, K, V, qoh, koh, s, window)
+    _close(o, ro, "O " + tag)
+    assert_lse(lse, rl, "LSE " + tag)
+    for name, a, b in zip(("dQ", "dK", "dV"), g, A.varlen_bwd(Q, K, V, dO, qoh, koh, s, window)):
+        _close(a, b, name + " " + tag)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_bcastq_random_batches(seed):
+    rng, H, D, idx, scale = _case(5000 + seed)
+    lengths = _lengths(rng, hi_b=10, cap=600)
+    if sum(lengths) == 0:
+        lengths[0] = 1
+    Lq = int(rng.choice([1, 37, 128, 129, 256, 300]))
+    s = scale if scale is not None else 1 / math.sqrt(D)
+    inp = W.bcast_inputs(lengths, Lq, H, D, 6000 + seed, device="cuda")
+    off = torch.from_numpy(W.offsets_of(lengths, idx)).cuda()
+    plan = jfa.Plan(off, H, D, kind="bcast", Lq=Lq)
+    o, lse = jfa.jfa_bcastq_fwd(inp["q"], inp["k"], inp["v"], off, scale=scale, plan=plan)
+    g = jfa.jfa_bcastq_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], off, scale=scale,
+                           plan=plan)
+    plan.check()
+    q, k, v, do = (f64(inp[n]) for n in ("q", "k", "v", "do"))
+    offs = W.offsets_of(lengths)
+    tag = "case %d (lengths %s, Lq=%d, H=%d, D=%d)" % (seed, lengths, Lq, H, D)
+    ro, rl = A.bcastq_fwd(q, k, v, offs, s)
+    _close(o, ro, "O " + tag)
+    assert_lse(lse, rl, "LSE " + tag)
+    rdq, rdk, rdv = A.bcastq_bwd(q, k, v, do, offs, s)
+    _close(g[0], rdq, "dQ " + tag, bf16_out=False)  # fp32 output: no bf16 rounding slack
+    _close(g[1], rdk, "dK " + tag)
+    _close(g[2], rdv, "dV " + tag)
