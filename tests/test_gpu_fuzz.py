@@ -1,5 +1,6 @@
-"""Seeded random sweeps of the jagged, masked / cross and broadcast-Q paths
-against the fp64 oracle, through the C ABI: batch sizes, lengths (zero,
+"""Seeded random sweeps of the jagged, masked / cross, broadcast-Q,
+block-sparse, block-diagonal and rotary paths against the fp64 oracle,
+through the C ABI: batch sizes, lengths (zero,
 one, every tile edge and random), head counts including odd ones, both head
 dimensions, both offset index types and non-default softmax scales, drawn
 per case from a fixed seed so that a failure names a reproducible case.
@@ -128,3 +129,90 @@ def test_bcastq_random_batches(seed):
     _close(g[0], rdq, "dQ " + tag, bf16_out=False)  # fp32 output: no bf16 rounding slack
     _close(g[1], rdk, "dK " + tag)
     _close(g[2], rdv, "dV " + tag)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_block_sparse_random_batches(seed):
+    rng, H, D, idx, scale = _case(7000 + seed)
+    ql = _lengths(rng, hi_b=8, cap=700)
+    kl = [int(x) if rng.random() < 0.5 else int(rng.integers(0, 700)) for x in ql]
+    if sum(ql) == 0:
+        ql[0] = 1
+    if sum(kl) == 0:
+        kl[0] = 1
+    masks = [rng.random((-(-a // 128), -(-b // 128))) < rng.uniform(0.1, 1.0) for a, b in zip(ql, kl)]
+    s = scale if scale is not None else 1 / math.sqrt(D)
+    qi = W.jagged_inputs(ql, H, D, 7500 + seed, device="cuda")
+    ki = W.jagged_inputs(kl, H, D, 7800 + seed, device="cuda")
+    q, do, k, v = qi["q"], qi["do"], ki["k"], ki["v"]
+    qo = torch.from_numpy(W.offsets_of(ql, idx)).cuda()
+    ko = torch.from_numpy(W.offsets_of(kl, idx)).cuda()
+    plan = jfa.Plan(ko, H, D, kind="sparse", q_offsets=qo, block_masks=masks)
+    o, lse = jfa.jfa_sparse_fwd(q, k, v, qo, ko, scale=scale, plan=plan)
+    g = jfa.jfa_sparse_bwd(q, k, v, o, lse, do, qo, ko, scale=scale, plan=plan)
+    plan.check()
+    Q, K, V, dO = (f64(x) for x in (q, k, v, do))
+    qoh, koh = W.offsets_of(ql), W.offsets_of(kl)
+    tag = "case %d (q %s, kv %s, H=%d, D=%d)" % (seed, ql, kl, H, D)
+    ro, rl = A.blocksparse_fwd(Q, K, V, qoh, koh, masks, s)
+    _close(o, ro, "O " + tag)
+    assert_lse(lse, rl, "LSE " + tag)
+    for name, a, b in zip(("dQ", "dK", "dV"), g, A.blocksparse_bwd(Q, K, V, dO, qoh, koh, masks, s)):
+        _close(a, b, name + " " + tag)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_blockdiag_random_shapes(seed):
+    rng, H, D, _, scale = _case(8000 + seed)
+    B, L = int(rng.integers(1, 5)), 64 * int(rng.integers(1, 11))
+    s = scale if scale is not None else 1 / math.sqrt(D)
+    inp = W.blockdiag_inputs(B, L, H, D, 8100 + seed, device="cuda")
+    o = jfa.blockdiag_fwd(inp["q"], inp["k"], inp["v"], scale=scale)
+    g = jfa.blockdiag_bwd(inp["q"], inp["k"], inp["v"], inp["do"], scale=scale)
+    jfa.check_status()
+    q, k, v, do = (f64(inp[n]) for n in ("q", "k", "v", "do"))
+    tag = "case %d (B=%d, L=%d, H=%d, D=%d)" % (seed, B, L, H, D)
+    _close(o, A.blockdiag_fwd(q, k, v, s), "O " + tag)
+    for name, a, b in zip(("dQ", "dK", "dV"), g, A.blockdiag_bwd(q, k, v, do, s)):
+        _close(a, b, name + " " + tag)
+    # the same shapes with rotary embeddings: the forward rotates q and k
+    # itself; the backward takes the oracle's rotated rows, rounded to bf16
+    cos, sin = W.rotary_tables(L, D, device="cuda")
+    o_r = jfa.blockdiag_rotary_fwd(inp["q"], inp["k"], inp["v"], cos, sin, scale=scale)
+    c, sn = f64(cos), f64(sin)
+    _close(o_r, A.blockdiag_rotary_fwd(q, k, v, c, sn, s), "rotary O " + tag)
+    qr64, kr64 = A.rope(q, c, sn), A.rope(k, c, sn)
+    qr = torch.from_numpy(qr64).to(torch.bfloat16).cuda()
+    kr = torch.from_numpy(kr64).to(torch.bfloat16).cuda()
+    g_r = jfa.blockdiag_rotary_bwd(qr, kr, inp["v"], inp["do"], cos, sin, scale=scale)
+    jfa.check_status()
+    ref = A.blockdiag_rotary_bwd_from_rotated(f64(qr), f64(kr), v, do, c, sn, s)
+    for name, a, b in zip(("dQ", "dK", "dV"), g_r, ref):
+        _close(a, b, "rotary " + name + " " + tag)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_jagged_rotary_random_batches(seed):
+    rng, H, D, idx, scale = _case(9000 + seed)
+    lengths = _lengths(rng, hi_b=8, cap=700)
+    if sum(lengths) == 0:
+        lengths[0] = 1
+    s = scale if scale is not None else 1 / math.sqrt(D)
+    offs = W.offsets_of(lengths)
+    inp = W.jagged_inputs(lengths, H, D, 9100 + seed, device="cuda")
+    off = torch.from_numpy(W.offsets_of(lengths, idx)).cuda()
+    cos, sin = W.rotary_tables(max(lengths), D, device="cuda")
+    c, sn = f64(cos), f64(sin)
+    plan = jfa.Plan(off, H, D)
+    tag = "case %d (lengths %s, H=%d, D=%d)" % (seed, lengths, H, D)
+    q_rot = jfa.jfa_rope(inp["q"], off, cos, sin, plan=plan)
+    _close(q_rot, A.jagged_rope(f64(inp["q"]), offs, c, sn), "q_rot " + tag)
+    qr = torch.from_numpy(A.jagged_rope(f64(inp["q"]), offs, c, sn)).to(torch.bfloat16).cuda()
+    kr = torch.from_numpy(A.jagged_rope(f64(inp["k"]), offs, c, sn)).to(torch.bfloat16).cuda()
+    o, lse = jfa.jfa_fwd(qr, kr, inp["v"], off, scale=scale, plan=plan)
+    g = jfa.jfa_rotary_bwd(qr, kr, inp["v"], o, lse, inp["do"], off, cos, sin, scale=scale, plan=plan)
+    plan.check()
+    ref = A.jagged_rotary_bwd_from_rotated(f64(qr), f64(kr), f64(inp["v"]), f64(inp["do"]), offs,
+                                           c, sn, s)
+    for name, a, b in zip(("dQ", "dK", "dV"), g, ref):
+        _close(a, b, name + " " + tag)
