@@ -216,3 +216,54 @@ def test_jagged_rotary_random_batches(seed):
                                            c, sn, s)
     for name, a, b in zip(("dQ", "dK", "dV"), g, ref):
         _close(a, b, name + " " + tag)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_schedules_and_modes_agree_random_batches(seed):
+    # Every way of running the same batch walks each tile's keys in the same
+    # order with the same arithmetic: O and LSE are bit-identical across the
+    # static zigzag and naive deals, both dynamic orders and (D = 128) the
+    # CTA-pair forward; dK and dV (fixed accumulation order) across the
+    # deals; the deterministic dQ across two runs.
+    rng, H, D, idx, scale = _case(9500 + seed)
+    lengths = _lengths(rng)
+    if sum(lengths) == 0:
+        lengths[0] = 1
+    tag = "case %d (lengths %s, H=%d, D=%d)" % (seed, lengths, H, D)
+    inp = W.jagged_inputs(lengths, H, D, 9600 + seed, device="cuda")
+    off = torch.from_numpy(W.offsets_of(lengths, idx)).cuda()
+    q, k, v, do = (inp[n] for n in ("q", "k", "v", "do"))
+    ref = None
+    for zz in (True, False):
+        plan = jfa.Plan(off, H, D, zigzag=zz)
+        o, lse = jfa.jfa_fwd(q, k, v, off, scale=scale, plan=plan)
+        g = jfa.jfa_bwd(q, k, v, o, lse, do, off, scale=scale, plan=plan)
+        plan.check()
+        if ref is None:
+            ref = (o, lse, g)
+        else:
+            assert torch.equal(o, ref[0]) and torch.equal(lse, ref[1]), "naive deal O/LSE " + tag
+            assert torch.equal(g[1], ref[2][1]) and torch.equal(g[2], ref[2][2]), "naive deal dK/dV " + tag
+    for order in ("device", "lpt"):
+        dplan = jfa.DynamicPlan(off, H, D, order=order)
+        o, lse = jfa.jfa_fwd_dynamic(q, k, v, off, scale=scale, plan=dplan)
+        dplan.check()
+        assert torch.equal(o, ref[0]) and torch.equal(lse, ref[1]), "dynamic %s %s" % (order, tag)
+    if D == 128:
+        pplan = jfa.Plan(off, H, D, pair=True)
+        o, lse = jfa.jfa_fwd(q, k, v, off, scale=scale, plan=pplan)
+        pplan.check()
+        assert torch.equal(o, ref[0]) and torch.equal(lse, ref[1]), "pair " + tag
+    dets = []
+    for _ in range(2):
+        vplan = jfa.Plan(off, H, D, kind="varlen", window=(-1, -1), deterministic=True)
+        o, lse = jfa.jfa_varlen_fwd(q, k, v, off, off, scale=scale, plan=vplan)
+        dets.append(jfa.jfa_varlen_bwd(q, k, v, o, lse, do, off, off, scale=scale, deterministic=True,
+                                       plan=vplan))
+        vplan.check()
+    assert torch.equal(dets[0][0], dets[1][0]), "deterministic dQ differs between runs " + tag
+    s = scale if scale is not None else 1 / math.sqrt(D)
+    offs = W.offsets_of(lengths)
+    Q, K, V, dO = (f64(x) for x in (q, k, v, do))
+    for name, a, b in zip(("dQ", "dK", "dV"), dets[0], A.jagged_bwd(Q, K, V, dO, offs, s)):
+        _close(a, b, "deterministic " + name + " " + tag)
