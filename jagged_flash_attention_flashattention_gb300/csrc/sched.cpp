@@ -152,8 +152,24 @@ void deal(const std::vector<Tile> &all, int num_sms, int zigzag, int32_t *sm_ptr
   std::vector<int32_t> order(n);
   std::iota(order.begin(), order.end(), 0);
   if (zigzag) {
-    std::stable_sort(order.begin(), order.end(),
-                     [&](int32_t a, int32_t b) { return all[a].work > all[b].work; });
+    // Stable sort by work, largest first: a counting sort when the work
+    // values span a modest range (they are token counts), else a merge sort;
+    // both keep equal works in enumeration order.
+    int64_t wmax = 0;
+    bool small = true;
+    for (const Tile &t : all) {
+      if (t.work < 0) small = false;
+      wmax = std::max(wmax, t.work);
+    }
+    if (small && wmax < (int64_t(1) << 20)) {
+      std::vector<int32_t> start(wmax + 2, 0);
+      for (const Tile &t : all) ++start[wmax - t.work + 1];  // bucket of work w: wmax - w
+      for (int64_t w = 0; w <= wmax; ++w) start[w + 1] += start[w];
+      for (int64_t i = 0; i < n; ++i) order[start[wmax - all[i].work]++] = (int32_t)i;
+    } else {
+      std::stable_sort(order.begin(), order.end(),
+                       [&](int32_t a, int32_t b) { return all[a].work > all[b].work; });
+    }
   }
   std::vector<int32_t> sm_of(n);
   std::vector<int32_t> cnt(num_sms, 0);
@@ -270,8 +286,18 @@ jfa_status enumerate_sparse(int64_t B, int H, jfa_op op, const void *q_off, cons
   if (need > 0 && !masks) return fail(JFA_ERR_INVALID_ARG, "masks is NULL");
   int64_t n = 0, ne = 0, moff = 0;
   std::vector<int32_t> ent;
-  std::vector<int64_t> work;
+  std::vector<int64_t> work, tb;
   std::vector<int32_t> meta;
+  if (fill) {  // sizes from a counting pass, so the fill never reallocates
+    int64_t cn = 0, cne = 0;
+    jfa_status cst = enumerate_sparse(B, H, op, q_off, kv_off, idx, masks, n_mask, false, nullptr,
+                                      &cn, &cne);
+    if (cst != JFA_OK) return cst;
+    out->tiles.reserve(cn);
+    out->beg.reserve(cn + 1);
+    out->entries.reserve(cne);
+    if (op == JFA_OP_FWD) out->meta.reserve(4 * cn);
+  }
   for (int64_t b = 0; b < B; ++b) {
     const int64_t Lq = offset_at(q_off, idx, b + 1) - offset_at(q_off, idx, b);
     const int64_t Lk = offset_at(kv_off, idx, b + 1) - offset_at(kv_off, idx, b);
@@ -281,7 +307,7 @@ jfa_status enumerate_sparse(int64_t B, int H, jfa_op op, const void *q_off, cons
     auto sees = [&](int64_t qb, int64_t kb) { return qb < nqb && mk[qb * nkb + kb] != 0; };
     const int64_t n_m = op == JFA_OP_FWD ? (Lq + kFwdTileRows - 1) / kFwdTileRows : nkb;
     // Per tile of this sequence (shared by its H heads): entries, work, meta.
-    std::vector<int64_t> tb(n_m + 1, 0);
+    tb.assign(n_m + 1, 0);
     ent.clear();
     work.assign(n_m, 0);
     meta.assign(4 * n_m, 0);
