@@ -360,8 +360,19 @@ class Plan:
                            zigzag=zigzag)
             bwd = schedule(host, H, tile_rows(OP_BCASTQ_BWD, D), self.n_sms, fixed_work=self.Lq,
                            zigzag=zigzag)
-        self._pinned = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in fwd + bwd]
-        d = [t.to(dev, non_blocking=True) for t in self._pinned]
+        # All the int32 lists go up in one pinned staging buffer and one copy,
+        # each starting on a 16-byte boundary (the kernels read some as int4).
+        arrs = [np.ascontiguousarray(a, dtype=np.int32) for a in fwd + bwd]
+        starts, total = [], 0
+        for a in arrs:
+            starts.append(total)
+            total += -(-a.size // 4) * 4
+        staging = np.zeros(max(total, 4), dtype=np.int32)
+        for a, s0 in zip(arrs, starts):
+            staging[s0:s0 + a.size] = a.ravel()
+        self._pinned = torch.from_numpy(staging).pin_memory()
+        dbuf = self._pinned.to(dev, non_blocking=True)
+        d = [dbuf[s0:s0 + a.size].view(a.shape) for a, s0 in zip(arrs, starts)]
         nf = len(fwd)
         self.fwd_sched, self.bwd_sched = tuple(d[:nf]), tuple(d[nf:])
         self.n_fwd_tiles, self.n_bwd_tiles = fwd[1].shape[0], bwd[1].shape[0]
