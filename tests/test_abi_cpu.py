@@ -125,6 +125,22 @@ def test_c_scheduler_matches_oracle_bcast(L):
     assert sp.tolist() == rp and [tuple(t) for t in tl.tolist()] == rt
 
 
+def test_c_scheduler_matches_oracle_on_both_sort_paths(L):
+    # The deal's stable sort by work is a counting sort while the works stay
+    # below 2^20 tokens and a merge sort beyond; a batch with a few
+    # sequences of millions of tokens takes the second path, and many equal
+    # works check that ties keep their enumeration order on both.
+    rng = np.random.default_rng(21)
+    lengths = [int(x) for x in rng.integers(1, 3000, 200)] + [1 << 21, 3 << 20, 1 << 21, 700]
+    lengths += [512] * 40
+    for sms in (152, 13):
+        for lens in (lengths, lengths[:200] + lengths[-41:]):
+            sp, tl = jfa.schedule(W.offsets_of(lens), 2, 256, sms)
+            rp, rt = S.schedule(list(lens), 2, 256, sms)
+            assert sp.tolist() == rp
+            assert [tuple(t) for t in tl.tolist()] == rt
+
+
 def test_c_scheduler_int32_offsets_and_empty(L):
     off = np.array([0, 0, 3, 3, 200], dtype=np.int32)
     sp, tl = jfa.schedule(off, 2, 64, 5)
