@@ -21,17 +21,19 @@
 // 4-7 softmax + epilogue (one query row per thread). Two TMEM slots of
 // (S 128 columns, O D columns), two (Q, K, V) shared-memory stages.
 //
-// Backward roles: same split. Per unit: dP = dO V^T and S = Q K^T (query
-// rows on TMEM lanes); the compute warps form P, Di, dS and write P and dS as
+// Backward roles: warp 0 TMA producer, warp 1 MMA, warp 2 TMEM owner, warps
+// 4-7 P and dS, warps 8-11 epilogue. Per unit: dP = dO V^T and S = Q K^T
+// (query rows on TMEM lanes); warps 4-7 form P, Di, dS and write P and dS as
 // bf16 [query][key] tiles to shared memory; then dV = P^T dO, dK = dS^T Q
 // (P^T, dS^T read MN-major) and dQ = dS K (dS read K-major) are fresh
-// products in TMEM. Input tiles go through a 5-slot ring loaded in the order
-// they are released (V after dP, dO after dV, Q after dK, K after dQ), so
-// the next unit's loads start while this unit computes. The epilogue drains
-// dK, dV and dQ in that order and releases each TMEM region as soon as it is
-// read, so the next unit's dP and S products overlap the rest of the stores
-// (each 128-byte piece of a row stored by four lanes after a shuffle
-// transpose, eight whole lines per store instruction).
+// products in TMEM. Input tiles go through a ring loaded in the order they
+// are released (V after dP, dO after dV, Q after dK, K after dQ), so the
+// next unit's loads start while this unit computes. Warps 8-11 drain dK, dV
+// and dQ in that order and release each TMEM region as soon as it is read,
+// so the next unit's dP and S products, and its P and dS on warps 4-7,
+// overlap the rest of the stores (each 128-byte piece of a row stored by
+// four lanes after a shuffle transpose, eight whole lines per store
+// instruction).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -411,7 +413,7 @@ struct BBars {
 };
 
 template <int D, bool ROPE>
-__global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_constant__ BlockdiagParams p) {
+__global__ void __launch_bounds__(384, 1) blockdiag_bwd_kernel(const __grid_constant__ BlockdiagParams p) {
   using C = BCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -455,118 +457,127 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
   const WaitCtl ctl{p.status, &bars.abort_flag, p.timeout_ns};
   const int n_units = (int)((p.rows + 127) / 128) * p.H;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      ArmedLoads armed;  // barrier s = full[s]
-      uint32_t eph = 0;
-      int slot = 0;
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit x = unit_of(u, p.H, p.rows);
-        for (int t = 0; t < 4; ++t) {
-          if (!mbar_wait(&bars.empty[slot], bit(eph, slot) ^ 1, ctl, 1)) goto drain;
-          eph ^= 1u << (slot);
-          uint64_t *fb = &bars.full[slot];
-          mbar_arrive_expect_tx(fb, C::TILE);
-          armed.arm(slot);
-          const CUtensorMap *m = t == T_V ? &p.tm_v : t == T_DO ? &p.tm_do : t == T_Q ? &p.tm_q : &p.tm_k;
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(smem + C::OFF_RING + slot * C::TILE + c * 16384, m, fb, c * 64, x.h, x.row0);
-          if (++slot == C::NSLOT) slot = 0;
+  // Register budgets at D = 64, where the P/dS warps' arrays need more than
+  // the 168 a 384-thread block gets (104 + 232 + 168 per warpgroup = 3 x 168
+  // x 128 threads: warps 0-3, the P/dS warps, the epilogue warps); at
+  // D = 128 the even split measured faster.
+  if (warp < 4) {
+    if constexpr (D == 64) regs_lower<104>();
+    if (warp == 0) {
+      if (lane == 0) {
+        ArmedLoads armed;  // barrier s = full[s]
+        uint32_t eph = 0;
+        int slot = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+          const Unit x = unit_of(u, p.H, p.rows);
+          for (int t = 0; t < 4; ++t) {
+            if (!mbar_wait(&bars.empty[slot], bit(eph, slot) ^ 1, ctl, 1)) goto drain;
+            eph ^= 1u << (slot);
+            uint64_t *fb = &bars.full[slot];
+            mbar_arrive_expect_tx(fb, C::TILE);
+            armed.arm(slot);
+            const CUtensorMap *m = t == T_V ? &p.tm_v : t == T_DO ? &p.tm_do : t == T_Q ? &p.tm_q : &p.tm_k;
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(smem + C::OFF_RING + slot * C::TILE + c * 16384, m, fb, c * 64, x.h, x.row0);
+            if (++slot == C::NSLOT) slot = 0;
+          }
+        }
+      drain:  // every armed copy has landed before the CTA can exit
+        armed.drain([&](int i) { return &bars.full[i]; }, p.timeout_ns);
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        uint32_t fph = 0, psr = 0, psf = 0, kf = 0, vf = 0, qf = 0;
+        const uint32_t ring = smem_u32(smem + C::OFF_RING);
+        const uint32_t pa = smem_u32(smem + C::OFF_P), dsa = smem_u32(smem + C::OFF_DS);
+        int slot = 0;
+        auto sl = [&](int t) { int s = slot + t; return s >= C::NSLOT ? s - C::NSLOT : s; };
+        auto wait_full = [&](int t) -> bool {
+          const int s = sl(t);
+          if (!mbar_wait(&bars.full[s], bit(fph, s), ctl, 10 + t)) return false;
+          fph ^= 1u << (s);
+          return true;
+        };
+        const uint64_t ring_kmaj = sdesc_sw128(ring, 16, 1024);  // k-steps add offset >> 4
+        const uint64_t ring_mn = sdesc_sw128(ring, 16384, 1024);
+        const uint64_t p_mn = sdesc_sw128(pa, 16384, 1024);
+        const uint64_t ds_mn = sdesc_sw128(dsa, 16384, 1024);
+        const uint64_t ds_kmaj = sdesc_sw128(dsa, 16, 1024);
+        auto tk = [&](int t) { return ring_kmaj + ((uint32_t)(sl(t) * C::TILE) >> 4); };
+        auto tm = [&](int t) { return ring_mn + ((uint32_t)(sl(t) * C::TILE) >> 4); };
+        auto xyT = [&](uint32_t dcol, uint64_t xd, uint64_t yd) {
+  #pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+            mma_ss(tmem + dcol, xd + off, yd + off, C::IDESC_S, k > 0);
+          }
+        };
+        for (int u = blockIdx.x, n = 0; u < n_units; u += gridDim.x, ++n) {
+          const int sb = n & 1;
+          const uint32_t sreg = sb ? BC_S2 : BC_S;
+          // Each product region is reused as soon as the previous unit's epilogue
+          // has drained it (dK, then dV, then dQ), so this unit's dP and S run
+          // while the rest of the previous epilogue is still being written.
+          if (!mbar_wait(&bars.dk_free, kf ^ 1, ctl, 20)) goto done;
+          kf ^= 1;
+          if (!wait_full(T_V) || !wait_full(T_DO)) goto done;
+          tc_fence_after();
+          xyT(BC_DP, tk(T_DO), tk(T_V));  // dP = dO V^T
+          mma_commit(&bars.dp_full);
+          mma_commit(&bars.empty[sl(T_V)]);
+          if (!mbar_wait(&bars.dv_free[sb], bit(vf, sb) ^ 1, ctl, 22)) goto done;
+          vf ^= 1u << sb;
+          if (!wait_full(T_Q) || !wait_full(T_K)) goto done;
+          tc_fence_after();
+          xyT(sreg, tk(T_Q), tk(T_K));  // S = Q K^T
+          mma_commit(&bars.s_full);
+          if (!mbar_wait(&bars.ps_ready, psr, ctl, 21)) goto done;
+          psr ^= 1;
+          tc_fence_after();
+          // dV = P^T dO  (A = P^T: MN-major view of the [q][k] tile; B = dO MN-major)
+          {
+            const uint64_t bd = tm(T_DO);
+  #pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ss(tmem + sreg, p_mn + (k * 2048 >> 4), bd + (k * 2048 >> 4), C::IDESC_T, k > 0);
+          }
+          mma_commit(&bars.empty[sl(T_DO)]);
+          // dK = dS^T Q
+          {
+            const uint64_t bd = tm(T_Q);
+  #pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ss(tmem + BC_DP, ds_mn + (k * 2048 >> 4), bd + (k * 2048 >> 4), C::IDESC_T, k > 0);
+          }
+          mma_commit(&bars.empty[sl(T_Q)]);
+          if (!mbar_wait(&bars.dq_free, qf ^ 1, ctl, 23)) goto done;
+          qf ^= 1;
+          tc_fence_after();
+          // dQ = dS K  (A = dS K-major; B = K MN-major)
+          {
+            const uint64_t bd = tm(T_K);
+  #pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ss(tmem + BC_DQ, ds_kmaj + (((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                     bd + (k * 2048 >> 4), C::IDESC_Q, k > 0);
+          }
+          mma_commit(&bars.empty[sl(T_K)]);
+          mma_commit(&bars.g_full);
+          mma_commit(&bars.ps_free);
+          slot = sl(4);
+          (void)psf;
         }
       }
-    drain:  // every armed copy has landed before the CTA can exit
-      armed.drain([&](int i) { return &bars.full[i]; }, p.timeout_ns);
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      uint32_t fph = 0, psr = 0, psf = 0, kf = 0, vf = 0, qf = 0;
-      const uint32_t ring = smem_u32(smem + C::OFF_RING);
-      const uint32_t pa = smem_u32(smem + C::OFF_P), dsa = smem_u32(smem + C::OFF_DS);
-      int slot = 0;
-      auto sl = [&](int t) { int s = slot + t; return s >= C::NSLOT ? s - C::NSLOT : s; };
-      auto wait_full = [&](int t) -> bool {
-        const int s = sl(t);
-        if (!mbar_wait(&bars.full[s], bit(fph, s), ctl, 10 + t)) return false;
-        fph ^= 1u << (s);
-        return true;
-      };
-      const uint64_t ring_kmaj = sdesc_sw128(ring, 16, 1024);  // k-steps add offset >> 4
-      const uint64_t ring_mn = sdesc_sw128(ring, 16384, 1024);
-      const uint64_t p_mn = sdesc_sw128(pa, 16384, 1024);
-      const uint64_t ds_mn = sdesc_sw128(dsa, 16384, 1024);
-      const uint64_t ds_kmaj = sdesc_sw128(dsa, 16, 1024);
-      auto tk = [&](int t) { return ring_kmaj + ((uint32_t)(sl(t) * C::TILE) >> 4); };
-      auto tm = [&](int t) { return ring_mn + ((uint32_t)(sl(t) * C::TILE) >> 4); };
-      auto xyT = [&](uint32_t dcol, uint64_t xd, uint64_t yd) {
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-          mma_ss(tmem + dcol, xd + off, yd + off, C::IDESC_S, k > 0);
-        }
-      };
-      for (int u = blockIdx.x, n = 0; u < n_units; u += gridDim.x, ++n) {
-        const int sb = n & 1;
-        const uint32_t sreg = sb ? BC_S2 : BC_S;
-        // Each product region is reused as soon as the previous unit's epilogue
-        // has drained it (dK, then dV, then dQ), so this unit's dP and S run
-        // while the rest of the previous epilogue is still being written.
-        if (!mbar_wait(&bars.dk_free, kf ^ 1, ctl, 20)) goto done;
-        kf ^= 1;
-        if (!wait_full(T_V) || !wait_full(T_DO)) goto done;
-        tc_fence_after();
-        xyT(BC_DP, tk(T_DO), tk(T_V));  // dP = dO V^T
-        mma_commit(&bars.dp_full);
-        mma_commit(&bars.empty[sl(T_V)]);
-        if (!mbar_wait(&bars.dv_free[sb], bit(vf, sb) ^ 1, ctl, 22)) goto done;
-        vf ^= 1u << sb;
-        if (!wait_full(T_Q) || !wait_full(T_K)) goto done;
-        tc_fence_after();
-        xyT(sreg, tk(T_Q), tk(T_K));  // S = Q K^T
-        mma_commit(&bars.s_full);
-        if (!mbar_wait(&bars.ps_ready, psr, ctl, 21)) goto done;
-        psr ^= 1;
-        tc_fence_after();
-        // dV = P^T dO  (A = P^T: MN-major view of the [q][k] tile; B = dO MN-major)
-        {
-          const uint64_t bd = tm(T_DO);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + sreg, p_mn + (k * 2048 >> 4), bd + (k * 2048 >> 4), C::IDESC_T, k > 0);
-        }
-        mma_commit(&bars.empty[sl(T_DO)]);
-        // dK = dS^T Q
-        {
-          const uint64_t bd = tm(T_Q);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + BC_DP, ds_mn + (k * 2048 >> 4), bd + (k * 2048 >> 4), C::IDESC_T, k > 0);
-        }
-        mma_commit(&bars.empty[sl(T_Q)]);
-        if (!mbar_wait(&bars.dq_free, qf ^ 1, ctl, 23)) goto done;
-        qf ^= 1;
-        tc_fence_after();
-        // dQ = dS K  (A = dS K-major; B = K MN-major)
-        {
-          const uint64_t bd = tm(T_K);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + BC_DQ, ds_kmaj + (((k >> 2) * 16384 + (k & 3) * 32) >> 4),
-                   bd + (k * 2048 >> 4), C::IDESC_Q, k > 0);
-        }
-        mma_commit(&bars.empty[sl(T_K)]);
-        mma_commit(&bars.g_full);
-        mma_commit(&bars.ps_free);
-        slot = sl(4);
-        (void)psf;
-      }
-    }
-  } else if (warp >= 4) {
+  } else if (warp < 8) {
+    if constexpr (D == 64) regs_raise<232>();
+    // ------------------------------------------------------- P and dS
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const int blk = wq >> 1;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float sl2 = p.scale_log2;
-    uint32_t sph = 0, dpph = 0, psf = 0, gph = 0;
+    uint32_t sph = 0, dpph = 0, psf = 0;
     uint8_t *prow = smem + C::OFF_P + blk * 16384 + r * 128;
     uint8_t *dsrow = smem + C::OFF_DS + blk * 16384 + r * 128;
     for (int u = blockIdx.x, n = 0; u < n_units; u += gridDim.x, ++n) {
@@ -652,6 +663,19 @@ __global__ void __launch_bounds__(256, 1) blockdiag_bwd_kernel(const __grid_cons
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.ps_ready);
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------- epilogue
+    // Warps 8-11 drain a unit's dK, dV and dQ (one row per thread, TMEM lane
+    // quarter warp % 4) while warps 4-7 already form the next unit's P and dS.
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    uint32_t gph = 0;
+    for (int u = blockIdx.x, n = 0; u < n_units; u += gridDim.x, ++n) {
+      const Unit x = unit_of(u, p.H, p.rows);
+      const int sb = n & 1;
+      const uint32_t sreg = sb ? BC_S2 : BC_S;
       // Rotary: this row's table values in 16-pair pieces (dK and dQ rows r
       // are at the same position and share them); the first two pieces load
       // while the products run, each later one two pieces ahead of its use.
@@ -784,10 +808,10 @@ cudaError_t launch_blockdiag_fwd(const BlockdiagParams &p, int D, int num_sms, c
 cudaError_t launch_blockdiag_bwd(const BlockdiagParams &p, int D, int num_sms, cudaStream_t st) {
   const bool rope = p.cos_t != nullptr;
   if (D == 128)
-    return rope ? launch_k(blockdiag_bwd_kernel<128, true>, BCfg<128>::SMEM, p, num_sms, st)
-                : launch_k(blockdiag_bwd_kernel<128, false>, BCfg<128>::SMEM, p, num_sms, st);
-  return rope ? launch_k(blockdiag_bwd_kernel<64, true>, BCfg<64>::SMEM, p, num_sms, st)
-              : launch_k(blockdiag_bwd_kernel<64, false>, BCfg<64>::SMEM, p, num_sms, st);
+    return rope ? launch_k(blockdiag_bwd_kernel<128, true>, BCfg<128>::SMEM, p, num_sms, st, 384)
+                : launch_k(blockdiag_bwd_kernel<128, false>, BCfg<128>::SMEM, p, num_sms, st, 384);
+  return rope ? launch_k(blockdiag_bwd_kernel<64, true>, BCfg<64>::SMEM, p, num_sms, st, 384)
+              : launch_k(blockdiag_bwd_kernel<64, false>, BCfg<64>::SMEM, p, num_sms, st, 384);
 }
 
 }  // namespace jfa

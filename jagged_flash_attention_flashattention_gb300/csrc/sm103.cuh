@@ -24,6 +24,19 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// Per-warpgroup register budgets: every warp of a warpgroup runs the same
+// instruction. Raising waits until other warpgroups have given registers
+// back, so the budgets of all warpgroups must sum to at most the block's
+// launch allocation (threads x registers per thread at launch).
+template <uint32_t N>
+__device__ __forceinline__ void regs_raise() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_lower() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
